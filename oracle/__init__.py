@@ -1,0 +1,213 @@
+"""Oracle for the speculative-decoding verify-and-sample step.
+
+TEST INFRASTRUCTURE ONLY: only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product (``speculative_decoding_verification_22_gb300``) never imports it,
+and this package never imports the product.
+
+The arithmetic lives in ``sv_oracle.c`` (plain C, fp64, one thread; built
+with ``-O2 -ffp-contract=off`` and no fast-math).  This module only marshals
+numpy arrays into it, plus two closed forms from the pages:
+
+* ``expected_tokens(alpha, K)`` -- "Speculative Decoding: Two Models, One
+  Voice", "How much faster" and Tool 2: with i.i.d. acceptance alpha, a round
+  emits (1 - alpha^(K+1)) / (1 - alpha) tokens on average.
+* ``expected_tokens_positions(alphas)`` -- "Speculative Decoding: The Algebra
+  and the Proof", "The algebra": with conditional acceptance alpha_j at
+  position j, E = 1 + sum_i prod_{j<=i} alpha_j.
+
+Every C function is described (with its source passages) in ``sv_oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sv_oracle.c")
+_LIB = os.path.join(_HERE, "libsv_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, EARG, ETOKEN, ENOMEM = 0, -1, -2, -3
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/libsv_oracle.so`` (gcc, fp64, no
+    fast-math, no FMA contraction so x86 and Arm round identically)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            i64, i32, vp, dbl = (ctypes.c_int64, ctypes.c_int32,
+                                 ctypes.c_void_p, ctypes.c_double)
+            lib.sv_oracle_logits.argtypes = [i64, i64, i64, i32, vp, vp, i64,
+                                             i64, vp]
+            lib.sv_oracle_logits.restype = ctypes.c_int
+            lib.sv_oracle_lse.argtypes = [i64, vp, dbl]
+            lib.sv_oracle_lse.restype = dbl
+            lib.sv_oracle_softmax.argtypes = [i64, vp, dbl, vp]
+            lib.sv_oracle_softmax.restype = None
+            lib.sv_oracle_verify.argtypes = [i64, i64, i32, i32, i32, vp, vp,
+                                             vp, vp, vp, dbl, vp, vp, vp, vp,
+                                             vp, vp]
+            lib.sv_oracle_verify.restype = ctypes.c_int
+            lib.sv_oracle_rule_batch.argtypes = [i64, i32, vp, vp, i64, vp,
+                                                 vp, vp, vp, vp]
+            lib.sv_oracle_rule_batch.restype = ctypes.c_int
+            lib.sv_oracle_emitted_law.argtypes = [i64, vp, vp, vp]
+            lib.sv_oracle_emitted_law.restype = dbl
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _matrix(a):
+    """bf16 matrices travel as their uint16 bit patterns (dtype code 0);
+    fp32 as float32 (code 1)."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return a, 0
+    if a.dtype == np.float32:
+        return a, 1
+    raise TypeError("matrices must be uint16 (bf16 bits) or float32")
+
+
+def logits(H, W, v0: int = 0, v1: int | None = None) -> np.ndarray:
+    """fp64 logits H @ W[v0:v1].T, summed in k order (LM-head contraction)."""
+    H, dt = _matrix(H)
+    W, dt2 = _matrix(W)
+    if dt != dt2:
+        raise TypeError("H and W must share a dtype")
+    R, d = H.shape
+    V, d2 = W.shape
+    if d != d2:
+        raise ValueError("hidden size mismatch")
+    v1 = V if v1 is None else v1
+    out = np.empty((R, v1 - v0), dtype=np.float64)
+    rc = _load().sv_oracle_logits(V, d, R, dt, _ptr(H), _ptr(W), v0, v1,
+                                  _ptr(out))
+    if rc != OK:
+        raise ValueError(f"sv_oracle_logits failed ({rc})")
+    return out
+
+
+def lse(x, T: float = 1.0) -> float:
+    """log-sum-exp of x / T (temperature softmax normaliser)."""
+    x = _c(x, np.float64)
+    return float(_load().sv_oracle_lse(x.size, _ptr(x), float(T)))
+
+
+def softmax(x, T: float = 1.0) -> np.ndarray:
+    """softmax(x / T) in fp64."""
+    x = _c(x, np.float64)
+    out = np.empty_like(x)
+    _load().sv_oracle_softmax(x.size, _ptr(x), float(T), _ptr(out))
+    return out
+
+
+def verify(hidden, W, draft, q_logits, uniforms, temperature: float,
+           want_logits: bool = False) -> dict:
+    """The whole verify-and-sample step for B sequences.
+
+    hidden [B, K+1, d] and W [V, d] as uint16 (bf16 bits) or float32;
+    draft [B, K] int32; q_logits [B, K, V] float32; uniforms [B, K+1] float32.
+    Returns tokens [B, K+1], n_accepted [B], dist [B], lse_p, lse_q, status
+    and (optionally) fp64 logits [B*(K+1), V].
+    """
+    hidden, dt = _matrix(hidden)
+    W, dt2 = _matrix(W)
+    if dt != dt2:
+        raise TypeError("hidden and W must share a dtype")
+    B, rows, d = hidden.shape
+    K = rows - 1
+    V = W.shape[0]
+    draft = _c(draft, np.int32).reshape(B, K)
+    T = float(temperature)
+    q = None if (T == 0.0 or K == 0) else _c(q_logits, np.float32).reshape(B, K, V)
+    u = None if T == 0.0 else _c(uniforms, np.float32).reshape(B, rows)
+    tokens = np.empty((B, rows), dtype=np.int32)
+    n_acc = np.empty((B,), dtype=np.int32)
+    dist = np.empty((B,), dtype=np.float64)
+    lg = np.empty((B * rows, V), dtype=np.float64) if want_logits else None
+    lse_p = np.full((B * rows,), np.nan)
+    lse_q = np.full((max(B * K, 1),), np.nan)
+    rc = _load().sv_oracle_verify(V, d, B, K, dt, _ptr(hidden), _ptr(W),
+                                  _ptr(draft), _ptr(q), _ptr(u), T,
+                                  _ptr(tokens), _ptr(n_acc), _ptr(dist),
+                                  _ptr(lg), _ptr(lse_p), _ptr(lse_q))
+    if rc not in (OK, ETOKEN):
+        raise ValueError(f"sv_oracle_verify failed ({rc})")
+    return {"tokens": tokens, "n_accepted": n_acc, "dist": dist,
+            "logits": lg, "lse_p": lse_p, "lse_q": lse_q[:B * K], "status": rc}
+
+
+def rule_batch(p, q, x, u):
+    """The accept / residual / bonus rule for n independent rounds that
+    share p [K+1, V] and q [K, V] (probabilities); x [n, K], u [n, K+1]."""
+    p = _c(p, np.float64)
+    K1, V = p.shape
+    K = K1 - 1
+    q = _c(q, np.float64).reshape(K, V) if K > 0 else np.zeros((1, V))
+    x = _c(x, np.int32).reshape(-1, K) if K > 0 else np.zeros((len(u), 1), np.int32)
+    u = _c(u, np.float64).reshape(-1, K1)
+    n = u.shape[0]
+    tokens = np.empty((n, K1), dtype=np.int32)
+    n_acc = np.empty((n,), dtype=np.int32)
+    dist = np.empty((n,), dtype=np.float64)
+    rc = _load().sv_oracle_rule_batch(V, K, _ptr(p), _ptr(q), n, _ptr(x),
+                                      _ptr(u), _ptr(tokens), _ptr(n_acc),
+                                      _ptr(dist))
+    if rc not in (OK, ETOKEN):
+        raise ValueError(f"sv_oracle_rule_batch failed ({rc})")
+    return tokens, n_acc, dist
+
+
+def emitted_law(p, q):
+    """Exact law of the token emitted at one draft position and the
+    acceptance mass alpha = sum min(p, q)."""
+    p = _c(p, np.float64)
+    q = _c(q, np.float64)
+    law = np.empty_like(p)
+    alpha = _load().sv_oracle_emitted_law(p.size, _ptr(p), _ptr(q), _ptr(law))
+    return law, float(alpha)
+
+
+def expected_tokens(alpha: float, K: int) -> float:
+    """(1 - alpha^(K+1)) / (1 - alpha); K + 1 at alpha == 1."""
+    if alpha == 1.0:
+        return float(K + 1)
+    return (1.0 - alpha ** (K + 1)) / (1.0 - alpha)
+
+
+def expected_tokens_positions(alphas) -> float:
+    """1 + sum_{i=1..K} prod_{j<=i} alpha_j (conditional acceptances)."""
+    total, prod = 1.0, 1.0
+    for a in alphas:
+        prod *= float(a)
+        total += prod
+    return total

@@ -1,0 +1,424 @@
+/*
+ * sv_oracle.c -- plain, slow, single-threaded fp64 CPU oracle for the
+ * target-side verify-and-sample step of speculative decoding.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: it exists so that tests, the smoke check and the CPU
+ * baseline of the benchmark can check the CUDA path against an independent
+ * restatement of the method.  It shares no code, header or constant with the
+ * CUDA library.
+ *
+ * Sources (page title, section):
+ *   [P1] "Speculative Decoding: Two Models, One Voice" -- "The idea" (draft,
+ *        verify, accept-or-fix), "The rule that makes it exact" (accept with
+ *        min(1, p/q), residual norm(max(0, p - q)), greedy corollary),
+ *        "Checking the math honestly" (the spec_round simulation).
+ *   [P2] "What Actually Happens During Speculative Decoding in LLMs" --
+ *        the speculative_sample_step reference function (K+1 target
+ *        distributions, zero-residual fallback to p).
+ *   [P3] "Speculative Decoding: Guess Several Tokens, Check Them in One
+ *        Pass" -- Step 2 (greedy verify_greedy), Step 3 (speculative
+ *        sampling, three-token example).
+ *   [P4] "Speculative Decoding: The Algebra and the Proof" -- "The proof"
+ *        (exact emitted law, identical-draft edge case), "Where it breaks"
+ *        (use the actual, normalised sampling distributions).
+ *   [P5] "Speculative Decoding" (library wiki) -- "One speculation round"
+ *        (strict r < min(1, p/q) test, bonus from p at position gamma+1).
+ *
+ * Readings where the pages leave a step open (each is listed in the design doc):
+ *   R1  p_i = softmax(L_i / T) and q_i = softmax(q_logits_i / T) with the
+ *       same temperature T for both ([P1] "three remarks", [P3] Step 3,
+ *       [P4] "Where it breaks").
+ *   R2  The accept test is the strict u < p/q of [P1], [P3] and [P5]; the
+ *       "+1e-10" guard and "<=" of [P2] are not used.  If q(x) == 0 the test
+ *       accepts iff p(x) > 0 (t = +inf); if both are 0 it rejects.
+ *   R3  One uniform per draft position (u[0..K-1]) and ONE final uniform
+ *       u[K] that drives whichever final draw happens (residual or bonus).
+ *   R4  Every categorical draw is an inverse CDF in token-id order: emit
+ *       the smallest v with u * S < C_v, C_v the inclusive prefix sum of the
+ *       unnormalised weights and S their total.  If rounding leaves no v,
+ *       take the largest v with positive weight.
+ *   R5  If the residual has zero total mass (p == q on that row), draw from
+ *       p_j instead ([P2] fallback; [P4] flags the division by zero).
+ *   R6  T == 0 is greedy: a_i = argmax_v L_i(v), ties to the smallest index;
+ *       accept while x_i == a_i, emit a_i at the first mismatch, else emit
+ *       the bonus a_{K+1} ([P1] first remark, [P3] Step 2).
+ *   R7  Token ids outside [0, V) make that sequence's result invalid: its
+ *       outputs are -1 and the function reports it.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define SV_ORACLE_OK 0
+#define SV_ORACLE_EARG (-1)
+#define SV_ORACLE_ETOKEN (-2)
+#define SV_ORACLE_ENOMEM (-3)
+
+/* A bf16 value is the top 16 bits of an IEEE binary32; widening is exact. */
+static double bf16_bits_to_double(uint16_t bits) {
+  uint32_t w = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
+/* Widen row `row` of a [rows, d] matrix stored as bf16 (dtype 0) or fp32
+ * (dtype 1) into `out` (d doubles).  Both widenings are exact. */
+static void widen_row(const void *base, int dtype, int64_t d, int64_t row,
+                      double *out) {
+  if (dtype == 0) {
+    const uint16_t *p = (const uint16_t *)base + row * d;
+    for (int64_t k = 0; k < d; ++k) out[k] = bf16_bits_to_double(p[k]);
+  } else {
+    const float *p = (const float *)base + row * d;
+    for (int64_t k = 0; k < d; ++k) out[k] = (double)p[k];
+  }
+}
+
+/* ------------------------------------------------------------------------
+ * Step 1 -- LM-head contraction ([P2] memory-bound section: the verify pass
+ * multiplies the [positions x d] hidden block against the LM-head weights):
+ *     L[r][v] = sum_{k=0}^{d-1} H[r][k] * W[v][k]
+ * summed in fp64 in the order k = 0, 1, ..., d-1.  A product of two bf16
+ * values is exact in fp64, and so is a product of two fp32 values, so the
+ * only rounding is in the running sum.
+ * Computes the columns v in [v0, v1) into L[r * (v1 - v0) + (v - v0)].
+ * ---------------------------------------------------------------------- */
+int sv_oracle_logits(int64_t V, int64_t d, int64_t R, int32_t dtype,
+                     const void *H, const void *W, int64_t v0, int64_t v1,
+                     double *L) {
+  if (V < 1 || d < 1 || R < 1 || (dtype != 0 && dtype != 1) || !H || !W ||
+      !L || v0 < 0 || v1 > V || v0 > v1)
+    return SV_ORACLE_EARG;
+  double *h = (double *)malloc(sizeof(double) * (size_t)(R * d));
+  double *w = (double *)malloc(sizeof(double) * (size_t)d);
+  double *acc = (double *)malloc(sizeof(double) * (size_t)R);
+  if (!h || !w || !acc) {
+    free(h); free(w); free(acc);
+    return SV_ORACLE_ENOMEM;
+  }
+  for (int64_t r = 0; r < R; ++r) widen_row(H, dtype, d, r, h + r * d);
+  const int64_t nv = v1 - v0;
+  for (int64_t v = v0; v < v1; ++v) {
+    widen_row(W, dtype, d, v, w);
+    for (int64_t r = 0; r < R; ++r) acc[r] = 0.0;
+    /* Each row keeps its own running sum in k order; the rows are
+     * independent, so visiting them inside the k loop changes no sum. */
+    for (int64_t k = 0; k < d; ++k) {
+      const double wk = w[k];
+      for (int64_t r = 0; r < R; ++r) acc[r] += h[r * d + k] * wk;
+    }
+    for (int64_t r = 0; r < R; ++r) L[r * nv + (v - v0)] = acc[r];
+  }
+  free(h); free(w); free(acc);
+  return SV_ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * Step 2 -- temperature softmax (reading R1):
+ *     LSE = m + log(sum_v exp(x_v / T - m)),  m = max_v x_v / T,
+ *     p(v) = exp(x_v / T - LSE).
+ * ---------------------------------------------------------------------- */
+double sv_oracle_lse(int64_t V, const double *x, double T) {
+  double m = -INFINITY;
+  for (int64_t v = 0; v < V; ++v) {
+    const double a = x[v] / T;
+    if (a > m) m = a;
+  }
+  if (!(m > -INFINITY) || m != m || m == INFINITY) return m;
+  double s = 0.0;
+  for (int64_t v = 0; v < V; ++v) s += exp(x[v] / T - m);
+  return m + log(s);
+}
+
+void sv_oracle_softmax(int64_t V, const double *x, double T, double *p) {
+  const double lse = sv_oracle_lse(V, x, T);
+  for (int64_t v = 0; v < V; ++v) p[v] = exp(x[v] / T - lse);
+}
+
+/* ------------------------------------------------------------------------
+ * Inverse-CDF draw (reading R4) over unnormalised weights w[0..V-1] >= 0
+ * with total S > 0.  Returns the chosen token; *dist receives the distance
+ * of u from the nearer edge of the chosen token's CDF interval, measured in
+ * u units: min(|u - C_{v-1}/S|, |u - C_v/S|).
+ * ---------------------------------------------------------------------- */
+static int32_t inverse_cdf(int64_t V, const double *w, double S, double u,
+                           double *dist) {
+  const double target = u * S;
+  double c_prev = 0.0, c = 0.0;
+  int64_t last_pos = -1;
+  for (int64_t v = 0; v < V; ++v) {
+    c_prev = c;
+    c += w[v];
+    if (w[v] > 0.0) last_pos = v;
+    if (target < c) {
+      const double d0 = fabs(u - c_prev / S), d1 = fabs(u - c / S);
+      *dist = d0 < d1 ? d0 : d1;
+      return (int32_t)v;
+    }
+  }
+  /* Rounding left no qualifying v: the upper edge of the last positive
+   * interval is within rounding of u. */
+  *dist = 0.0;
+  return (int32_t)last_pos;
+}
+
+/* ------------------------------------------------------------------------
+ * Steps 3-5 -- the accept / residual / bonus rule for ONE sequence, given
+ * its K+1 target distributions p[i][v] (i = 0..K; row i scores draft
+ * position i+1, row K is position K+1) and K draft distributions q[i][v].
+ * Walk the draft left to right ([P1] "The idea" step 3; [P5] steps 3-5):
+ *   accept x_{i+1} iff u[i] < t_i,  t_i = p_i(x) / q_i(x)     (R2)
+ *   at the first rejection (row j): draw from max(0, p_j - q_j) (R4, R5)
+ *   if all K survive: draw the bonus from p_K                  (R3, R4)
+ * Writes tokens[0..K] (accepted prefix, final token, then -1) and returns
+ * the number of accepted draft tokens, or SV_ORACLE_ETOKEN.
+ * *dist = the smallest distance between a uniform and the threshold of a
+ * decision this round actually took (accept tests use |u - t|, the final
+ * draw its inverse-CDF interval edges).
+ * `scratch` must hold V doubles.
+ * ---------------------------------------------------------------------- */
+static int32_t rule_one_sequence(int64_t V, int32_t K, const double *p,
+                                 const double *q, const int32_t *x,
+                                 const double *u, int32_t *tokens,
+                                 double *dist, double *scratch) {
+  double best = INFINITY;
+  for (int32_t i = 0; i <= K; ++i) tokens[i] = -1;
+  for (int32_t i = 0; i < K; ++i)
+    if (x[i] < 0 || (int64_t)x[i] >= V) {
+      *dist = INFINITY;
+      return SV_ORACLE_ETOKEN;
+    }
+  int32_t j = K; /* row of the final draw */
+  int residual = 0;
+  for (int32_t i = 0; i < K; ++i) {
+    const double px = p[(int64_t)i * V + x[i]];
+    const double qx = q[(int64_t)i * V + x[i]];
+    int accept;
+    double t;
+    if (qx > 0.0) {
+      t = px / qx;
+      accept = u[i] < t;
+    } else {
+      t = px > 0.0 ? INFINITY : 0.0;
+      accept = px > 0.0;
+    }
+    const double dd = fabs(u[i] - t);
+    if (dd < best) best = dd;
+    if (accept) {
+      tokens[i] = x[i];
+    } else {
+      j = i;
+      residual = 1;
+      break;
+    }
+  }
+  const double uf = u[K];
+  const double *pj = p + (int64_t)j * V;
+  double S = 0.0;
+  int32_t tok;
+  double dfinal;
+  if (residual) {
+    const double *qj = q + (int64_t)j * V;
+    for (int64_t v = 0; v < V; ++v) {
+      const double r = pj[v] - qj[v];
+      scratch[v] = r > 0.0 ? r : 0.0;
+      S += scratch[v];
+    }
+  }
+  if (!residual || !(S > 0.0)) {
+    /* bonus draw from p_K, or the zero-residual fallback to p_j (R5) */
+    S = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+      scratch[v] = pj[v];
+      S += pj[v];
+    }
+  }
+  tok = inverse_cdf(V, scratch, S, uf, &dfinal);
+  if (dfinal < best) best = dfinal;
+  tokens[j] = tok;
+  *dist = best;
+  return j;
+}
+
+/* ------------------------------------------------------------------------
+ * Greedy rule (reading R6) for one sequence given its K+1 logit rows.
+ * *gap = the smallest (top1 - top2) logit gap over the rows whose argmax
+ * decided something this round.
+ * ---------------------------------------------------------------------- */
+static int32_t greedy_one_sequence(int64_t V, int32_t K, const double *L,
+                                   const int32_t *x, int32_t *tokens,
+                                   double *gap) {
+  double best = INFINITY;
+  for (int32_t i = 0; i <= K; ++i) tokens[i] = -1;
+  for (int32_t i = 0; i < K; ++i)
+    if (x[i] < 0 || (int64_t)x[i] >= V) {
+      *gap = INFINITY;
+      return SV_ORACLE_ETOKEN;
+    }
+  for (int32_t i = 0; i <= K; ++i) {
+    const double *row = L + (int64_t)i * V;
+    int64_t a = 0;
+    for (int64_t v = 1; v < V; ++v)
+      if (row[v] > row[a]) a = v; /* strict: ties keep the smaller index */
+    double second = -INFINITY;
+    for (int64_t v = 0; v < V; ++v)
+      if (v != a && row[v] > second) second = row[v];
+    const double g = row[a] - second;
+    if (g < best) best = g;
+    if (i == K || x[i] != (int32_t)a) {
+      tokens[i] = (int32_t)a;
+      *gap = best;
+      return i;
+    }
+    tokens[i] = x[i];
+  }
+  *gap = best; /* unreachable */
+  return K;
+}
+
+/* ------------------------------------------------------------------------
+ * The whole verify-and-sample step for B sequences, the same argument
+ * meaning as the CUDA library's run call:
+ *   hidden   [B, K+1, d]  bf16 (dtype 0) or fp32 (dtype 1)
+ *   W        [V, d]       same dtype
+ *   draft    [B, K]       int32
+ *   q_logits [B, K, V]    fp32   (unused when T == 0)
+ *   u        [B, K+1]     fp32   (unused when T == 0)
+ *   T        temperature; 0 selects the greedy rule
+ * Outputs: tokens [B, K+1] (-1 after the emitted prefix), n_accepted [B].
+ * Optional outputs (may be NULL):
+ *   dist   [B]            threshold distance (probability units when T > 0,
+ *                         logit gap when T == 0)
+ *   logits [B*(K+1), V]   fp64 logits
+ *   lse_p  [B*(K+1)]      log-sum-exp of logits / T   (T > 0)
+ *   lse_q  [B*K]          log-sum-exp of q_logits / T (T > 0)
+ * Returns 0, SV_ORACLE_EARG, SV_ORACLE_ENOMEM, or SV_ORACLE_ETOKEN if any
+ * sequence held an out-of-range draft token (that sequence's outputs are
+ * -1 and the others are still computed).
+ * ---------------------------------------------------------------------- */
+int sv_oracle_verify(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
+                     const void *hidden, const void *W, const int32_t *draft,
+                     const float *q_logits, const float *u, double T,
+                     int32_t *out_tokens, int32_t *out_n, double *dist,
+                     double *logits, double *lse_p, double *lse_q) {
+  if (V < 1 || d < 1 || B < 1 || K < 0 || (dtype != 0 && dtype != 1) ||
+      !hidden || !W || !out_tokens || !out_n || !(T >= 0.0) || T == INFINITY)
+    return SV_ORACLE_EARG;
+  if (K > 0 && !draft) return SV_ORACLE_EARG;
+  if (T > 0.0 && (!u || (K > 0 && !q_logits))) return SV_ORACLE_EARG;
+  const int64_t rows = (int64_t)K + 1;
+  const size_t esz = dtype == 0 ? 2 : 4;
+  double *L = (double *)malloc(sizeof(double) * (size_t)(rows * V));
+  double *p = (double *)malloc(sizeof(double) * (size_t)(rows * V));
+  double *q = (double *)malloc(sizeof(double) * (size_t)((K > 0 ? K : 1) * V));
+  double *qrow = (double *)malloc(sizeof(double) * (size_t)V);
+  double *scratch = (double *)malloc(sizeof(double) * (size_t)V);
+  double *ud = (double *)malloc(sizeof(double) * (size_t)rows);
+  if (!L || !p || !q || !qrow || !scratch || !ud) {
+    free(L); free(p); free(q); free(qrow); free(scratch); free(ud);
+    return SV_ORACLE_ENOMEM;
+  }
+  int status = SV_ORACLE_OK;
+  for (int32_t b = 0; b < B; ++b) {
+    const char *hb = (const char *)hidden + (size_t)b * (size_t)(rows * d) * esz;
+    int rc = sv_oracle_logits(V, d, rows, dtype, hb, W, 0, V, L);
+    if (rc != SV_ORACLE_OK) { status = rc; break; }
+    if (logits)
+      memcpy(logits + (size_t)b * (size_t)(rows * V), L,
+             sizeof(double) * (size_t)(rows * V));
+    const int32_t *xb = K > 0 ? draft + (int64_t)b * K : NULL;
+    int32_t *tb = out_tokens + (int64_t)b * rows;
+    double dd;
+    int32_t n;
+    if (T == 0.0) {
+      n = greedy_one_sequence(V, K, L, xb, tb, &dd);
+    } else {
+      for (int64_t i = 0; i < rows; ++i) {
+        const double lse = sv_oracle_lse(V, L + i * V, T);
+        if (lse_p) lse_p[(int64_t)b * rows + i] = lse;
+        for (int64_t v = 0; v < V; ++v) p[i * V + v] = exp(L[i * V + v] / T - lse);
+      }
+      for (int64_t i = 0; i < K; ++i) {
+        const float *ql = q_logits + ((int64_t)b * K + i) * V;
+        for (int64_t v = 0; v < V; ++v) qrow[v] = (double)ql[v];
+        const double lse = sv_oracle_lse(V, qrow, T);
+        if (lse_q) lse_q[(int64_t)b * K + i] = lse;
+        for (int64_t v = 0; v < V; ++v) q[i * V + v] = exp(qrow[v] / T - lse);
+      }
+      for (int64_t i = 0; i < rows; ++i) ud[i] = (double)u[(int64_t)b * rows + i];
+      n = rule_one_sequence(V, K, p, q, xb, ud, tb, &dd, scratch);
+    }
+    if (n == SV_ORACLE_ETOKEN) {
+      status = SV_ORACLE_ETOKEN;
+      for (int64_t i = 0; i < rows; ++i) tb[i] = -1;
+      out_n[b] = -1;
+    } else {
+      out_n[b] = n;
+    }
+    if (dist) dist[b] = dd;
+  }
+  free(L); free(p); free(q); free(qrow); free(scratch); free(ud);
+  return status;
+}
+
+/* ------------------------------------------------------------------------
+ * The rule alone, for many independent rounds that share the same p and q
+ * (the i.i.d.-position setting of the pages' simulations, [P1] "Checking
+ * the math honestly", [P3] three-token example):
+ *   p [K+1, V], q [K, V] probabilities; x [n, K]; u [n, K+1]
+ * Outputs tokens [n, K+1], n_accepted [n], dist [n] (may be NULL).
+ * ---------------------------------------------------------------------- */
+int sv_oracle_rule_batch(int64_t V, int32_t K, const double *p, const double *q,
+                         int64_t n, const int32_t *x, const double *u,
+                         int32_t *out_tokens, int32_t *out_n, double *dist) {
+  if (V < 1 || K < 0 || n < 0 || !p || (K > 0 && (!q || !x)) || !u ||
+      !out_tokens || !out_n)
+    return SV_ORACLE_EARG;
+  double *scratch = (double *)malloc(sizeof(double) * (size_t)V);
+  if (!scratch) return SV_ORACLE_ENOMEM;
+  int status = SV_ORACLE_OK;
+  for (int64_t r = 0; r < n; ++r) {
+    double dd;
+    int32_t *tr = out_tokens + r * (K + 1);
+    int32_t k = rule_one_sequence(V, K, p, q, K > 0 ? x + r * K : NULL,
+                                  u + r * (K + 1), tr, &dd, scratch);
+    if (k == SV_ORACLE_ETOKEN) {
+      status = SV_ORACLE_ETOKEN;
+      out_n[r] = -1;
+    } else {
+      out_n[r] = k;
+    }
+    if (dist) dist[r] = dd;
+  }
+  free(scratch);
+  return status;
+}
+
+/* ------------------------------------------------------------------------
+ * Closed forms of one draft position ([P1] Tool 1, [P4] "The proof"):
+ *   alpha = sum_v min(p(v), q(v))                       (acceptance mass)
+ *   law(v) = min(p, q)(v) + (1 - alpha) * r(v),
+ *            r = max(0, p - q) / sum max(0, p - q)      (emitted law)
+ * With an empty residual (p == q) the second term is dropped (R5 gives the
+ * rejection branch probability zero mass there).  Returns alpha.
+ * ---------------------------------------------------------------------- */
+double sv_oracle_emitted_law(int64_t V, const double *p, const double *q,
+                             double *law) {
+  double alpha = 0.0, S = 0.0;
+  for (int64_t v = 0; v < V; ++v) {
+    alpha += p[v] < q[v] ? p[v] : q[v];
+    const double r = p[v] - q[v];
+    S += r > 0.0 ? r : 0.0;
+  }
+  if (law) {
+    for (int64_t v = 0; v < V; ++v) {
+      const double a = p[v] < q[v] ? p[v] : q[v];
+      const double r = p[v] - q[v];
+      law[v] = a + (S > 0.0 ? (1.0 - alpha) * (r > 0.0 ? r : 0.0) / S : 0.0);
+    }
+  }
+  return alpha;
+}
