@@ -1,0 +1,473 @@
+"""Benchmark of the GB300 verify-and-sample step.
+
+One step = one full verify round (LM-head contraction over the whole
+vocabulary, softmax normalisers, left-to-right accept tests, residual or
+bonus draw) for the Llama-3.1-8B-shaped LM head (V=128256, d=4096, B=1,
+K=4, T=1) on synthetic inputs, through the C ABI.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  Metric: verify rounds/s; ``roofline`` is
+the LM-head contraction kernel's algorithmic bytes over its CUDA-event
+duration against the measured HBM copy bandwidth; ``e2e`` is the same
+metric through spec_verify_run_host with host buffers; ``cpu_baseline``
+times the CPU oracle on a bounded sample.  ``--impl reference`` times the
+CPU oracle alone (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "spec-verify rounds/s and % of HBM roofline at V=128256, d=4096, K=4, B=1"
+UNIT = "rounds/s"
+L2_BYTES = 129 * 1024 * 1024
+NOMINAL_HBM_GBS = 8000.0
+KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_22_gb300", "csrc",
+                          "sv_lmhead_tc.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lmhead_tc_llama8b.md")
+
+
+# ---------------------------------------------------------------------------
+# host-side helpers (no GPU needed; covered by the CPU tests)
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(V, d, B, K, greedy=False, elt=2):
+    """Bytes one verify round must move: W_lm + q_logits + hidden + draft
+    tokens + uniforms + outputs (q and uniforms are not read when greedy)."""
+    w = elt * V * d
+    q = 0 if greedy else 4 * B * K * V
+    h = elt * B * (K + 1) * d
+    small = 4 * B * K + (0 if greedy else 4 * B * (K + 1)) + 4 * B * (K + 1) + 4 * B
+    return w + q + h + small
+
+
+def contraction_bytes(V, d, B, K, greedy=False, elt=2):
+    """Algorithmic bytes of the contraction kernel alone: W_lm, hidden and
+    (sampling) the draft logits it streams for the softmax partials."""
+    return elt * V * d + elt * B * (K + 1) * d + (0 if greedy else 4 * B * K * V)
+
+
+def n_input_sets(set_bytes, minimum=4, cap=256):
+    """Rotating input sets whose total is at least twice the L2 size."""
+    return int(min(cap, max(minimum, math.ceil(2 * L2_BYTES / max(set_bytes, 1)))))
+
+
+def aggregate(elapsed_s: float, rounds: int, group=None):
+    """Max elapsed time and total rounds over all ranks (weak scaling: each
+    rank runs its own rounds on its own W replica)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, rounds
+    dev = torch.device("cuda", torch.cuda.current_device()) \
+        if dist.get_backend(group) == "nccl" else torch.device("cpu")
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    n = torch.tensor([rounds], dtype=torch.int64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), int(n.item())
+
+
+REASON_COLS = {
+    "clocks_event_reasons.hw_slowdown": "hw_slowdown",
+    "clocks_event_reasons.hw_thermal_slowdown": "hw_thermal_slowdown",
+    "clocks_event_reasons.sw_thermal_slowdown": "sw_thermal_slowdown",
+    "clocks_event_reasons.sw_power_cap": "sw_power_cap",
+}
+
+
+def parse_clocks(text: str):
+    """Summarise an nvidia-smi --format=csv clock log: median SM clock under
+    load (samples above 30% of max power draw or any, if none), max clock,
+    and every throttle reason seen Active."""
+    rows = list(csv.reader(io.StringIO(text)))
+    if not rows:
+        return None
+    head = [h.strip().split(" [")[0] for h in rows[0]]
+    idx = {h: i for i, h in enumerate(head)}
+    sm, smax, power, reasons = [], [], [], set()
+    for r in rows[1:]:
+        if len(r) != len(head):
+            continue
+        try:
+            sm.append(float(r[idx["clocks.sm"]].split()[0]))
+            smax.append(float(r[idx["clocks.max.sm"]].split()[0]))
+            power.append(float(r[idx["power.draw"]].split()[0]))
+        except (KeyError, ValueError, IndexError):
+            continue
+        for col, name in REASON_COLS.items():
+            if col in idx and r[idx[col]].strip() == "Active":
+                reasons.add(name)
+    if not sm:
+        return None
+    pmax = max(power) if power else 0.0
+    loaded = [s for s, p in zip(sm, power) if p >= 0.3 * pmax] or sm
+    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+            "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the contraction kernel from the committed
+    ncu summary, or None if the kernel source changed since the capture."""
+    try:
+        text = open(TRAFFIC_FILE).read()
+        src = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    traffic, sha = None, None
+    for line in text.splitlines():
+        if line.startswith("dram_bytes_per_full_launch:"):
+            traffic = int(float(line.split(":", 1)[1].split()[0]))
+        if line.startswith("kernel_source_sha256_16:"):
+            sha = line.split(":", 1)[1].strip()
+    return traffic if (sha == src and traffic) else None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+class ClockSampler:
+    def __init__(self, out_path=None):
+        self.proc = None
+        self.out = out_path
+
+    def start(self, uuid=None):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             + ",".join(REASON_COLS))
+        cmd = ["nvidia-smi", f"--query-gpu={q}", "--format=csv", "-lms", "200"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        if self.out:
+            with open(self.out, "w") as f:
+                f.write(out)
+        return parse_clocks(out)
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_rate(wl, W_np, inputs, budget_s):
+    """Times the CPU oracle (one thread) on this workload.  Full rounds while
+    they fit the budget; otherwise a vocabulary slice of the contraction,
+    which is >99.9% of an oracle round at this shape, scaled to a round."""
+    import oracle
+    import spec_inputs as si
+    h = si.to_oracle(inputs["hidden"]).reshape(wl.B * (wl.K + 1), wl.d)
+    t0 = time.perf_counter()
+    rows = 1024
+    oracle.logits(h, W_np, 0, rows)
+    per_row = (time.perf_counter() - t0) / rows
+    round_est = per_row * wl.V
+    if round_est <= budget_s / 2:
+        args = (si.to_oracle(inputs["hidden"]), W_np, si.to_oracle(inputs["draft"]),
+                si.to_oracle(inputs["q_logits"]), si.to_oracle(inputs["uniforms"]), wl.T)
+        n, t0 = 0, time.perf_counter()
+        while True:
+            oracle.verify(*args)
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s / 2 or n >= 1000:
+                break
+        return n / el, f"{n} full oracle rounds", n
+    rows = max(1024, int(wl.V * (budget_s / 2) / round_est))
+    rows = min(rows, wl.V)
+    t0 = time.perf_counter()
+    oracle.logits(h, W_np, 0, rows)
+    el = time.perf_counter() - t0
+    frac = rows / wl.V
+    return frac / el, (f"contraction over {rows} of {wl.V} vocabulary rows "
+                       f"({frac:.3f} of a round), scaled to one round"), frac
+
+
+def reference_arm(args, wl, dev):
+    import torch
+    import spec_inputs as si
+    W = si.make_weights(wl, seed=1, device=dev)
+    inputs = si.make_round(wl, W, seed=2)
+    W_np = si.to_oracle(W)
+    budget_per_step = max(0.05, 150.0 / max(1, args.steps + args.warmup))
+    import oracle
+    h = si.to_oracle(inputs["hidden"]).reshape(wl.B * (wl.K + 1), wl.d)
+    t0 = time.perf_counter()
+    oracle.logits(h, W_np, 0, 1024)
+    per_row = (time.perf_counter() - t0) / 1024
+    rows = int(min(wl.V, max(256, budget_per_step / per_row)))
+    full = rows == wl.V
+    args_full = (si.to_oracle(inputs["hidden"]), W_np, si.to_oracle(inputs["draft"]),
+                 si.to_oracle(inputs["q_logits"]), si.to_oracle(inputs["uniforms"]), wl.T)
+
+    def step(i):
+        if full:
+            oracle.verify(*args_full)
+        else:
+            v0 = (i * rows) % (wl.V - rows + 1)
+            oracle.logits(h, W_np, v0, v0 + rows)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    el = time.perf_counter() - t0
+    frac = rows / wl.V
+    value = args.steps * frac / el
+    sample = ("full oracle rounds" if full else
+              f"each step: the oracle's contraction over {rows} of {wl.V} vocabulary rows "
+              f"({frac:.4f} of a round, >99.9% of a round's oracle time), scaled to rounds")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def workload_config(wl, extra=None):
+    cfg = {"workload": f"Llama-3.1-8B-shaped LM-head verify round, V={wl.V}, d={wl.d}, "
+                       f"B={wl.B}, K={wl.K}, T={wl.T}, draft acceptance ~{wl.alpha}",
+           "V": wl.V, "d": wl.d, "B": wl.B, "K": wl.K, "T": wl.T,
+           "weights": "bf16 N(0, 0.02^2)", "alpha_target": wl.alpha}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--clock-log", default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import torch
+    import torch.distributed as dist
+    import spec_inputs as si
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = si.workload(args.workload)
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args, wl, dev)), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    import speculative_decoding_verification_22_gb300 as sv
+
+    T = wl.T
+    W = si.make_weights(wl, seed=1 + 1000 * rank, device=dev)
+    set_bytes = (2 * wl.B * (wl.K + 1) * wl.d + 4 * wl.B * wl.K * wl.V
+                 + 4 * wl.B * wl.K + 4 * wl.B * (wl.K + 1))
+    nsets = n_input_sets(set_bytes)
+    sets = [si.make_round(wl, W, seed=10_000 + 1000 * rank + i) for i in range(nsets)]
+    eng = sv.SpecVerify(wl.V, wl.d, wl.B, wl.K, "bf16", device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sv.spec_verify_set_stream(eng.h, stream)
+    out_tok = torch.empty((nsets, wl.B, wl.K + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((nsets, wl.B), dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+
+    def run_set(i):
+        s = sets[i]
+        sv.spec_verify_run(eng.h, s["hidden"], W, s["draft"], s["q_logits"],
+                           s["uniforms"], T, out_tok[i], out_n[i])
+
+    launches_per_run = sv.spec_verify_launches_per_run(eng.h, T)
+    # warm-up (also the first use of every input set)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, nsets)):
+            run_set(i % nsets)
+    stream.synchronize()
+    code = eng.status()
+    if code != sv.SV_OK:
+        raise RuntimeError(f"device status after warm-up: {sv.spec_verify_strerror(code)}")
+
+    graph = None
+    if not args.no_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(nsets):
+                    run_set(i)
+            stream.synchronize()
+            with torch.cuda.stream(stream):
+                graph.replay()
+            stream.synchronize()
+        except Exception as exc:  # capture unsupported: launch directly
+            print(f"[bench] graph capture failed ({exc}); direct launches", file=sys.stderr)
+            graph = None
+    reps = max(1, round(args.steps / nsets)) if graph is not None else 0
+    steps = reps * nsets if graph is not None else args.steps
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(args.clock_log)
+    sampler.start(uuid)
+    time.sleep(0.4)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        if graph is not None:
+            for _ in range(reps):
+                graph.replay()
+        else:
+            for i in range(steps):
+                run_set(i % nsets)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    clocks = sampler.stop()
+    code = eng.status()
+    if code != sv.SV_OK:
+        raise RuntimeError(f"device status after timing: {sv.spec_verify_strerror(code)}")
+    max_el, total_rounds = aggregate(elapsed, steps)
+    value = total_rounds / max_el
+
+    # emitted tokens per round over the input sets
+    n_host = out_n.cpu().numpy()
+    tokens_per_round = float((n_host + 1).mean())
+
+    # contraction kernel timing (CUDA events on the launching stream)
+    kt_steps = min(steps, 2000)
+    sv.spec_verify_timing(eng.h, True)
+    with torch.cuda.stream(stream):
+        for i in range(kt_steps):
+            run_set(i % nsets)
+    ms_k1, n_k1 = sv.spec_verify_timing_read(eng.h)
+    sv.spec_verify_timing(eng.h, False)
+    k1_s = ms_k1 / 1e3 / n_k1
+    peaks, peak_src = measured_peaks()
+    k1_bytes = contraction_bytes(wl.V, wl.d, wl.B, wl.K)
+    achieved = k1_bytes / k1_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": recorded_traffic(),
+                "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                "kernel": "lmhead_tc_kernel (LM-head contraction + softmax partials)",
+                "kernel_us": k1_s * 1e6, "algorithmic_bytes_per_launch": k1_bytes,
+                "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
+                "step_frac_of_measured": algorithmic_bytes(wl.V, wl.d, wl.B, wl.K)
+                * value / world / 1e9 / peaks["hbm_gbs"]}
+
+    # end to end through the host-buffer entry point
+    e2e_steps = min(steps, 1000)
+    pin = [{k: sets[i][k].cpu().pin_memory() for k in ("hidden", "draft", "q_logits", "uniforms")}
+           for i in range(min(nsets, 8))]
+    ht = torch.empty((wl.B, wl.K + 1), dtype=torch.int32).pin_memory()
+    hn = torch.empty((wl.B,), dtype=torch.int32).pin_memory()
+    for i in range(3):
+        p = pin[i % len(pin)]
+        sv.spec_verify_run_host(eng.h, p["hidden"], W, p["draft"], p["q_logits"],
+                                p["uniforms"], T, ht, hn)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        p = pin[i % len(pin)]
+        sv.spec_verify_run_host(eng.h, p["hidden"], W, p["draft"], p["q_logits"],
+                                p["uniforms"], T, ht, hn)
+    e2e_el = time.perf_counter() - t0
+    _, e2e_total = aggregate(e2e_el, e2e_steps)
+    e2e_max, _ = aggregate(e2e_el, e2e_steps)
+    h2d = sum(pin[0][k].numel() * pin[0][k].element_size() for k in pin[0])
+    d2h = ht.numel() * 4 + hn.numel() * 4
+
+    cpu = None
+    if rank == 0:
+        W_np = si.to_oracle(W)
+        rate, sample, _ = oracle_rate(wl, W_np, sets[0], args.cpu_budget)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": steps, "warmup": max(args.warmup, nsets),
+            "ms_per_step": 1e3 * max_el / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": workload_config(wl, {
+                "l2": f"inputs larger than L2: W_lm {2 * wl.V * wl.d} B per round plus "
+                      f"{nsets} rotating hidden/q/uniform sets ({nsets * set_bytes} B)",
+                "graph": graph is not None,
+                "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}),
+            "emitted_tokens_per_round": tokens_per_round,
+            "emitted_tokens_per_s": value * tokens_per_round,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_total / e2e_max, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_run * steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    eng.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,183 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) verify-and-sample step of
+ * speculative decoding.
+ *
+ * One call to spec_verify_run performs, for B independent sequences, the
+ * target-side tail of one speculative round:
+ *
+ *   1. LM-head contraction: logits L[b, i, v] = sum_k hidden[b, i, k] * W_lm[v, k]
+ *      for the K+1 verified positions i = 0..K of every sequence.
+ *      ("What Actually Happens During Speculative Decoding in LLMs", the
+ *      memory-bound section: the verify pass multiplies a [positions x d]
+ *      block against weights that are read from memory once.)
+ *   2. Temperature softmax: p_{i+1} = softmax(L[b, i, :] / T) and
+ *      q_{i+1} = softmax(q_logits[b, i, :] / T), the same T for both.
+ *      ("Speculative Decoding: Two Models, One Voice", "The rule that makes
+ *      it exact", third remark; "Speculative Decoding: The Algebra and the
+ *      Proof", "Where it breaks".)
+ *   3. Left-to-right accept test: draft token x_{i+1} survives iff
+ *      u[b, i] < p_{i+1}(x) / q_{i+1}(x) (strict; if q(x) == 0 it survives
+ *      iff p(x) > 0).  The round stops at the first rejection.
+ *      ("Speculative Decoding: Two Models, One Voice", "The idea", step 3;
+ *      "Speculative Decoding" (library wiki), "One speculation round".)
+ *   4. Final draw with the last uniform u[b, K]: at a rejection at position
+ *      j, from norm(max(0, p_j - q_j)) (from p_j if that residual is empty);
+ *      if all K survive, the bonus token from p_{K+1}.  Every draw is an
+ *      inverse CDF in token-id order: the smallest v with u * S < C_v.
+ *      ("Speculative Decoding: Guess Several Tokens, Check Them in One
+ *      Pass", Step 3; "What Actually Happens ...", speculative_sample_step.)
+ *   5. T == 0 is greedy verification: accept while x_{i+1} equals the
+ *      argmax of L[b, i, :] (ties to the smallest id), emit that argmax at
+ *      the first mismatch, or the argmax of L[b, K, :] as the bonus.
+ *      ("Speculative Decoding: Guess Several Tokens, Check Them in One
+ *      Pass", Step 2, verify_greedy; "Two Models, One Voice", first remark.)
+ *
+ * Conventions for every function:
+ *   - Return value: 0 (SV_OK) or a negative SV_ERR_* code.  No function
+ *     throws, aborts or prints.
+ *   - Pointers named "device" must be device memory (or managed memory)
+ *     visible to the handle's device; they are owned by the caller and are
+ *     never freed or retained by the library beyond the call.
+ *   - All tensors are dense, row-major, and 16-byte aligned.
+ *   - Host-detectable errors (bad arguments, alignment, shapes) return
+ *     before anything is launched.  Errors found on the device (draft token
+ *     out of range, non-finite logits, a bounded wait that ran out) are
+ *     written to a device status word; read them with spec_verify_status.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define SV_OK 0
+#define SV_ERR_ARG (-1)       /* null pointer, bad size, bad temperature     */
+#define SV_ERR_ALIGN (-2)     /* pointer not 16-byte aligned                 */
+#define SV_ERR_SHAPE (-3)     /* V, d, B, K outside the supported limits     */
+#define SV_ERR_CUDA (-4)      /* a CUDA runtime/driver call failed           */
+#define SV_ERR_ARCH (-5)      /* device is not compute capability 10.3       */
+#define SV_ERR_TIMEOUT (-6)   /* a bounded device-side wait ran out          */
+#define SV_ERR_TOKEN (-7)     /* a draft token was outside [0, V)            */
+#define SV_ERR_NONFINITE (-8) /* logits or draft logits were NaN/inf         */
+
+/* Element type of hidden and W_lm. */
+#define SV_BF16 0 /* production path: TMA + tcgen05 tensor-core contraction   */
+#define SV_FP32 1 /* reference-precision path for small vocabularies         */
+
+/* Limits checked at create time. */
+#define SV_MAX_K 16      /* draft tokens per sequence                        */
+#define SV_MAX_B 4096    /* sequences per call                               */
+#define SV_MAX_ROWS_BF16 384 /* B * (K+1) for the bf16 path                  */
+
+typedef struct spec_verify spec_verify_t; /* opaque handle */
+
+typedef struct {
+  int64_t V;      /* vocabulary size, >= 1                                   */
+  int64_t d;      /* hidden size; bf16: multiple of 8, fp32: multiple of 4   */
+  int32_t B;      /* sequences per call, 1..SV_MAX_B                         */
+  int32_t K;      /* draft tokens per sequence, 0..SV_MAX_K                  */
+  int32_t dtype;  /* SV_BF16 or SV_FP32                                      */
+  void *stream;   /* cudaStream_t the calls are enqueued on (NULL = legacy)  */
+} sv_config_t;
+
+/* Creates a handle for one problem shape on the current CUDA device and
+ * allocates its device workspace (logits scratch, softmax partials,
+ * per-sequence state, status word, staging buffers for
+ * spec_verify_run_host).  *out receives the handle.
+ * Errors: SV_ERR_ARG (null pointer, bad dtype), SV_ERR_SHAPE (limits
+ * above), SV_ERR_ARCH (not compute capability 10.3), SV_ERR_CUDA
+ * (allocation failed).  On error *out is set to NULL. */
+int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out);
+
+/* Enqueues one verify-and-sample step (steps 1-5 above) on the handle's
+ * stream and returns without synchronising.  Outputs are valid once the
+ * stream has reached this point.  The call allocates nothing and does not
+ * synchronise the host, so it can be captured in a CUDA graph.
+ *   hidden         device, [B, K+1, d] of dtype; row i of sequence b is the
+ *                  final hidden state that scores draft position i+1 (row K
+ *                  scores the bonus position K+1)
+ *   W_lm           device, [V, d] of dtype (the LM-head matrix, read once)
+ *   draft_tokens   device, int32 [B, K], each in [0, V); may be NULL if K == 0
+ *   q_logits       device, fp32 [B, K, V] draft logits; unused if T == 0
+ *   uniforms       device, fp32 [B, K+1] in [0, 1): u[b, i] for the accept
+ *                  test of position i+1, u[b, K] for the final draw;
+ *                  unused if T == 0
+ *   temperature    T > 0 samples; T == 0 selects greedy verification
+ *   out_tokens     device, int32 [B, K+1]: the accepted prefix, then the
+ *                  resampled or bonus token, then -1
+ *   out_n_accepted device, int32 [B]: accepted draft tokens (the round
+ *                  emitted n + 1 tokens); -1 for a sequence with an invalid
+ *                  draft token or non-finite logits
+ * Errors (returned): SV_ERR_ARG (null handle/pointer, T < 0 or not finite),
+ * SV_ERR_ALIGN, SV_ERR_CUDA (launch failed).
+ * Errors (device status word): SV_ERR_TOKEN, SV_ERR_NONFINITE,
+ * SV_ERR_TIMEOUT. */
+int spec_verify_run(spec_verify_t *h, const void *hidden, const void *W_lm,
+                    const int32_t *draft_tokens, const float *q_logits,
+                    const float *uniforms, float temperature,
+                    int32_t *out_tokens, int32_t *out_n_accepted);
+
+/* The same step end to end from HOST buffers: copies hidden, draft_tokens,
+ * q_logits and uniforms (host; pinned memory recommended) into the handle's
+ * staging buffers, runs the step, copies out_tokens and out_n_accepted back
+ * to the host buffers, and synchronises the stream before returning.  W_lm
+ * stays a DEVICE pointer (model weights are resident).  Argument meaning
+ * and errors as spec_verify_run; the device status word is also checked
+ * and returned. */
+int spec_verify_run_host(spec_verify_t *h, const void *hidden_host,
+                         const void *W_lm, const int32_t *draft_tokens_host,
+                         const float *q_logits_host, const float *uniforms_host,
+                         float temperature, int32_t *out_tokens_host,
+                         int32_t *out_n_accepted_host);
+
+/* Synchronises the handle's stream, then returns and clears the device
+ * status word (SV_OK if no device-side error occurred since the last call),
+ * or SV_ERR_CUDA if synchronisation failed. */
+int spec_verify_status(spec_verify_t *h);
+
+/* Replaces the stream that later calls are enqueued on. */
+int spec_verify_set_stream(spec_verify_t *h, void *stream);
+
+/* Copies the last run's fp32 logits [B*(K+1), V] (row b*(K+1)+i) to dst
+ * (host or device, B*(K+1)*V floats).  Synchronises.  For tests. */
+int spec_verify_debug_logits(spec_verify_t *h, float *dst);
+
+/* Copies the last run's log-sum-exp normalisers (fp64) to dst (host or
+ * device): B*(K+1) values of logits/T, then B*K values of q_logits/T.
+ * Synchronises.  For tests; meaningful only when T > 0. */
+int spec_verify_debug_lse(spec_verify_t *h, double *dst);
+
+/* Upper bound, in nanoseconds, of every device-side wait (default 1e9).
+ * A wait that runs out sets SV_ERR_TIMEOUT and the kernel returns early
+ * after draining its own copies in flight.  0 makes the first wait that is
+ * not already satisfied give up at once (used to test that path). */
+int spec_verify_set_wait_limit(spec_verify_t *h, uint64_t limit_ns);
+
+/* Kernel timing for the benchmark: while enabled, each run records CUDA
+ * events on the handle's stream around the LM-head contraction kernel.
+ * spec_verify_timing_read synchronises and returns the summed duration in
+ * milliseconds and the number of timed launches since enabling. */
+int spec_verify_timing(spec_verify_t *h, int enable);
+int spec_verify_timing_read(spec_verify_t *h, double *total_ms,
+                            int64_t *launches);
+
+/* Number of kernel launches one spec_verify_run enqueues for temperature
+ * T (the contraction, the decision pass, and for T > 0 the residual and
+ * selection passes). */
+int spec_verify_launches_per_run(spec_verify_t *h, float temperature);
+
+/* Static description of an error code. */
+const char *spec_verify_strerror(int code);
+
+/* Frees the handle and its workspace.  NULL is ignored. */
+void spec_verify_destroy(spec_verify_t *h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

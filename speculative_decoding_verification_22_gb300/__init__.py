@@ -1,0 +1,242 @@
+"""Python binding of the GB300 verify-and-sample library (libspec_verify.so).
+
+Argument marshalling only: every step of the verify path runs in the CUDA
+kernels behind the C ABI of ``include/spec_verify.h``; the functions here
+carry the same names as the C entry points, take torch tensors (device
+memory) and pass their pointers and the current CUDA stream through.
+There is no fallback: if the library has not been built, importing the
+entry points raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspec_verify.so")
+
+SV_OK = 0
+SV_ERR_ARG = -1
+SV_ERR_ALIGN = -2
+SV_ERR_SHAPE = -3
+SV_ERR_CUDA = -4
+SV_ERR_ARCH = -5
+SV_ERR_TIMEOUT = -6
+SV_ERR_TOKEN = -7
+SV_ERR_NONFINITE = -8
+SV_BF16 = 0
+SV_FP32 = 1
+SV_MAX_K = 16
+SV_MAX_B = 4096
+SV_MAX_ROWS_BF16 = 384
+
+# every symbol of include/spec_verify.h
+EXPORTS = ("spec_verify_create", "spec_verify_run", "spec_verify_run_host",
+           "spec_verify_status", "spec_verify_set_stream",
+           "spec_verify_debug_logits", "spec_verify_debug_lse",
+           "spec_verify_set_wait_limit", "spec_verify_timing",
+           "spec_verify_timing_read", "spec_verify_launches_per_run",
+           "spec_verify_strerror", "spec_verify_destroy")
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {spec_verify_strerror(code)} ({code})")
+        self.code = code
+
+
+class sv_config_t(ctypes.Structure):
+    _fields_ = [("V", ctypes.c_int64), ("d", ctypes.c_int64),
+                ("B", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("stream", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load_library():
+    """Loads the in-tree CUDA library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                "(or python -m speculative_decoding_verification_22_gb300.build)")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64, f32 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                             ctypes.c_float)
+        lib.spec_verify_create.argtypes = [ctypes.POINTER(sv_config_t),
+                                           ctypes.POINTER(vp)]
+        lib.spec_verify_run.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, vp]
+        lib.spec_verify_run_host.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, vp]
+        lib.spec_verify_status.argtypes = [vp]
+        lib.spec_verify_set_stream.argtypes = [vp, vp]
+        lib.spec_verify_debug_logits.argtypes = [vp, vp]
+        lib.spec_verify_debug_lse.argtypes = [vp, vp]
+        lib.spec_verify_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
+        lib.spec_verify_timing.argtypes = [vp, ctypes.c_int]
+        lib.spec_verify_timing_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double),
+                                                ctypes.POINTER(i64)]
+        lib.spec_verify_launches_per_run.argtypes = [vp, f32]
+        lib.spec_verify_strerror.argtypes = [ctypes.c_int]
+        lib.spec_verify_strerror.restype = ctypes.c_char_p
+        lib.spec_verify_destroy.argtypes = [vp]
+        lib.spec_verify_destroy.restype = None
+        for name in EXPORTS:
+            if name not in ("spec_verify_strerror", "spec_verify_destroy"):
+                getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _check(code: int, what: str):
+    if code != SV_OK:
+        raise SpecVerifyError(code, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def spec_verify_strerror(code: int) -> str:
+    return load_library().spec_verify_strerror(int(code)).decode()
+
+
+def spec_verify_create(V: int, d: int, B: int, K: int, dtype="bf16", stream=None):
+    """Creates a handle; ``dtype`` is "bf16"/"fp32" (or SV_BF16/SV_FP32)."""
+    code = {"bf16": SV_BF16, "fp32": SV_FP32}.get(dtype, dtype)
+    cfg = sv_config_t(int(V), int(d), int(B), int(K), int(code),
+                      _stream_handle(stream))
+    h = ctypes.c_void_p()
+    _check(load_library().spec_verify_create(ctypes.byref(cfg), ctypes.byref(h)),
+           "spec_verify_create")
+    return h
+
+
+def spec_verify_run(h, hidden, W_lm, draft_tokens, q_logits, uniforms,
+                    temperature: float, out_tokens, out_n_accepted) -> None:
+    _check(load_library().spec_verify_run(
+        h, _ptr(hidden), _ptr(W_lm), _ptr(draft_tokens), _ptr(q_logits),
+        _ptr(uniforms), float(temperature), _ptr(out_tokens),
+        _ptr(out_n_accepted)), "spec_verify_run")
+
+
+def spec_verify_run_host(h, hidden, W_lm, draft_tokens, q_logits, uniforms,
+                         temperature: float, out_tokens, out_n_accepted) -> None:
+    """Host-buffer variant: hidden/draft/q/uniforms/outputs are host
+    (preferably pinned) tensors, W_lm a device tensor; returns after the
+    outputs have been copied back."""
+    _check(load_library().spec_verify_run_host(
+        h, _ptr(hidden), _ptr(W_lm), _ptr(draft_tokens), _ptr(q_logits),
+        _ptr(uniforms), float(temperature), _ptr(out_tokens),
+        _ptr(out_n_accepted)), "spec_verify_run_host")
+
+
+def spec_verify_status(h) -> int:
+    return int(load_library().spec_verify_status(h))
+
+
+def spec_verify_set_stream(h, stream=None) -> None:
+    _check(load_library().spec_verify_set_stream(h, _stream_handle(stream)),
+           "spec_verify_set_stream")
+
+
+def spec_verify_debug_logits(h, dst) -> None:
+    _check(load_library().spec_verify_debug_logits(h, _ptr(dst)),
+           "spec_verify_debug_logits")
+
+
+def spec_verify_debug_lse(h, dst) -> None:
+    _check(load_library().spec_verify_debug_lse(h, _ptr(dst)),
+           "spec_verify_debug_lse")
+
+
+def spec_verify_set_wait_limit(h, limit_ns: int) -> None:
+    _check(load_library().spec_verify_set_wait_limit(h, int(limit_ns)),
+           "spec_verify_set_wait_limit")
+
+
+def spec_verify_timing(h, enable: bool) -> None:
+    _check(load_library().spec_verify_timing(h, int(bool(enable))),
+           "spec_verify_timing")
+
+
+def spec_verify_timing_read(h):
+    ms = ctypes.c_double()
+    n = ctypes.c_int64()
+    _check(load_library().spec_verify_timing_read(h, ctypes.byref(ms), ctypes.byref(n)),
+           "spec_verify_timing_read")
+    return ms.value, n.value
+
+
+def spec_verify_launches_per_run(h, temperature: float) -> int:
+    n = load_library().spec_verify_launches_per_run(h, float(temperature))
+    if n < 0:
+        raise SpecVerifyError(n, "spec_verify_launches_per_run")
+    return n
+
+
+def spec_verify_destroy(h) -> None:
+    if h:
+        load_library().spec_verify_destroy(h)
+
+
+class SpecVerify:
+    """Owns one handle; ``run`` writes tokens [B, K+1] and n_accepted [B]."""
+
+    def __init__(self, V, d, B, K, dtype="bf16", device=None, stream=None):
+        self.V, self.d, self.B, self.K, self.dtype = V, d, B, K, dtype
+        self.device = torch.device("cuda" if device is None else device)
+        with torch.cuda.device(self.device):
+            self.h = spec_verify_create(V, d, B, K, dtype, stream)
+
+    def run(self, hidden, W_lm, draft_tokens, q_logits, uniforms, temperature,
+            out_tokens=None, out_n_accepted=None):
+        if out_tokens is None:
+            out_tokens = torch.empty((self.B, self.K + 1), dtype=torch.int32,
+                                     device=self.device)
+        if out_n_accepted is None:
+            out_n_accepted = torch.empty((self.B,), dtype=torch.int32, device=self.device)
+        spec_verify_run(self.h, hidden, W_lm, draft_tokens, q_logits, uniforms,
+                        temperature, out_tokens, out_n_accepted)
+        return out_tokens, out_n_accepted
+
+    def status(self) -> int:
+        return spec_verify_status(self.h)
+
+    def logits(self):
+        out = torch.empty((self.B * (self.K + 1), self.V), dtype=torch.float32,
+                          device=self.device)
+        spec_verify_debug_logits(self.h, out)
+        return out
+
+    def lse(self):
+        out = torch.empty((self.B * (self.K + 1) + self.B * self.K,), dtype=torch.float64,
+                          device=self.device)
+        spec_verify_debug_lse(self.h, out)
+        return out
+
+    def close(self):
+        if getattr(self, "h", None):
+            spec_verify_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,423 @@
+// sv_api.cu -- the C ABI declared in include/spec_verify.h: handle
+// lifetime, argument checks, workspace, TMA descriptors and the launch
+// sequence of one verify-and-sample step.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "sv_internal.cuh"
+#include "sv_kernels.h"
+
+namespace {
+
+constexpr int kTimingRing = 256;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct spec_verify {
+  sv_config_t cfg{};
+  int device = 0;
+  int num_sms = 0;
+  int smem_optin = 0;
+  cudaStream_t stream = nullptr;
+  sv::Dims dims{};
+  sv::Work w{};
+  sv::TcPlan plan{};
+  unsigned epoch = 0;
+  uint64_t wait_limit_ns = 1000000000ull;
+  // staging for spec_verify_run_host
+  void *st_hidden = nullptr;
+  int32_t *st_draft = nullptr;
+  float *st_q = nullptr;
+  float *st_u = nullptr;
+  int32_t *st_tokens = nullptr;
+  int32_t *st_n = nullptr;
+  // TMA descriptors, re-encoded when the tensor moves
+  CUtensorMap tmW{}, tmH{};
+  const void *tmW_ptr = nullptr, *tmH_ptr = nullptr;
+  // kernel timing
+  bool timing = false;
+  std::vector<cudaEvent_t> ev0, ev1;
+  int64_t timed = 0, folded = 0;
+  double timed_ms = 0.0;
+};
+
+namespace {
+
+size_t esize(int dtype) { return dtype == SV_BF16 ? 2 : 4; }
+
+void free_all(spec_verify *h) {
+  void *ptrs[] = {h->w.logits, h->w.part_p, h->w.part_q, h->w.lse, h->w.seq, h->w.chunk_mass,
+                  h->w.split_buf, h->w.split_cnt, h->w.status, h->w.abort_epoch, h->st_hidden,
+                  h->st_draft, h->st_q, h->st_u, h->st_tokens, h->st_n};
+  for (void *p : ptrs)
+    if (p) cudaFree(p);
+  for (cudaEvent_t e : h->ev0) cudaEventDestroy(e);
+  for (cudaEvent_t e : h->ev1) cudaEventDestroy(e);
+}
+
+template <typename T>
+bool dalloc(T **p, size_t count) {
+  if (count == 0) count = 1;
+  return cudaMalloc(reinterpret_cast<void **>(p), count * sizeof(T)) == cudaSuccess;
+}
+
+int encode_2d(CUtensorMap *map, const void *base, int64_t inner, int64_t outer,
+              uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return SV_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SV_OK : SV_ERR_CUDA;
+}
+
+// Folds finished timing pairs into the running total (blocking on them).
+void fold_timing(spec_verify *h, int64_t upto) {
+  for (; h->folded < upto; ++h->folded) {
+    const int i = static_cast<int>(h->folded % kTimingRing);
+    float ms = 0.0f;
+    cudaEventSynchronize(h->ev1[i]);
+    if (cudaEventElapsedTime(&ms, h->ev0[i], h->ev1[i]) == cudaSuccess) h->timed_ms += ms;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *spec_verify_strerror(int code) {
+  switch (code) {
+    case SV_OK: return "ok";
+    case SV_ERR_ARG: return "invalid argument";
+    case SV_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case SV_ERR_SHAPE: return "shape outside supported limits";
+    case SV_ERR_CUDA: return "CUDA call failed";
+    case SV_ERR_ARCH: return "device is not compute capability 10.3 (sm_103a)";
+    case SV_ERR_TIMEOUT: return "a device-side wait ran out";
+    case SV_ERR_TOKEN: return "draft token outside [0, V)";
+    case SV_ERR_NONFINITE: return "non-finite logits or draft logits";
+    default: return "unknown error";
+  }
+}
+
+int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
+  if (!out) return SV_ERR_ARG;
+  *out = nullptr;
+  if (!cfg) return SV_ERR_ARG;
+  if (cfg->dtype != SV_BF16 && cfg->dtype != SV_FP32) return SV_ERR_ARG;
+  if (cfg->V < 1 || cfg->V > INT32_MAX || cfg->d < 1 || cfg->d > (1 << 20) || cfg->B < 1 ||
+      cfg->B > SV_MAX_B || cfg->K < 0 || cfg->K > SV_MAX_K)
+    return SV_ERR_SHAPE;
+  if (cfg->d % (cfg->dtype == SV_BF16 ? 8 : 4) != 0) return SV_ERR_SHAPE;
+  const int64_t R = static_cast<int64_t>(cfg->B) * (cfg->K + 1);
+  if (cfg->dtype == SV_BF16 && R > SV_MAX_ROWS_BF16) return SV_ERR_SHAPE;
+  if (R * cfg->V > (int64_t(1) << 40)) return SV_ERR_SHAPE;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return SV_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return SV_ERR_ARCH;
+
+  spec_verify *h = new (std::nothrow) spec_verify();
+  if (!h) return SV_ERR_CUDA;
+  h->cfg = *cfg;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  h->smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
+  h->stream = static_cast<cudaStream_t>(cfg->stream);
+
+  sv::Dims &D = h->dims;
+  D.V = cfg->V;
+  D.d = cfg->d;
+  D.B = cfg->B;
+  D.K = cfg->K;
+  D.R = static_cast<int>(R);
+  D.RQ = cfg->B * cfg->K;
+  D.nsub = static_cast<int>((cfg->V + sv::kSub - 1) / sv::kSub);
+  D.ntile = static_cast<int>((cfg->V + sv::kTileM - 1) / sv::kTileM);
+  D.nchunk = static_cast<int>((cfg->V + sv::kChunk - 1) / sv::kChunk);
+
+  size_t split_floats = 1;
+  if (cfg->dtype == SV_BF16) {
+    h->plan = sv::plan_tc(D, h->num_sms, h->smem_optin);
+    if (!h->plan.valid) {
+      delete h;
+      return SV_ERR_SHAPE;
+    }
+    split_floats = static_cast<size_t>(h->plan.grid) * 2 * sv::kTileM * h->plan.npad;
+  }
+  const size_t es = esize(cfg->dtype);
+  bool ok = dalloc(&h->w.logits, static_cast<size_t>(R) * D.V) &&
+            dalloc(&h->w.part_p, static_cast<size_t>(R) * D.nsub) &&
+            dalloc(&h->w.part_q, static_cast<size_t>(D.RQ) * D.nsub) &&
+            dalloc(&h->w.lse, static_cast<size_t>(R + D.RQ)) && dalloc(&h->w.seq, D.B) &&
+            dalloc(&h->w.chunk_mass, static_cast<size_t>(D.B) * D.nchunk) &&
+            dalloc(&h->w.split_buf, split_floats) &&
+            dalloc(&h->w.split_cnt, static_cast<size_t>(h->num_sms) * 4) &&
+            dalloc(&h->w.status, 1) && dalloc(&h->w.abort_epoch, 1) &&
+            dalloc(reinterpret_cast<uint8_t **>(&h->st_hidden), static_cast<size_t>(R) * D.d * es) &&
+            dalloc(&h->st_draft, static_cast<size_t>(D.RQ)) &&
+            dalloc(&h->st_q, static_cast<size_t>(D.RQ) * D.V) && dalloc(&h->st_u, R) &&
+            dalloc(&h->st_tokens, R) && dalloc(&h->st_n, D.B);
+  if (ok)
+    ok = cudaMemset(h->w.split_cnt, 0, sizeof(int) * h->num_sms * 4) == cudaSuccess &&
+         cudaMemset(h->w.status, 0, sizeof(int)) == cudaSuccess &&
+         cudaMemset(h->w.abort_epoch, 0, sizeof(unsigned)) == cudaSuccess &&
+         cudaMemset(h->w.lse, 0, sizeof(double) * (R + D.RQ)) == cudaSuccess &&
+         cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok) {
+    free_all(h);
+    delete h;
+    return SV_ERR_CUDA;
+  }
+  *out = h;
+  return SV_OK;
+}
+
+void spec_verify_destroy(spec_verify_t *h) {
+  if (!h) return;
+  cudaStreamSynchronize(h->stream);
+  free_all(h);
+  delete h;
+}
+
+int spec_verify_set_stream(spec_verify_t *h, void *stream) {
+  if (!h) return SV_ERR_ARG;
+  h->stream = static_cast<cudaStream_t>(stream);
+  return SV_OK;
+}
+
+int spec_verify_set_wait_limit(spec_verify_t *h, uint64_t limit_ns) {
+  if (!h) return SV_ERR_ARG;
+  h->wait_limit_ns = limit_ns;
+  return SV_OK;
+}
+
+int spec_verify_launches_per_run(spec_verify_t *h, float temperature) {
+  if (!h) return SV_ERR_ARG;
+  return temperature > 0.0f ? 4 : 2;
+}
+
+int spec_verify_run(spec_verify_t *h, const void *hidden, const void *W_lm,
+                    const int32_t *draft_tokens, const float *q_logits, const float *uniforms,
+                    float temperature, int32_t *out_tokens, int32_t *out_n_accepted) {
+  if (!h || !hidden || !W_lm || !out_tokens || !out_n_accepted) return SV_ERR_ARG;
+  if (!(temperature >= 0.0f) || !std::isfinite(temperature)) return SV_ERR_ARG;
+  const sv::Dims &D = h->dims;
+  const bool greedy = temperature == 0.0f;
+  if (D.K > 0 && !draft_tokens) return SV_ERR_ARG;
+  if (!greedy && ((D.K > 0 && !q_logits) || !uniforms)) return SV_ERR_ARG;
+  const void *ptrs[] = {hidden, W_lm, draft_tokens, q_logits, uniforms, out_tokens,
+                        out_n_accepted};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return SV_ERR_ALIGN;
+
+  cudaStream_t st = h->stream;
+  const unsigned epoch = ++h->epoch;
+  const float inv_t = greedy ? 1.0f : static_cast<float>(1.0 / static_cast<double>(temperature));
+  cudaError_t e = cudaSuccess;
+
+  int ti = -1;
+  if (h->timing) {
+    if (h->timed >= kTimingRing) fold_timing(h, h->timed - kTimingRing + 1);
+    ti = static_cast<int>(h->timed % kTimingRing);
+    if (cudaEventRecord(h->ev0[ti], st) != cudaSuccess) return SV_ERR_CUDA;
+  }
+
+  if (h->cfg.dtype == SV_BF16) {
+    const sv::TcPlan &pl = h->plan;
+    if (h->tmW_ptr != W_lm) {
+      if (encode_2d(&h->tmW, W_lm, D.d, D.V, 64, sv::kTileM) != SV_OK) return SV_ERR_CUDA;
+      h->tmW_ptr = W_lm;
+    }
+    if (h->tmH_ptr != hidden) {
+      if (encode_2d(&h->tmH, hidden, D.d, D.R, 64, static_cast<uint32_t>(pl.h_box_rows)) != SV_OK)
+        return SV_ERR_CUDA;
+      h->tmH_ptr = hidden;
+    }
+    sv::TcParams P{};
+    P.dims = D;
+    P.w = h->w;
+    P.q_logits = q_logits;
+    P.inv_t = inv_t;
+    P.greedy = greedy ? 1 : 0;
+    P.npad = pl.npad;
+    P.nkb = pl.nkb;
+    P.stages = pl.stages;
+    P.stage_bytes = pl.stage_bytes;
+    P.h_boxes = pl.h_boxes;
+    P.h_box_rows = pl.h_box_rows;
+    P.nslot = pl.nslot;
+    P.tmem_cols = pl.tmem_cols;
+    P.wait_limit_ns = h->wait_limit_ns;
+    P.epoch = epoch;
+    e = sv::launch_tc(pl, P, h->tmW, h->tmH, st);
+  } else {
+    sv::SimtParams P{};
+    P.dims = D;
+    P.w = h->w;
+    P.H = static_cast<const float *>(hidden);
+    P.W = static_cast<const float *>(W_lm);
+    P.q_logits = q_logits;
+    P.inv_t = inv_t;
+    P.greedy = greedy ? 1 : 0;
+    e = sv::launch_simt(P, st);
+  }
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  if (ti >= 0) {
+    if (cudaEventRecord(h->ev1[ti], st) != cudaSuccess) return SV_ERR_CUDA;
+    ++h->timed;
+  }
+
+  sv::TailParams T{};
+  T.dims = D;
+  T.w = h->w;
+  T.H = hidden;
+  T.W = W_lm;
+  T.dtype = h->cfg.dtype;
+  T.draft = draft_tokens;
+  T.q_logits = q_logits;
+  T.u = uniforms;
+  T.T = static_cast<double>(temperature);
+  T.inv_t = inv_t;
+  T.greedy = greedy ? 1 : 0;
+  T.out_tokens = out_tokens;
+  T.out_n = out_n_accepted;
+  T.epoch = epoch;
+  T.split_cnt_n = h->num_sms * 4;
+  if (sv::launch_decide(T, st) != cudaSuccess) return SV_ERR_CUDA;
+  if (!greedy) {
+    if (sv::launch_residual(T, st) != cudaSuccess) return SV_ERR_CUDA;
+    if (sv::launch_select(T, st) != cudaSuccess) return SV_ERR_CUDA;
+  }
+  return SV_OK;
+}
+
+int spec_verify_status(spec_verify_t *h) {
+  if (!h) return SV_ERR_ARG;
+  if (cudaStreamSynchronize(h->stream) != cudaSuccess) return SV_ERR_CUDA;
+  int code = 0;
+  if (cudaMemcpy(&code, h->w.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (code != 0) {
+    // after a contraction gave up, split-tile counters may be half-used
+    if (cudaMemset(h->w.status, 0, sizeof(int)) != cudaSuccess ||
+        cudaMemset(h->w.split_cnt, 0, sizeof(int) * h->num_sms * 4) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+      return SV_ERR_CUDA;
+  }
+  return code;
+}
+
+int spec_verify_run_host(spec_verify_t *h, const void *hidden_host, const void *W_lm,
+                         const int32_t *draft_tokens_host, const float *q_logits_host,
+                         const float *uniforms_host, float temperature,
+                         int32_t *out_tokens_host, int32_t *out_n_accepted_host) {
+  if (!h || !hidden_host || !W_lm || !out_tokens_host || !out_n_accepted_host)
+    return SV_ERR_ARG;
+  const sv::Dims &D = h->dims;
+  const bool greedy = temperature == 0.0f;
+  if (D.K > 0 && !draft_tokens_host) return SV_ERR_ARG;
+  if (!greedy && ((D.K > 0 && !q_logits_host) || !uniforms_host)) return SV_ERR_ARG;
+  cudaStream_t st = h->stream;
+  const size_t es = esize(h->cfg.dtype);
+  if (cudaMemcpyAsync(h->st_hidden, hidden_host, static_cast<size_t>(D.R) * D.d * es,
+                      cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (D.K > 0 && cudaMemcpyAsync(h->st_draft, draft_tokens_host, sizeof(int32_t) * D.RQ,
+                                 cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (!greedy) {
+    if (D.K > 0 &&
+        cudaMemcpyAsync(h->st_q, q_logits_host, sizeof(float) * static_cast<size_t>(D.RQ) * D.V,
+                        cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return SV_ERR_CUDA;
+    if (cudaMemcpyAsync(h->st_u, uniforms_host, sizeof(float) * D.R, cudaMemcpyHostToDevice,
+                        st) != cudaSuccess)
+      return SV_ERR_CUDA;
+  }
+  int rc = spec_verify_run(h, h->st_hidden, W_lm, D.K > 0 ? h->st_draft : nullptr,
+                           greedy ? nullptr : h->st_q, greedy ? nullptr : h->st_u, temperature,
+                           h->st_tokens, h->st_n);
+  if (rc != SV_OK) return rc;
+  if (cudaMemcpyAsync(out_tokens_host, h->st_tokens, sizeof(int32_t) * D.R,
+                      cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(out_n_accepted_host, h->st_n, sizeof(int32_t) * D.B,
+                      cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SV_ERR_CUDA;
+  int code = 0;
+  if (cudaMemcpy(&code, h->w.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return code == 0 ? SV_OK : spec_verify_status(h);
+}
+
+int spec_verify_debug_logits(spec_verify_t *h, float *dst) {
+  if (!h || !dst) return SV_ERR_ARG;
+  if (cudaStreamSynchronize(h->stream) != cudaSuccess) return SV_ERR_CUDA;
+  const size_t n = static_cast<size_t>(h->dims.R) * h->dims.V;
+  return cudaMemcpy(dst, h->w.logits, n * sizeof(float), cudaMemcpyDefault) == cudaSuccess
+             ? SV_OK
+             : SV_ERR_CUDA;
+}
+
+int spec_verify_debug_lse(spec_verify_t *h, double *dst) {
+  if (!h || !dst) return SV_ERR_ARG;
+  if (cudaStreamSynchronize(h->stream) != cudaSuccess) return SV_ERR_CUDA;
+  const size_t n = static_cast<size_t>(h->dims.R + h->dims.RQ);
+  return cudaMemcpy(dst, h->w.lse, n * sizeof(double), cudaMemcpyDefault) == cudaSuccess
+             ? SV_OK
+             : SV_ERR_CUDA;
+}
+
+int spec_verify_timing(spec_verify_t *h, int enable) {
+  if (!h) return SV_ERR_ARG;
+  if (enable && h->ev0.empty()) {
+    h->ev0.resize(kTimingRing);
+    h->ev1.resize(kTimingRing);
+    for (int i = 0; i < kTimingRing; ++i)
+      if (cudaEventCreate(&h->ev0[i]) != cudaSuccess || cudaEventCreate(&h->ev1[i]) != cudaSuccess)
+        return SV_ERR_CUDA;
+  }
+  if (h->timing) fold_timing(h, h->timed);
+  h->timing = enable != 0;
+  h->timed = 0;
+  h->folded = 0;
+  h->timed_ms = 0.0;
+  return SV_OK;
+}
+
+int spec_verify_timing_read(spec_verify_t *h, double *total_ms, int64_t *launches) {
+  if (!h || !total_ms || !launches) return SV_ERR_ARG;
+  if (h->timed > 0) fold_timing(h, h->timed);
+  *total_ms = h->timed_ms;
+  *launches = h->timed;
+  return SV_OK;
+}
+
+}  // extern "C"

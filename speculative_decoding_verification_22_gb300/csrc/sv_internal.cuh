@@ -1,0 +1,290 @@
+// sv_internal.cuh -- definitions shared by the kernels of the verify step:
+// workspace layout, status handling, bounded waits, and thin inline-PTX
+// wrappers for mbarrier, TMA (cp.async.bulk.tensor) and tcgen05 (Blackwell
+// tensor cores with TMEM accumulators) on sm_103a.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/spec_verify.h"
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// Problem geometry
+// ---------------------------------------------------------------------------
+constexpr int kSub = 32;        // vocab entries per softmax partial (one warp)
+constexpr int kTileM = 128;     // vocab rows per tensor-core tile (MMA M)
+constexpr int kChunk = 2048;    // vocab entries per residual-mass chunk
+constexpr int kTailThreads = 256;
+constexpr int kChunkPerThread = kChunk / kTailThreads;  // 8
+
+// Per-sequence state handed from the decision pass to the residual and
+// selection passes.
+enum : int { kModeSkip = 0, kModeResidual = 1, kModeP = 2 };
+
+struct SeqState {
+  int mode;      // kModeSkip: nothing to draw (greedy, invalid, error)
+  int p_row;     // logits row of the final draw
+  int q_row;     // q_logits row (kModeResidual)
+  int n_acc;     // accepted draft tokens
+  float p_max;   // p(v) = expf(L[v] * inv_t - p_max) * p_corr
+  float p_corr;
+  float q_max;   // q(v) = expf(ql[v] * inv_t - q_max) * q_corr
+  float q_corr;
+  float u_final; // the final uniform
+  int pad[3];
+};
+
+struct Dims {
+  int64_t V, d;
+  int B, K;
+  int R;        // B * (K + 1) target rows
+  int RQ;       // B * K draft rows
+  int nsub;     // ceil(V / 32)
+  int ntile;    // ceil(V / 128)
+  int nchunk;   // ceil(V / 2048)
+};
+
+// Device workspace (owned by the handle).
+struct Work {
+  float *logits;       // [R, V]
+  float2 *part_p;      // [R, nsub]   (max, sum-exp) of logits / T; T == 0: (max, 0)
+  float2 *part_q;      // [RQ, nsub]  (max, sum-exp) of q_logits / T
+  double *lse;         // [R + RQ]    normalisers (debug copy)
+  SeqState *seq;       // [B]
+  double *chunk_mass;  // [B, nchunk]
+  float *split_buf;    // [grid, 2, 128 * npad]  partial tiles (tensor-core path)
+  int *split_cnt;      // [grid, 4]
+  int *status;         // [1]   first device-side error since last read
+  unsigned *abort_epoch;  // [1] epoch of the last run whose contraction gave up
+};
+
+// ---------------------------------------------------------------------------
+// Status word: the first device-side error wins.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_status(int *status, int code) {
+  atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits until the phase with the given parity has completed.  Gives up
+// (returns false) after limit_ns nanoseconds or as soon as *abort is set.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns,
+                                          const volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 >= limit_ns) return false;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m))
+               : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// 2-D tiled load of box {c0 .. c0+box0, c1 .. c1+box1} into shared memory,
+// completing `bar` with the box's byte count.  c0 (innermost) must be a
+// multiple of 16 bytes' worth of elements.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m,
+                                            int32_t c0, int32_t c1, uint32_t bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (TMEM + tensor cores), cta_group::1
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 in, fp32 out).
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc,
+                                          uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives once on `bar` when all tcgen05.mma issued so far by this thread
+// have completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          bar)
+      : "memory");
+}
+// 32 lanes x 16 consecutive fp32 columns: thread i of the warp receives lane
+// (quadrant base + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand written by TMA with
+// 128-byte swizzling: rows of 128 bytes (64 bf16), 8-row groups 1024 bytes
+// apart (stride byte offset), leading byte offset unused (1), descriptor
+// version 1 (bit 46), swizzle mode 2 = 128B (bits 61-63).  The buffer must be
+// 1024-byte aligned; the k-th 16-element slice starts 32*k bytes further.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
+  uint64_t desc = 0;
+  desc |= static_cast<uint64_t>((smem_addr & 0x3FFFF) >> 4);
+  desc |= static_cast<uint64_t>(1) << 16;
+  desc |= static_cast<uint64_t>(1024 >> 4) << 32;
+  desc |= static_cast<uint64_t>(1) << 46;
+  desc |= static_cast<uint64_t>(2) << 61;
+  return desc;
+}
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bits 17-22, M >> 4 at
+// bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) |
+         (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// Warp reductions
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+__device__ __forceinline__ double warp_sum_d(double x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// (max, sum-exp) partial of one 32-entry vocab subtile held one entry per
+// lane.  `valid` masks entries past V.  T == 0 (greedy) keeps only the max.
+// All lanes return the result.
+__device__ __forceinline__ float2 subtile_partial(float logit, bool valid, float inv_t,
+                                                  bool greedy) {
+  if (greedy) {
+    const float m = warp_max(valid ? logit : -INFINITY);
+    return make_float2(m, 0.0f);
+  }
+  const float a = valid ? logit * inv_t : -INFINITY;
+  const float m = warp_max(a);
+  const float e = valid ? expf(a - m) : 0.0f;
+  return make_float2(m, warp_sum(e));
+}
+
+// Error-free sum of two floats (Knuth's TwoSum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+  s = a + b;
+  const float bp = s - a;
+  e = (a - (s - bp)) + (b - bp);
+}
+
+}  // namespace sv

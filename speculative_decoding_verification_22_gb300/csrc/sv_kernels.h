@@ -1,0 +1,77 @@
+// sv_kernels.h -- launch interfaces of the kernels of the verify step
+// (host side of the library; see sv_api.cu for the C ABI).
+#pragma once
+
+#include "sv_internal.cuh"
+
+namespace sv {
+
+// ---- (a) LM-head contraction, bf16 tensor-core path -----------------------
+struct TcParams {
+  Dims dims;
+  Work w;
+  const float *q_logits;   // [RQ, V]
+  float inv_t;             // 1/T (T > 0); unused for greedy
+  int greedy;              // T == 0
+  int npad;                // MMA N = R rounded up to 16
+  int nkb;                 // 64-wide k blocks per tile
+  int stages;              // shared-memory ring depth
+  int stage_bytes;         // W slab + H slab, multiple of 1024
+  int h_boxes;             // TMA boxes per H slab (1 or 2)
+  int h_box_rows;          // rows per H box
+  int nslot;               // direct mode: TMEM accumulators per tile
+  uint32_t tmem_cols;      // TMEM columns allocated per CTA
+  uint64_t wait_limit_ns;  // bound of every device-side wait
+  unsigned epoch;          // run counter (stamps an abort)
+};
+
+struct TcPlan {
+  int npad, ncol, nkb, stage_bytes, stages, smem, h_boxes, h_box_rows, nslot;
+  uint32_t tmem_cols;
+  int grid, threads;
+  bool valid;
+};
+
+TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin);
+cudaError_t launch_tc(const TcPlan &pl, const TcParams &P, const CUtensorMap &tmW,
+                      const CUtensorMap &tmH, cudaStream_t stream);
+
+// ---- (a) LM-head contraction, fp32 SIMT path -----------------------------
+struct SimtParams {
+  Dims dims;
+  Work w;
+  const float *H;          // [R, d]
+  const float *W;          // [V, d]
+  const float *q_logits;   // [RQ, V]
+  float inv_t;
+  int greedy;
+};
+cudaError_t launch_simt(const SimtParams &P, cudaStream_t stream);
+
+// ---- (b) decision, residual and (c) selection passes ---------------------
+struct TailParams {
+  Dims dims;
+  Work w;
+  const void *H;           // [R, d] bf16 or fp32
+  const void *W;           // [V, d] bf16 or fp32
+  int dtype;               // SV_BF16 / SV_FP32
+  const int32_t *draft;    // [B, K]
+  const float *q_logits;   // [RQ, V]
+  const float *u;          // [B, K+1]
+  double T;
+  float inv_t;
+  int greedy;
+  int32_t *out_tokens;     // [B, K+1]
+  int32_t *out_n;          // [B]
+  unsigned epoch;          // run counter
+  int split_cnt_n;         // entries of w.split_cnt
+};
+cudaError_t launch_decide(const TailParams &P, cudaStream_t stream);
+cudaError_t launch_residual(const TailParams &P, cudaStream_t stream);
+cudaError_t launch_select(const TailParams &P, cudaStream_t stream);
+
+// cudaLaunchKernelEx with programmatic stream serialisation (PDL).
+cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, void **args);
+
+}  // namespace sv

@@ -1,0 +1,515 @@
+// sv_lmhead_tc.cu -- kernel (a) of the verify step, bf16 path: the
+// weight-streaming skinny contraction L = H * W^T on Blackwell tensor cores.
+//
+// The verify pass multiplies the [positions x d] block of final hidden
+// states against the LM-head matrix, which is read from memory once
+// ("What Actually Happens During Speculative Decoding in LLMs", memory-bound
+// section; "Speculative Decoding: Guess Several Tokens, Check Them in One
+// Pass", Step 1).  With R = B*(K+1) rows (5..384) the step is HBM-bound, so
+// the kernel is built around streaming W exactly once:
+//
+//  * swap-AB: the vocabulary is the MMA M dimension (128 W rows per tile)
+//    and the R hidden rows, padded to npad (multiple of 16), are N;
+//  * persistent grid, one CTA per SM, stream-K split of the
+//    (tile, 64-wide k block) units so every SM streams the same number of
+//    bytes; a tile cut between two CTAs is finished by whichever CTA
+//    completes its part second;
+//  * warp 0 issues TMA loads (128B swizzle, W evict-first in L2) into a
+//    ring of shared-memory stages; warp 1 issues tcgen05.mma (kind::f16,
+//    M=128, K=16) into TMEM; warps 2..5 drain TMEM and run the epilogue;
+//  * drain mode (npad <= 64): every k block accumulates into its own TMEM
+//    slot of a ring and the epilogue adds it into fp32 registers with Kahan
+//    compensation, so no long tensor-core accumulation chain can bias the
+//    logits; direct mode (npad > 64): up to four TMEM accumulators per tile
+//    (contiguous k ranges) summed in registers;
+//  * the epilogue writes the fp32 logits, the per-32-entry (max, sum-exp)
+//    partials of logits / T (or the max for T == 0), and the same partials
+//    of the draft logits q / T for the tile, which it streams alongside.
+#include "sv_internal.cuh"
+#include "sv_kernels.h"
+
+namespace sv {
+namespace tc {
+
+constexpr int kBK = 64;                            // k per stage (128 bytes)
+constexpr int kWSlabBytes = kTileM * kBK * 2;      // 16 KB
+constexpr int kMaxStages = 12;
+constexpr int kNumEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kNumEpiWarps;   // 192
+constexpr int kDrainSlots = 8;
+constexpr uint64_t kCleanupLimitNs = 2000000000ull;
+
+struct Ctl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t tfull[kDrainSlots];
+  uint64_t tempty[kDrainSlots];
+  uint64_t teardown;
+  uint32_t tmem_base;
+  int abort_flag;
+  int issued;
+  int consumed;
+};
+
+__device__ __forceinline__ void tile_range(int t, int64_t u0, int64_t u1, int nkb,
+                                           int &kb0, int &kb1) {
+  const int64_t tb = static_cast<int64_t>(t) * nkb;
+  kb0 = static_cast<int>((u0 > tb ? u0 : tb) - tb);
+  kb1 = static_cast<int>((u1 < tb + nkb ? u1 : tb + nkb) - tb);
+}
+
+__device__ __forceinline__ void raise_abort(Ctl *ctl, const TcParams &P) {
+  *reinterpret_cast<volatile int *>(&ctl->abort_flag) = 1;
+  set_status(P.w.status, SV_ERR_TIMEOUT);
+  atomicExch(P.w.abort_epoch, P.epoch);
+}
+
+// Streams the draft logits of one 32-entry subtile for every draft row and
+// writes their (max, sum-exp) partials of q / T.
+__device__ __forceinline__ void q_partials(const TcParams &P, int64_t v, bool valid,
+                                           int sub, int lane) {
+  const int RQ = P.dims.RQ;
+  const int64_t V = P.dims.V;
+  for (int r0 = 0; r0 < RQ; r0 += 8) {
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      x[j] = (r0 + j < RQ && valid) ? P.q_logits[static_cast<int64_t>(r0 + j) * V + v] : 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (r0 + j < RQ) {
+        const float2 pm = subtile_partial(x[j], valid, P.inv_t, false);
+        if (lane == 0 && sub < P.dims.nsub)
+          P.w.part_q[static_cast<int64_t>(r0 + j) * P.dims.nsub + sub] = pm;
+      }
+    }
+  }
+}
+
+// Writes logits and target partials for columns n0 .. n0+15 of a finished
+// tile (this thread holds vocab entry v).
+__device__ __forceinline__ void finish_group(const TcParams &P, const float (&x)[16], int n0,
+                                             int64_t v, bool valid, int sub, int lane) {
+  const int64_t V = P.dims.V;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int n = n0 + i;
+    if (n < P.dims.R) {
+      if (valid) P.w.logits[static_cast<int64_t>(n) * V + v] = x[i];
+      const float2 pm = subtile_partial(x[i], valid, P.inv_t, P.greedy != 0);
+      if (lane == 0 && sub < P.dims.nsub)  // the last tile may end inside a subtile row
+        P.w.part_p[static_cast<int64_t>(n) * P.dims.nsub + sub] = pm;
+    }
+  }
+}
+
+// Split-tile hand-off, per warp (each warp owns 32 vocab rows of the tile and
+// has its own counter, so no cross-warp barrier is needed): publish this
+// CTA's part and learn whether the other part is already there.  Returns
+// true (on every lane) if this warp must finish its rows of the tile.
+__device__ __forceinline__ bool split_publish(const TcParams &P, int bidx, int quad,
+                                              int lane) {
+  __threadfence();
+  __syncwarp();
+  int flag = 0;
+  if (lane == 0) flag = atomicAdd(&P.w.split_cnt[bidx * 4 + quad], 1);
+  flag = __shfl_sync(0xffffffffu, flag, 0);
+  if (flag != 0) __threadfence();
+  return flag != 0;
+}
+
+__device__ __forceinline__ void split_reset(const TcParams &P, int bidx, int quad, int lane) {
+  if (lane == 0) P.w.split_cnt[bidx * 4 + quad] = 0;
+}
+
+template <int NCOL>
+__global__ void __launch_bounds__(kThreads, 1)
+    lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmW,
+                     const __grid_constant__ CUtensorMap tmH, const TcParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  Ctl *ctl = reinterpret_cast<Ctl *>(smem_raw + (base - raw) +
+                                     static_cast<uint32_t>(P.stages * P.stage_bytes));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int nkb = P.nkb;
+  const int64_t U = static_cast<int64_t>(P.dims.ntile) * nkb;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int64_t u0 = U * c / G, u1 = U * (c + 1) / G;
+  const int t_first = static_cast<int>(u0 / nkb);
+  const int t_last = static_cast<int>((u1 - 1) / nkb);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P.stages; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int s = 0; s < kDrainSlots; ++s) {
+      mbar_init(smem_u32(&ctl->tfull[s]), 1);
+      mbar_init(smem_u32(&ctl->tempty[s]), kNumEpiWarps);
+    }
+    mbar_init(smem_u32(&ctl->teardown), 1);
+    ctl->abort_flag = 0;
+    ctl->issued = 0;
+    ctl->consumed = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmH);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), P.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const volatile int *abort = &ctl->abort_flag;
+
+  // Everything above only touched this CTA's own resources; inputs written
+  // by earlier work in the stream are visible after this point.
+  pdl_wait();
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_h = policy_evict_last();
+      const uint32_t tx = static_cast<uint32_t>(kWSlabBytes + P.npad * 128);
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      for (int t = t_first; t <= t_last; ++t) {
+        int kb0, kb1;
+        tile_range(t, u0, u1, nkb, kb0, kb1);
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(smem_u32(&ctl->empty[stage]), phase ^ 1u, P.wait_limit_ns, abort)) {
+            raise_abort(ctl, P);
+            ok = false;
+            break;
+          }
+          const uint32_t sbase = base + static_cast<uint32_t>(stage * P.stage_bytes);
+          const uint32_t full = smem_u32(&ctl->full[stage]);
+          mbar_arrive_expect_tx(full, tx);
+          tma_load_2d(sbase, &tmW, kb * kBK, t * kTileM, full, pol_w);
+          for (int hb = 0; hb < P.h_boxes; ++hb)
+            tma_load_2d(sbase + kWSlabBytes + static_cast<uint32_t>(hb * P.h_box_rows * 128),
+                        &tmH, kb * kBK, hb * P.h_box_rows, full, pol_h);
+          ++issued;
+          if (++stage == P.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      ctl->issued = issued;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int stage = 0, consumed = 0;
+      uint32_t sphase = 0;
+      int slot = 0;
+      uint32_t tphase = 0;
+      bool ok = true;
+      for (int t = t_first; t <= t_last && ok; ++t) {
+        int kb0, kb1;
+        tile_range(t, u0, u1, nkb, kb0, kb1);
+        if constexpr (NCOL == 0) {
+          if (!mbar_wait(smem_u32(&ctl->tempty[0]), tphase ^ 1u, P.wait_limit_ns, abort)) {
+            raise_abort(ctl, P);
+            break;
+          }
+          tc_fence_after();
+        }
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if constexpr (NCOL != 0) {
+            if (!mbar_wait(smem_u32(&ctl->tempty[slot]), tphase ^ 1u, P.wait_limit_ns, abort)) {
+              raise_abort(ctl, P);
+              ok = false;
+              break;
+            }
+          }
+          if (!mbar_wait(smem_u32(&ctl->full[stage]), sphase, P.wait_limit_ns, abort)) {
+            raise_abort(ctl, P);
+            ok = false;
+            break;
+          }
+          ++consumed;
+          tc_fence_after();
+          const uint32_t sbase = base + static_cast<uint32_t>(stage * P.stage_bytes);
+          const uint64_t adesc = sw128_desc(sbase);
+          const uint64_t bdesc = sw128_desc(sbase + kWSlabBytes);
+          if constexpr (NCOL != 0) {
+            const uint32_t d = tmem + static_cast<uint32_t>(slot * NCOL);
+            const uint32_t idesc = idesc_bf16(kTileM, P.npad);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              umma_bf16(d, adesc + 2u * k, bdesc + 2u * k, idesc, k > 0 ? 1u : 0u);
+          } else {
+            const int s = static_cast<int>(static_cast<int64_t>(kb) * P.nslot / nkb);
+            const bool first =
+                kb == kb0 || static_cast<int>(static_cast<int64_t>(kb - 1) * P.nslot / nkb) != s;
+            const uint32_t d = tmem + static_cast<uint32_t>(s * P.npad);
+            const int n1 = P.npad <= 256 ? P.npad : 256;
+            const uint32_t idesc1 = idesc_bf16(kTileM, n1);
+            const uint32_t idesc2 = idesc_bf16(kTileM, P.npad > 256 ? P.npad - 256 : 16);
+            const uint64_t bdesc2 = sw128_desc(sbase + kWSlabBytes + 256u * 128u);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint32_t acc = (k > 0 || !first) ? 1u : 0u;
+              umma_bf16(d, adesc + 2u * k, bdesc + 2u * k, idesc1, acc);
+              if (P.npad > 256) umma_bf16(d + 256u, adesc + 2u * k, bdesc2 + 2u * k, idesc2, acc);
+            }
+          }
+          umma_commit(smem_u32(&ctl->empty[stage]));
+          if constexpr (NCOL != 0) {
+            umma_commit(smem_u32(&ctl->tfull[slot]));
+            if (++slot == kDrainSlots) {
+              slot = 0;
+              tphase ^= 1u;
+            }
+          }
+          if (++stage == P.stages) {
+            stage = 0;
+            sphase ^= 1u;
+          }
+        }
+        if constexpr (NCOL == 0) {
+          if (ok) {
+            umma_commit(smem_u32(&ctl->tfull[0]));
+            tphase ^= 1u;
+          }
+        }
+      }
+      ctl->consumed = consumed;
+      // every MMA issued by this thread must finish before TMEM is freed
+      umma_commit(smem_u32(&ctl->teardown));
+      const int never = 0;
+      mbar_wait(smem_u32(&ctl->teardown), 0u, kCleanupLimitNs, &never);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps ----------------
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    int slot = 0;
+    uint32_t tphase = 0;
+    for (int t = t_first; t <= t_last; ++t) {
+      int kb0, kb1;
+      tile_range(t, u0, u1, nkb, kb0, kb1);
+      const int64_t v = static_cast<int64_t>(t) * kTileM + row_in_tile;
+      const bool valid = v < P.dims.V;
+      const int sub = t * (kTileM / kSub) + quad;
+      if (!P.greedy && kb0 == 0 && P.dims.RQ > 0) q_partials(P, v, valid, sub, lane);
+      const bool split = kb0 != 0 || kb1 != nkb;
+      const int bidx = kb0 == 0 ? c : c - 1;
+      const int part = kb0 == 0 ? 0 : 1;
+      float *mine = P.w.split_buf + (static_cast<int64_t>(bidx) * 2 + part) * (kTileM * P.npad);
+      float *other =
+          P.w.split_buf + (static_cast<int64_t>(bidx) * 2 + (1 - part)) * (kTileM * P.npad);
+
+      if constexpr (NCOL != 0) {
+        float acc[NCOL], cmp[NCOL];
+#pragma unroll
+        for (int n = 0; n < NCOL; ++n) {
+          acc[n] = 0.0f;
+          cmp[n] = 0.0f;
+        }
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->tfull[slot]), tphase,
+                                                 P.wait_limit_ns, abort))) {
+            if (lane == 0) raise_abort(ctl, P);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int g = 0; g < NCOL / 16; ++g) {
+            float x[16];
+            tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(slot * NCOL + g * 16), x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {  // Kahan: acc + x with carried error
+              const float y = x[i] - cmp[g * 16 + i];
+              const float s = acc[g * 16 + i] + y;
+              cmp[g * 16 + i] = (s - acc[g * 16 + i]) - y;
+              acc[g * 16 + i] = s;
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[slot]));
+          if (++slot == kDrainSlots) {
+            slot = 0;
+            tphase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        float val[NCOL];
+#pragma unroll
+        for (int n = 0; n < NCOL; ++n) val[n] = acc[n] - cmp[n];
+        if (split) {
+#pragma unroll
+          for (int n = 0; n < NCOL; ++n)
+            if (n < P.npad) mine[n * kTileM + row_in_tile] = val[n];
+          if (!split_publish(P, bidx, quad, lane)) continue;
+#pragma unroll
+          for (int n = 0; n < NCOL; ++n)
+            if (n < P.npad) val[n] = val[n] + __ldcg(&other[n * kTileM + row_in_tile]);
+          split_reset(P, bidx, quad, lane);
+        }
+#pragma unroll
+        for (int g = 0; g < NCOL / 16; ++g) {
+          float x[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[i] = val[g * 16 + i];
+          finish_group(P, x, g * 16, v, valid, sub, lane);
+        }
+      } else {
+        // direct mode: sum the tile's accumulators column group by group
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->tfull[0]), tphase,
+                                               P.wait_limit_ns, abort))) {
+          if (lane == 0) raise_abort(ctl, P);
+          break;
+        }
+        tc_fence_after();
+        const int s_lo = static_cast<int>(static_cast<int64_t>(kb0) * P.nslot / nkb);
+        const int s_hi = static_cast<int>(static_cast<int64_t>(kb1 - 1) * P.nslot / nkb);
+        for (int g = 0; g < P.npad / 16; ++g) {
+          float x[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[i] = 0.0f;
+          for (int s = s_lo; s <= s_hi; ++s) {
+            float y[16];
+            tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(s * P.npad + g * 16), y);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] += y[i];
+          }
+          if (split) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mine[(g * 16 + i) * kTileM + row_in_tile] = x[i];
+          } else {
+            finish_group(P, x, g * 16, v, valid, sub, lane);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[0]));
+        tphase ^= 1u;
+        if (split) {
+          if (!split_publish(P, bidx, quad, lane)) continue;
+          for (int g = 0; g < P.npad / 16; ++g) {
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int idx = (g * 16 + i) * kTileM + row_in_tile;
+              x[i] = __ldcg(&mine[idx]) + __ldcg(&other[idx]);
+            }
+            finish_group(P, x, g * 16, v, valid, sub, lane);
+          }
+          split_reset(P, bidx, quad, lane);
+        }
+      }
+    }
+  }
+
+  // ---------------- teardown ----------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0) {
+    // only after an abort can loads still be in flight: wait for them so
+    // no copy lands in shared memory after this CTA has exited
+    const int never = 0;
+    for (int i = ctl->consumed; i < ctl->issued; ++i)
+      mbar_wait(smem_u32(&ctl->full[i % P.stages]),
+                static_cast<uint32_t>((i / P.stages) & 1), kCleanupLimitNs, &never);
+  }
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, P.tmem_cols);
+  }
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin) {
+  TcPlan pl{};
+  pl.npad = ((dims.R + 15) / 16) * 16;
+  pl.ncol = pl.npad <= 16 ? 16 : pl.npad <= 32 ? 32 : pl.npad <= 64 ? 64 : 0;
+  pl.nkb = static_cast<int>((dims.d + tc::kBK - 1) / tc::kBK);
+  pl.stage_bytes = ((tc::kWSlabBytes + pl.npad * 128 + 1023) / 1024) * 1024;
+  const int ctl_bytes = static_cast<int>(sizeof(tc::Ctl));
+  int stages = (smem_optin - 1024 - ctl_bytes) / pl.stage_bytes;
+  if (stages > tc::kMaxStages) stages = tc::kMaxStages;
+  pl.stages = stages;
+  pl.smem = stages * pl.stage_bytes + ctl_bytes + 1024;
+  // above half of the SM's shared memory: exactly one CTA per SM, so the
+  // TMEM allocation below can never wait on another CTA
+  if (pl.smem < 120 * 1024) pl.smem = 120 * 1024;
+  pl.h_boxes = pl.npad <= 256 ? 1 : 2;
+  pl.h_box_rows = pl.npad <= 256 ? pl.npad : pl.npad / 2;
+  if (pl.ncol != 0) {
+    pl.nslot = 1;
+    pl.tmem_cols = static_cast<uint32_t>(tc::kDrainSlots * pl.ncol);
+  } else {
+    // contiguous k ranges, one per accumulator; never more accumulators
+    // than k blocks, so every accumulator of a tile range receives a block
+    int ns = 512 / pl.npad;
+    ns = ns < 1 ? 1 : (ns > 4 ? 4 : ns);
+    pl.nslot = ns < pl.nkb ? ns : pl.nkb;
+    pl.tmem_cols = 512;
+  }
+  pl.grid = dims.ntile < num_sms ? dims.ntile : num_sms;
+  pl.threads = tc::kThreads;
+  pl.valid = stages >= 2 && pl.npad <= SV_MAX_ROWS_BF16;
+  return pl;
+}
+
+static int g_attr_smem[4] = {0, 0, 0, 0};
+
+cudaError_t launch_tc(const TcPlan &pl, const TcParams &P, const CUtensorMap &tmW,
+                      const CUtensorMap &tmH, cudaStream_t stream) {
+  const void *fn;
+  int which;
+  switch (pl.ncol) {
+    case 16: fn = reinterpret_cast<const void *>(&tc::lmhead_tc_kernel<16>); which = 0; break;
+    case 32: fn = reinterpret_cast<const void *>(&tc::lmhead_tc_kernel<32>); which = 1; break;
+    case 64: fn = reinterpret_cast<const void *>(&tc::lmhead_tc_kernel<64>); which = 2; break;
+    default: fn = reinterpret_cast<const void *>(&tc::lmhead_tc_kernel<0>); which = 3; break;
+  }
+  if (g_attr_smem[which] < pl.smem) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
+    if (e != cudaSuccess) return e;
+    g_attr_smem[which] = pl.smem;
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.grid);
+  cfg.blockDim = dim3(pl.threads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void *args[] = {const_cast<CUtensorMap *>(&tmW), const_cast<CUtensorMap *>(&tmH),
+                  const_cast<TcParams *>(&P)};
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace sv

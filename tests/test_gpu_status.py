@@ -1,0 +1,105 @@
+"""GPU error paths: every failure is reported through a return code or the
+device status word, the context stays usable, and later runs are correct.
+No test here faults, traps or hangs the GPU: the timeout test sets the
+device-side wait limit to zero, so the first wait that is not already
+satisfied gives up at once and the kernel returns after draining its own
+copies in flight."""
+import numpy as np
+import pytest
+import torch
+
+import spec_inputs as si
+import speculative_decoding_verification_22_gb300 as sv
+from gpu_common import compare_tokens, gpu_verify, oracle_verify
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def setup():
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    wl = si.workload("tiny", dtype="bf16", B=3, K=4, V=3000, d=512, w_std=1 / 22.6)
+    W = si.make_weights(wl, seed=5, device=dev)
+    inp = si.make_round(wl, W, seed=6)
+    eng = sv.SpecVerify(wl.V, wl.d, wl.B, wl.K, wl.dtype, device=dev)
+    yield dev, wl, W, si.to_oracle(W), inp, eng
+    eng.close()
+
+
+def _check_ok(eng, W, W_np, inp, T=1.0):
+    got = gpu_verify(eng, W, inp, T)
+    assert got["status"] == sv.SV_OK
+    ref = oracle_verify(inp["hidden"], W_np, inp["draft"], inp["q_logits"], inp["uniforms"], T)
+    assert compare_tokens(got, ref, T)[0] == 0
+
+
+def test_out_of_range_draft_token(setup):
+    dev, wl, W, W_np, inp, eng = setup
+    bad = dict(inp)
+    bad["draft"] = inp["draft"].clone()
+    bad["draft"][1, 2] = wl.V          # sequence 1 invalid
+    got = gpu_verify(eng, W, bad, 1.0)
+    assert got["status"] == sv.SV_ERR_TOKEN
+    assert got["n_accepted"][1] == -1 and np.all(got["tokens"][1] == -1)
+    ref = oracle_verify(bad["hidden"], W_np, bad["draft"], bad["q_logits"], bad["uniforms"], 1.0)
+    assert ref["n_accepted"][1] == -1
+    for b in (0, 2):
+        assert np.array_equal(got["tokens"][b], ref["tokens"][b])
+    _check_ok(eng, W, W_np, inp)
+
+
+def test_misaligned_and_bad_arguments_are_rejected_on_the_host(setup):
+    dev, wl, W, W_np, inp, eng = setup
+    out_t = torch.empty((wl.B, wl.K + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((wl.B,), dtype=torch.int32, device=dev)
+    q_off = torch.empty(inp["q_logits"].numel() + 1, device=dev)[1:].view_as(inp["q_logits"])
+    with pytest.raises(sv.SpecVerifyError) as e:
+        sv.spec_verify_run(eng.h, inp["hidden"], W, inp["draft"], q_off, inp["uniforms"],
+                           1.0, out_t, out_n)
+    assert e.value.code == sv.SV_ERR_ALIGN
+    for T in (float("nan"), -1.0, float("inf")):
+        with pytest.raises(sv.SpecVerifyError) as e:
+            sv.spec_verify_run(eng.h, inp["hidden"], W, inp["draft"], inp["q_logits"],
+                               inp["uniforms"], T, out_t, out_n)
+        assert e.value.code == sv.SV_ERR_ARG
+    with pytest.raises(sv.SpecVerifyError) as e:
+        sv.spec_verify_run(eng.h, inp["hidden"], W, inp["draft"], None, inp["uniforms"],
+                           1.0, out_t, out_n)
+    assert e.value.code == sv.SV_ERR_ARG
+    assert eng.status() == sv.SV_OK
+    _check_ok(eng, W, W_np, inp)
+
+
+def test_non_finite_weights_are_reported(setup):
+    dev, wl, W, W_np, inp, eng = setup
+    Wbad = W.clone()
+    Wbad[17, 3] = float("inf")
+    for T in (1.0, 0.0):
+        got = gpu_verify(eng, Wbad, inp, T)
+        assert got["status"] == sv.SV_ERR_NONFINITE
+        assert np.all(got["n_accepted"] == -1)
+    _check_ok(eng, W, W_np, inp)
+
+
+def test_wait_limit_zero_times_out_and_recovers(setup):
+    dev, wl, W, W_np, inp, eng = setup
+    sv.spec_verify_set_wait_limit(eng.h, 0)
+    got = gpu_verify(eng, W, inp, 1.0)
+    assert got["status"] == sv.SV_ERR_TIMEOUT
+    assert np.all(got["n_accepted"] == -1) and np.all(got["tokens"] == -1)
+    sv.spec_verify_set_wait_limit(eng.h, 1_000_000_000)
+    for _ in range(3):
+        _check_ok(eng, W, W_np, inp)
+
+
+def test_run_host_matches_device_run(setup):
+    dev, wl, W, W_np, inp, eng = setup
+    tok_d, n_d = eng.run(inp["hidden"], W, inp["draft"], inp["q_logits"], inp["uniforms"], 1.0)
+    host = {k: inp[k].cpu().pin_memory() for k in ("hidden", "draft", "q_logits", "uniforms")}
+    ht = torch.empty((wl.B, wl.K + 1), dtype=torch.int32).pin_memory()
+    hn = torch.empty((wl.B,), dtype=torch.int32).pin_memory()
+    sv.spec_verify_run_host(eng.h, host["hidden"], W, host["draft"], host["q_logits"],
+                            host["uniforms"], 1.0, ht, hn)
+    assert torch.equal(ht, tok_d.cpu()) and torch.equal(hn, n_d.cpu())
+    assert eng.status() == sv.SV_OK

@@ -1,0 +1,129 @@
+"""CPU-only checks: the C-ABI library loads and exports every symbol its
+header declares, host-side argument checks reject bad configurations before
+touching CUDA, and the benchmark's host logic (byte counts, clock parsing,
+multi-rank aggregation over gloo) is right."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bench
+import speculative_decoding_verification_22_gb300 as sv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_symbols():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if fn.endswith(".h"):
+            text = open(os.path.join(inc, fn)).read()
+            names.update(re.findall(r"^[\w\s\*]*?\b(spec_verify_\w+)\s*\(", text, re.M))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_22_gb300 import build as b
+    b.build()
+    return sv.load_library()
+
+
+def test_library_exports_every_header_symbol(lib):
+    names = header_symbols()
+    assert len(names) >= 13
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing
+    assert set(names) == set(sv.EXPORTS)
+
+
+def test_strerror_covers_every_code(lib):
+    for code in range(0, -9, -1):
+        assert sv.spec_verify_strerror(code) != "unknown error"
+    assert sv.spec_verify_strerror(-99) == "unknown error"
+
+
+@pytest.mark.parametrize("cfg,want", [
+    (dict(V=0, d=4096, B=1, K=4, dtype=0), sv.SV_ERR_SHAPE),
+    (dict(V=128256, d=4095, B=1, K=4, dtype=0), sv.SV_ERR_SHAPE),   # d % 8
+    (dict(V=128256, d=4096, B=0, K=4, dtype=0), sv.SV_ERR_SHAPE),
+    (dict(V=128256, d=4096, B=1, K=17, dtype=0), sv.SV_ERR_SHAPE),  # K > 16
+    (dict(V=128256, d=4096, B=65, K=5, dtype=0), sv.SV_ERR_SHAPE),  # 390 rows
+    (dict(V=1000, d=256, B=1, K=4, dtype=7), sv.SV_ERR_ARG),
+    (dict(V=1000, d=6, B=1, K=4, dtype=1), sv.SV_ERR_SHAPE),        # d % 4
+])
+def test_create_rejects_bad_configurations_before_cuda(lib, cfg, want):
+    c = sv.sv_config_t(cfg["V"], cfg["d"], cfg["B"], cfg["K"], cfg["dtype"], None)
+    h = ctypes.c_void_p(1)
+    assert lib.spec_verify_create(ctypes.byref(c), ctypes.byref(h)) == want
+    assert not h.value
+
+
+def test_null_arguments_are_rejected(lib):
+    assert lib.spec_verify_create(None, None) == sv.SV_ERR_ARG
+    assert lib.spec_verify_run(None, None, None, None, None, None, 1.0, None, None) == sv.SV_ERR_ARG
+    assert lib.spec_verify_status(None) == sv.SV_ERR_ARG
+    lib.spec_verify_destroy(None)
+
+
+def test_algorithmic_bytes_of_the_llama8b_round():
+    # W_lm + q_logits + hidden + tokens + uniforms + outputs at V=128256,
+    # d=4096, B=1, K=4
+    assert bench.algorithmic_bytes(128256, 4096, 1, 4) == 1_052_766_268
+    assert bench.contraction_bytes(128256, 4096, 1, 4) == (2 * 128256 * 4096 + 2 * 5 * 4096
+                                                           + 4 * 4 * 128256)
+    greedy = bench.algorithmic_bytes(128256, 4096, 8, 7, greedy=True)
+    assert greedy == 2 * 128256 * 4096 + 2 * 64 * 4096 + 4 * 56 + 4 * 64 + 4 * 8
+
+
+def test_input_sets_exceed_l2():
+    n = bench.n_input_sets(2_100_000)
+    assert n * 2_100_000 >= 2 * bench.L2_BYTES
+    assert bench.n_input_sets(10 ** 10) == 4
+
+
+def test_parse_clocks():
+    text = ("index, clocks.sm [MHz], clocks.max.sm [MHz], power.draw [W], "
+            "clocks_event_reasons.active, clocks_event_reasons.hw_slowdown, "
+            "clocks_event_reasons.hw_thermal_slowdown, clocks_event_reasons.sw_thermal_slowdown, "
+            "clocks_event_reasons.sw_power_cap\n"
+            "0, 1965 MHz, 2070 MHz, 900.1 W, 0x0000, Not Active, Not Active, Not Active, Not Active\n"
+            "0, 1800 MHz, 2070 MHz, 1300.0 W, 0x0004, Not Active, Not Active, Not Active, Active\n"
+            "0, 345 MHz, 2070 MHz, 150.0 W, 0x0001, Not Active, Not Active, Not Active, Not Active\n")
+    c = bench.parse_clocks(text)
+    assert c["sm_max_mhz"] == 2070
+    assert c["sm_mhz"] == pytest.approx((1965 + 1800) / 2)
+    assert c["reasons"] == ["sw_power_cap"]
+
+
+def _gloo_worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        q.put((rank, bench.aggregate(0.5 + rank, 100 + rank)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_rank_aggregation_over_gloo():
+    import multiprocessing as mp
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_gloo_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in (0, 1):
+        assert results[r] == (1.5, 201)
