@@ -104,7 +104,8 @@ def parse_clocks(text: str):
         if len(r) != len(head):
             continue
         try:
-            sm.append(float(r[idx["clocks.sm"]].split()[0]))
+            col = "clocks.sm" if "clocks.sm" in idx else "clocks.current.sm"
+            sm.append(float(r[idx[col]].split()[0]))
             smax.append(float(r[idx["clocks.max.sm"]].split()[0]))
             power.append(float(r[idx["power.draw"]].split()[0]))
         except (KeyError, ValueError, IndexError):
@@ -319,8 +320,10 @@ def main():
     eng = sv.SpecVerify(wl.V, wl.d, wl.B, wl.K, "bf16", device=dev)
     stream = torch.cuda.Stream(device=dev)
     sv.spec_verify_set_stream(eng.h, stream)
-    out_tok = torch.empty((nsets, wl.B, wl.K + 1), dtype=torch.int32, device=dev)
-    out_n = torch.empty((nsets, wl.B), dtype=torch.int32, device=dev)
+    # one (16-byte aligned) output pair per input set
+    out_tok = [torch.empty((wl.B, wl.K + 1), dtype=torch.int32, device=dev)
+               for _ in range(nsets)]
+    out_n = [torch.empty((wl.B,), dtype=torch.int32, device=dev) for _ in range(nsets)]
     torch.cuda.synchronize()
 
     def run_set(i):
@@ -389,7 +392,7 @@ def main():
     value = total_rounds / max_el
 
     # emitted tokens per round over the input sets
-    n_host = out_n.cpu().numpy()
+    n_host = torch.stack(out_n).cpu().numpy()
     tokens_per_round = float((n_host + 1).mean())
 
     # contraction kernel timing (CUDA events on the launching stream)

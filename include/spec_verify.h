@@ -166,8 +166,8 @@ int spec_verify_timing_read(spec_verify_t *h, double *total_ms,
                             int64_t *launches);
 
 /* Number of kernel launches one spec_verify_run enqueues for temperature
- * T (the contraction, the decision pass, and for T > 0 the residual and
- * selection passes). */
+ * T: the LM-head contraction and one fused decision / residual / selection
+ * launch (2 for every T). */
 int spec_verify_launches_per_run(spec_verify_t *h, float temperature);
 
 /* Static description of an error code. */

@@ -66,9 +66,13 @@ namespace {
 size_t esize(int dtype) { return dtype == SV_BF16 ? 2 : 4; }
 
 void free_all(spec_verify *h) {
-  void *ptrs[] = {h->w.logits, h->w.part_p, h->w.part_q, h->w.lse, h->w.seq, h->w.chunk_mass,
-                  h->w.split_buf, h->w.split_cnt, h->w.status, h->w.abort_epoch, h->st_hidden,
-                  h->st_draft, h->st_q, h->st_u, h->st_tokens, h->st_n};
+  void *ptrs[] = {h->w.logits,    h->w.part_p,      h->w.part_q,    h->w.row_m,
+                  h->w.row_s,     h->w.seq,         h->w.chunk_mass, h->w.split_buf,
+                  h->w.split_cnt, h->w.status,      h->w.abort_epoch, h->w.ticket,
+                  h->w.finished,  h->w.row_count,   h->w.chunk_count, h->w.seq_flag,
+                  h->w.cand,
+                  h->st_hidden,   h->st_draft,      h->st_q,        h->st_u,
+                  h->st_tokens,   h->st_n};
   for (void *p : ptrs)
     if (p) cudaFree(p);
   for (cudaEvent_t e : h->ev0) cudaEventDestroy(e);
@@ -175,7 +179,12 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
   bool ok = dalloc(&h->w.logits, static_cast<size_t>(R) * D.V) &&
             dalloc(&h->w.part_p, static_cast<size_t>(R) * D.nsub) &&
             dalloc(&h->w.part_q, static_cast<size_t>(D.RQ) * D.nsub) &&
-            dalloc(&h->w.lse, static_cast<size_t>(R + D.RQ)) && dalloc(&h->w.seq, D.B) &&
+            dalloc(&h->w.row_m, static_cast<size_t>(R + D.RQ)) &&
+            dalloc(&h->w.row_s, static_cast<size_t>(R + D.RQ)) && dalloc(&h->w.seq, D.B) &&
+            dalloc(&h->w.ticket, 1) && dalloc(&h->w.finished, 1) &&
+            dalloc(&h->w.row_count, D.B) && dalloc(&h->w.chunk_count, D.B) &&
+            dalloc(&h->w.seq_flag, D.B) &&
+            dalloc(&h->w.cand, static_cast<size_t>(R) * (1 + sv::kMaxCand)) &&
             dalloc(&h->w.chunk_mass, static_cast<size_t>(D.B) * D.nchunk) &&
             dalloc(&h->w.split_buf, split_floats) &&
             dalloc(&h->w.split_cnt, static_cast<size_t>(h->num_sms) * 4) &&
@@ -188,7 +197,13 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
     ok = cudaMemset(h->w.split_cnt, 0, sizeof(int) * h->num_sms * 4) == cudaSuccess &&
          cudaMemset(h->w.status, 0, sizeof(int)) == cudaSuccess &&
          cudaMemset(h->w.abort_epoch, 0, sizeof(unsigned)) == cudaSuccess &&
-         cudaMemset(h->w.lse, 0, sizeof(double) * (R + D.RQ)) == cudaSuccess &&
+         cudaMemset(h->w.row_m, 0, sizeof(float) * (R + D.RQ)) == cudaSuccess &&
+         cudaMemset(h->w.row_s, 0, sizeof(float2) * (R + D.RQ)) == cudaSuccess &&
+         cudaMemset(h->w.ticket, 0, sizeof(unsigned)) == cudaSuccess &&
+         cudaMemset(h->w.finished, 0, sizeof(unsigned)) == cudaSuccess &&
+         cudaMemset(h->w.row_count, 0, sizeof(int) * D.B) == cudaSuccess &&
+         cudaMemset(h->w.chunk_count, 0, sizeof(int) * D.B) == cudaSuccess &&
+         cudaMemset(h->w.seq_flag, 0, sizeof(unsigned) * D.B) == cudaSuccess &&
          cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     free_all(h);
@@ -220,7 +235,8 @@ int spec_verify_set_wait_limit(spec_verify_t *h, uint64_t limit_ns) {
 
 int spec_verify_launches_per_run(spec_verify_t *h, float temperature) {
   if (!h) return SV_ERR_ARG;
-  return temperature > 0.0f ? 4 : 2;
+  (void)temperature;
+  return 2;
 }
 
 int spec_verify_run(spec_verify_t *h, const void *hidden, const void *W_lm,
@@ -309,12 +325,9 @@ int spec_verify_run(spec_verify_t *h, const void *hidden, const void *W_lm,
   T.out_tokens = out_tokens;
   T.out_n = out_n_accepted;
   T.epoch = epoch;
+  T.wait_limit_ns = h->wait_limit_ns;
   T.split_cnt_n = h->num_sms * 4;
-  if (sv::launch_decide(T, st) != cudaSuccess) return SV_ERR_CUDA;
-  if (!greedy) {
-    if (sv::launch_residual(T, st) != cudaSuccess) return SV_ERR_CUDA;
-    if (sv::launch_select(T, st) != cudaSuccess) return SV_ERR_CUDA;
-  }
+  if (sv::launch_tail(T, st) != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
 }
 
@@ -390,7 +403,16 @@ int spec_verify_debug_lse(spec_verify_t *h, double *dst) {
   if (!h || !dst) return SV_ERR_ARG;
   if (cudaStreamSynchronize(h->stream) != cudaSuccess) return SV_ERR_CUDA;
   const size_t n = static_cast<size_t>(h->dims.R + h->dims.RQ);
-  return cudaMemcpy(dst, h->w.lse, n * sizeof(double), cudaMemcpyDefault) == cudaSuccess
+  std::vector<float> m(n);
+  std::vector<float2> s(n);
+  std::vector<double> lse(n);
+  if (cudaMemcpy(m.data(), h->w.row_m, n * sizeof(float), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(s.data(), h->w.row_s, n * sizeof(float2), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SV_ERR_CUDA;
+  for (size_t i = 0; i < n; ++i)
+    lse[i] = static_cast<double>(m[i]) +
+             std::log(static_cast<double>(s[i].x) + static_cast<double>(s[i].y));
+  return cudaMemcpy(dst, lse.data(), n * sizeof(double), cudaMemcpyDefault) == cudaSuccess
              ? SV_OK
              : SV_ERR_CUDA;
 }

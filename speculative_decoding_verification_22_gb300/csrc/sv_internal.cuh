@@ -17,9 +17,10 @@ namespace sv {
 // ---------------------------------------------------------------------------
 constexpr int kSub = 32;        // vocab entries per softmax partial (one warp)
 constexpr int kTileM = 128;     // vocab rows per tensor-core tile (MMA M)
-constexpr int kChunk = 2048;    // vocab entries per residual-mass chunk
-constexpr int kTailThreads = 256;
+constexpr int kChunk = 4096;    // vocab entries per residual-mass chunk
+constexpr int kTailThreads = 512;
 constexpr int kChunkPerThread = kChunk / kTailThreads;  // 8
+constexpr int kMaxCand = 64;    // greedy: near-maximal subtiles listed per row
 
 // Per-sequence state handed from the decision pass to the residual and
 // selection passes.
@@ -45,7 +46,7 @@ struct Dims {
   int RQ;       // B * K draft rows
   int nsub;     // ceil(V / 32)
   int ntile;    // ceil(V / 128)
-  int nchunk;   // ceil(V / 2048)
+  int nchunk;   // ceil(V / 4096)
 };
 
 // Device workspace (owned by the handle).
@@ -53,13 +54,21 @@ struct Work {
   float *logits;       // [R, V]
   float2 *part_p;      // [R, nsub]   (max, sum-exp) of logits / T; T == 0: (max, 0)
   float2 *part_q;      // [RQ, nsub]  (max, sum-exp) of q_logits / T
-  double *lse;         // [R + RQ]    normalisers (debug copy)
+  float *row_m;        // [R + RQ]    row maximum M of logits / T (then of q_logits / T)
+  float2 *row_s;       // [R + RQ]    row sum S = sum exp(x - M) as float-float (hi, lo);
+                       //             LSE = M + log S
   SeqState *seq;       // [B]
-  double *chunk_mass;  // [B, nchunk]
+  float2 *chunk_mass;  // [B, nchunk]  float-float residual masses
   float *split_buf;    // [grid, 2, 128 * npad]  partial tiles (tensor-core path)
   int *split_cnt;      // [grid, 4]
   int *status;         // [1]   first device-side error since last read
   unsigned *abort_epoch;  // [1] epoch of the last run whose contraction gave up
+  unsigned *ticket;    // [1]   tail-kernel CTA order (rewound by its last CTA)
+  unsigned *finished;  // [1]
+  int *row_count;      // [B]   row CTAs finished per sequence
+  int *chunk_count;    // [B]   chunk CTAs finished per sequence
+  unsigned *seq_flag;  // [B]   epoch of the sequence's published decision
+  int *cand;           // [R, 1 + kMaxCand] greedy: count, then subtile ids
 };
 
 // ---------------------------------------------------------------------------
@@ -267,24 +276,92 @@ __device__ __forceinline__ double warp_sum_d(double x) {
 
 // (max, sum-exp) partial of one 32-entry vocab subtile held one entry per
 // lane.  `valid` masks entries past V.  T == 0 (greedy) keeps only the max.
-// All lanes return the result.
+// -inf entries are allowed (probability zero); a NaN or +inf entry makes the
+// whole partial (NaN, NaN), which the decision pass reports.  All lanes
+// return the result.
 __device__ __forceinline__ float2 subtile_partial(float logit, bool valid, float inv_t,
                                                   bool greedy) {
+  if (__any_sync(0xffffffffu, valid && (isnan(logit) || logit == INFINITY)))
+    return make_float2(NAN, NAN);
   if (greedy) {
     const float m = warp_max(valid ? logit : -INFINITY);
     return make_float2(m, 0.0f);
   }
   const float a = valid ? logit * inv_t : -INFINITY;
   const float m = warp_max(a);
-  const float e = valid ? expf(a - m) : 0.0f;
+  const float e = (valid && m > -INFINITY) ? expf(a - m) : 0.0f;
   return make_float2(m, warp_sum(e));
 }
 
 // Error-free sum of two floats (Knuth's TwoSum): s + e == a + b exactly.
 __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
-  s = a + b;
-  const float bp = s - a;
-  e = (a - (s - bp)) + (b - bp);
+  s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// ---------------------------------------------------------------------------
+// Float-float ("double-float") numbers: value = hi + lo with |lo| <= ulp(hi)/2,
+// about 48 significant bits, on the fp32 pipe (GB300's fp64 rate is a small
+// fraction of its fp32 rate).  Addition uses TwoSum, so its result does not
+// depend on the order of the operands.
+// ---------------------------------------------------------------------------
+struct ff {
+  float hi, lo;
+};
+__device__ __forceinline__ ff ff_make(float x) { return ff{x, 0.0f}; }
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+  const float hi = __fadd_rn(s, e);
+  return ff{hi, __fsub_rn(e, __fsub_rn(hi, s))};
+}
+__device__ __forceinline__ ff ff_neg(ff a) { return ff{-a.hi, -a.lo}; }
+// a * b for a float b, exact product of the heads via FMA
+__device__ __forceinline__ ff ff_mul_f(ff a, float b) {
+  const float p = __fmul_rn(a.hi, b);
+  const float pe = fmaf(a.hi, b, -p);
+  const float e = fmaf(a.lo, b, pe);
+  const float hi = __fadd_rn(p, e);
+  return ff{hi, __fsub_rn(e, __fsub_rn(hi, p))};
+}
+// a / b for a float b (one correction step)
+__device__ __forceinline__ ff ff_div_f(ff a, float b) {
+  const float q = __fdiv_rn(a.hi, b);
+  const float r = __fadd_rn(fmaf(-q, b, a.hi), a.lo);
+  const float ql = __fdiv_rn(r, b);
+  const float hi = __fadd_rn(q, ql);
+  return ff{hi, __fsub_rn(ql, __fsub_rn(hi, q))};
+}
+// a / b, both float-float, to float-float accuracy
+__device__ __forceinline__ ff ff_div(ff a, ff b) {
+  const float q = __fdiv_rn(a.hi, b.hi);
+  // r = a - q * b
+  const ff qb = ff_mul_f(b, q);
+  const ff r = ff_add(a, ff_neg(qb));
+  const float ql = __fdiv_rn(r.hi, b.hi);
+  const float hi = __fadd_rn(q, ql);
+  return ff{hi, __fsub_rn(ql, __fsub_rn(hi, q))};
+}
+__device__ __forceinline__ bool ff_lt(ff a, ff b) {
+  return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+}
+__device__ __forceinline__ float ff_to_f(ff a) { return __fadd_rn(a.hi, a.lo); }
+__device__ __forceinline__ ff ff_shfl_xor(ff a, int o) {
+  return ff{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ ff ff_shfl_up(ff a, int o) {
+  return ff{__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ ff ff_shfl(ff a, int src) {
+  return ff{__shfl_sync(0xffffffffu, a.hi, src), __shfl_sync(0xffffffffu, a.lo, src)};
+}
+// butterfly sum: every lane ends with the same value
+__device__ __forceinline__ ff warp_sum_ff(ff x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = ff_add(x, ff_shfl_xor(x, o));
+  return x;
 }
 
 }  // namespace sv

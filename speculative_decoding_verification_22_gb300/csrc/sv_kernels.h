@@ -48,7 +48,7 @@ struct SimtParams {
 };
 cudaError_t launch_simt(const SimtParams &P, cudaStream_t stream);
 
-// ---- (b) decision, residual and (c) selection passes ---------------------
+// ---- (b) decision/residual and (c) selection, one fused launch -----------
 struct TailParams {
   Dims dims;
   Work w;
@@ -64,11 +64,10 @@ struct TailParams {
   int32_t *out_tokens;     // [B, K+1]
   int32_t *out_n;          // [B]
   unsigned epoch;          // run counter
+  uint64_t wait_limit_ns;  // bound of the wait for a sequence's decision
   int split_cnt_n;         // entries of w.split_cnt
 };
-cudaError_t launch_decide(const TailParams &P, cudaStream_t stream);
-cudaError_t launch_residual(const TailParams &P, cudaStream_t stream);
-cudaError_t launch_select(const TailParams &P, cudaStream_t stream);
+cudaError_t launch_tail(const TailParams &P, cudaStream_t stream);
 
 // cudaLaunchKernelEx with programmatic stream serialisation (PDL).
 cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem,

@@ -1,23 +1,34 @@
-// sv_tail.cu -- kernels (b) and (c) of the verify step.
+// sv_tail.cu -- kernels (b) and (c) of the verify step, fused into one
+// launch that follows the LM-head contraction.
 //
-// (b1) decide_kernel, one CTA per sequence: combines the per-subtile
-//      softmax partials into fp64 log-sum-exp normalisers of logits / T and
-//      q_logits / T, recomputes the K draft-token logits with a compensated
-//      dot product, and walks the draft left to right: x_{i+1} survives iff
-//      u_i < p_{i+1}(x) / q_{i+1}(x) ("Speculative Decoding: Two Models, One
-//      Voice", "The idea" step 3; "Speculative Decoding" (library wiki),
-//      "One speculation round").  It writes the accepted prefix and hands
-//      the row of the final draw to the next passes.  At T == 0 it performs
-//      greedy verification instead ("Speculative Decoding: Guess Several
-//      Tokens, Check Them in One Pass", Step 2) with an exact re-ranking of
-//      the near-maximal logits, and writes every output itself.
-// (b2) residual_kernel, vocab-parallel: per 2048-entry chunk, the mass of
-//      max(0, p_j - q_j) (or of p_{K+1} for the bonus) with 128-bit loads.
-// (c)  select_kernel, one CTA per sequence: locates u * S in the chunk
-//      prefix sums, rescans that chunk and emits the smallest v with
-//      u * S < C_v (inverse CDF in token-id order); an empty residual falls
-//      back to p_j ("What Actually Happens During Speculative Decoding in
-//      LLMs", speculative_sample_step).
+// CTAs take tickets from a device counter, so a CTA with a lower ticket is
+// known to be running before any CTA with a higher ticket starts waiting:
+//
+//  row CTAs (tickets 0 .. R+RQ-1), one per target row (logits / T) and per
+//      draft row (q_logits / T): combine the per-32-entry softmax partials
+//      into the row maximum M and sum S = sum_v exp(x_v - M).  The last row
+//      CTA of a sequence becomes its decider: it recomputes the K
+//      draft-token logits with a compensated dot product and walks the
+//      draft left to right, x_{i+1} surviving iff u_i < p_{i+1}(x) /
+//      q_{i+1}(x) ("Speculative Decoding: Two Models, One Voice", "The idea"
+//      step 3; "Speculative Decoding" (library wiki), "One speculation
+//      round"), writes the accepted prefix and publishes the row of the
+//      final draw.  At T == 0 it runs greedy verification instead, with an
+//      exact re-ranking of the near-maximal logits ("Speculative Decoding:
+//      Guess Several Tokens, Check Them in One Pass", Step 2).
+//  chunk CTAs (higher tickets), one per 4096-entry vocabulary chunk and
+//      sequence: wait (bounded) for the decision, compute the chunk's mass
+//      of max(0, p_j - q_j) (or of p_{K+1} for the bonus) with 128-bit
+//      loads; the last chunk CTA of a sequence inverts the CDF: the smallest
+//      v with u * S < C_v, falling back to p_j when the residual is empty
+//      ("What Actually Happens During Speculative Decoding in LLMs",
+//      speculative_sample_step).
+//
+// All arithmetic is fp32 or float-float (hi + lo pairs carried with
+// error-free transforms): with the row statistics (M, S), exp(M - LSE) is
+// 1 / S, and the accept threshold is p/q = exp(delta) * S_q / S_p with
+// delta = (l / T - M_p) - (ql / T - M_q), evaluated as expf of delta's head
+// times (1 + its tail).  No transcendental function needs more than fp32.
 #include <cuda_bf16.h>
 
 #include "sv_internal.cuh"
@@ -26,130 +37,223 @@
 namespace sv {
 
 // ---------------------------------------------------------------------------
-// Helpers
+// Block-level helpers (kTailThreads threads)
 // ---------------------------------------------------------------------------
+constexpr int kTailWarps = kTailThreads / 32;
 
-// Dot product of hidden row `hrow` with W row `wrow` by one warp.  Products
-// are formed without rounding error (bf16 x bf16 is exact in fp32; fp32 x
-// fp32 via an FMA error term) and summed with TwoSum error tracking, so the
-// result is accurate to a few fp64 ulps of the logit.  Every lane returns
-// the same value.
-__device__ double dot_warp(const TailParams &P, int64_t hrow, int64_t wrow, int lane) {
-  const int64_t d = P.dims.d;
-  float s = 0.0f, c = 0.0f;
-  if (P.dtype == SV_BF16) {
-    const __nv_bfloat16 *h = static_cast<const __nv_bfloat16 *>(P.H) + hrow * d;
-    const __nv_bfloat16 *w = static_cast<const __nv_bfloat16 *>(P.W) + wrow * d;
-#pragma unroll 8
-    for (int64_t k = lane; k < d; k += 32) {
-      const float p = __fmul_rn(__bfloat162float(h[k]), __bfloat162float(w[k]));
-      float t, e;
-      two_sum(s, p, t, e);
-      s = t;
-      c += e;
-    }
-  } else {
-    const float *h = static_cast<const float *>(P.H) + hrow * d;
-    const float *w = static_cast<const float *>(P.W) + wrow * d;
-#pragma unroll 8
-    for (int64_t k = lane; k < d; k += 32) {
-      const float a = h[k], b = w[k];
-      const float p = __fmul_rn(a, b);
-      const float pe = fmaf(a, b, -p);
-      float t, e;
-      two_sum(s, p, t, e);
-      s = t;
-      c += e + pe;
-    }
-  }
-  return warp_sum_d(static_cast<double>(s) + static_cast<double>(c));
-}
-
-// Greedy argmax of target row r with ties to the smallest id.  Only entries
-// whose fp32 logit is within eps of the row maximum can be the argmax (the
-// fp32 logits are far more accurate than eps); those are re-ranked with the
-// exact dot product in increasing id order.  Returns -1 if the row is not
-// finite.
-__device__ int exact_argmax(const TailParams &P, int64_t r, int lane) {
-  const int nsub = P.dims.nsub;
-  const int64_t V = P.dims.V;
-  const float2 *part = P.w.part_p + r * nsub;
-  float M = -INFINITY;
-  for (int s = lane; s < nsub; s += 32) M = fmaxf(M, part[s].x);
-  M = warp_max(M);
-  if (!isfinite(M)) return -1;
-  const float thr = M - (1e-3f + 1e-5f * fabsf(M));
-  double best = -INFINITY;
-  int best_v = -1;
-  for (int s0 = 0; s0 < nsub; s0 += 32) {
-    const int s = s0 + lane;
-    unsigned cand = __ballot_sync(0xffffffffu, s < nsub && part[s].x >= thr);
-    while (cand) {
-      const int sc = s0 + __ffs(cand) - 1;
-      cand &= cand - 1;
-      const int64_t v = static_cast<int64_t>(sc) * kSub + lane;
-      unsigned hit = __ballot_sync(0xffffffffu, v < V && P.w.logits[r * V + v] >= thr);
-      while (hit) {
-        const int64_t vv = static_cast<int64_t>(sc) * kSub + __ffs(hit) - 1;
-        hit &= hit - 1;
-        const double e = dot_warp(P, r, vv, lane);
-        if (e > best) {
-          best = e;
-          best_v = static_cast<int>(vv);
-        }
-      }
-    }
-  }
-  return best_v;
-}
-
-__device__ __forceinline__ double block_sum_d(double x, double *s_warp) {
+__device__ __forceinline__ ff block_sum_ff(ff x, ff *s_warp) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  x = warp_sum_d(x);
+  x = warp_sum_ff(x);
   __syncthreads();
   if (lane == 0) s_warp[warp] = x;
   __syncthreads();
-  double t = 0.0;
   if (warp == 0) {
-    t = lane < (blockDim.x >> 5) ? s_warp[lane] : 0.0;
-    t = warp_sum_d(t);
+    ff t = lane < kTailWarps ? s_warp[lane] : ff_make(0.0f);
+    t = warp_sum_ff(t);
     if (lane == 0) s_warp[0] = t;
   }
   __syncthreads();
   return s_warp[0];
 }
 
-// Exclusive prefix sum over the block (fixed order).
-__device__ __forceinline__ double block_excl_scan_d(double x, double *s_warp) {
+__device__ __forceinline__ float block_max_f(float x, float *s_warp) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  double inc = x;
+  x = warp_max(x);
+  __syncthreads();
+  if (lane == 0) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    float t = lane < kTailWarps ? s_warp[lane] : -INFINITY;
+    t = warp_max(t);
+    if (lane == 0) s_warp[0] = t;
+  }
+  __syncthreads();
+  return s_warp[0];
+}
+
+// Exclusive prefix sum over the block, in thread order (float-float).
+__device__ __forceinline__ ff block_excl_scan_ff(ff x, ff *s_warp) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ff inc = x;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += y;
+    const ff y = ff_shfl_up(inc, o);
+    if (lane >= o) inc = ff_add(y, inc);
   }
   __syncthreads();
   if (lane == 31) s_warp[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    double t = lane < (blockDim.x >> 5) ? s_warp[lane] : 0.0;
+    ff t = lane < kTailWarps ? s_warp[lane] : ff_make(0.0f);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
+      const ff y = ff_shfl_up(t, o);
+      if (lane >= o) t = ff_add(y, t);
     }
-    if (lane < (blockDim.x >> 5)) s_warp[lane] = t;  // inclusive warp totals
+    if (lane < kTailWarps) s_warp[lane] = t;
   }
   __syncthreads();
-  const double before = warp > 0 ? s_warp[warp - 1] : 0.0;
-  return before + inc - x;
+  const ff before = warp > 0 ? s_warp[warp - 1] : ff_make(0.0f);
+  return ff_add(before, ff_add(inc, ff_neg(x)));
 }
+
+// Bounded wait until *flag == value (one thread).
+__device__ __forceinline__ bool wait_flag(const unsigned *flag, unsigned value,
+                                          uint64_t limit_ns) {
+  const volatile unsigned *f = flag;
+  if (*f == value) return true;
+  const uint64_t t0 = globaltimer();
+  while (*f != value) {
+    if (globaltimer() - t0 >= limit_ns) return false;
+    __nanosleep(32);
+  }
+  return true;
+}
+
+__device__ __forceinline__ ff ld_ff(const float2 *p) {
+  const float2 v = __ldcg(p);
+  return ff{v.x, v.y};
+}
+__device__ __forceinline__ void st_ff(float2 *p, ff v) { *p = make_float2(v.hi, v.lo); }
+
+// ---------------------------------------------------------------------------
+// Dot products and the greedy argmax
+// ---------------------------------------------------------------------------
+
+// Accumulates a * b exactly into the pair (s, c): the product's rounding
+// error comes from an FMA (zero when the product is exact, as for bf16) and
+// the sum's from TwoSum.
+__device__ __forceinline__ void acc_product(float a, float b, float &s, float &c) {
+  const float p = __fmul_rn(a, b);
+  const float pe = fmaf(a, b, -p);
+  float t, e;
+  two_sum(s, p, t, e);
+  s = t;
+  c = __fadd_rn(c, __fadd_rn(e, pe));
+}
+
+// Part `part` of `nparts` (contiguous ranges of 16-byte vectors) of the dot
+// product of hidden row `hrow` with W row `wrow`, by one warp with 16-byte
+// loads (rows are 16-byte aligned: d is a multiple of 8 for bf16, of 4 for
+// fp32, and the base pointers are 16-byte aligned).  The result is a
+// float-float accurate to about 2^-40 of the row's sum of |h * w|; every
+// lane returns the same value, and the parts sum to the whole in a fixed
+// order.
+__device__ ff dot_warp(const TailParams &P, int64_t hrow, int64_t wrow, int lane, int part = 0,
+                       int nparts = 1) {
+  const int64_t d = P.dims.d;
+  float s = 0.0f, c = 0.0f;
+  constexpr int kBatch = 4;
+  if (P.dtype == SV_BF16) {
+    const uint4 *h =
+        reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.H) + hrow * d);
+    const uint4 *w =
+        reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.W) + wrow * d);
+    const int64_t n = d / 8;
+    const int64_t lo = n * part / nparts, hi = n * (part + 1) / nparts;
+    for (int64_t k0 = lo; k0 < hi; k0 += 32 * kBatch) {
+      uint4 hv[kBatch], wv[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int64_t k = k0 + j * 32 + lane;
+        hv[j] = k < hi ? __ldg(&h[k]) : make_uint4(0, 0, 0, 0);
+        wv[j] = k < hi ? __ldg(&w[k]) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const __nv_bfloat162 *hb = reinterpret_cast<const __nv_bfloat162 *>(&hv[j]);
+        const __nv_bfloat162 *wb = reinterpret_cast<const __nv_bfloat162 *>(&wv[j]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 hf = __bfloat1622float2(hb[e]);
+          const float2 wf = __bfloat1622float2(wb[e]);
+          acc_product(hf.x, wf.x, s, c);
+          acc_product(hf.y, wf.y, s, c);
+        }
+      }
+    }
+  } else {
+    const float4 *h = reinterpret_cast<const float4 *>(static_cast<const float *>(P.H) + hrow * d);
+    const float4 *w = reinterpret_cast<const float4 *>(static_cast<const float *>(P.W) + wrow * d);
+    const int64_t n = d / 4;
+    const int64_t lo = n * part / nparts, hi = n * (part + 1) / nparts;
+    for (int64_t k0 = lo; k0 < hi; k0 += 32 * kBatch) {
+      float4 hv[kBatch], wv[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int64_t k = k0 + j * 32 + lane;
+        hv[j] = k < hi ? __ldg(&h[k]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        wv[j] = k < hi ? __ldg(&w[k]) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        acc_product(hv[j].x, wv[j].x, s, c);
+        acc_product(hv[j].y, wv[j].y, s, c);
+        acc_product(hv[j].z, wv[j].z, s, c);
+        acc_product(hv[j].w, wv[j].w, s, c);
+      }
+    }
+  }
+  // renormalise this lane's pair, then sum the lanes
+  const float hi = __fadd_rn(s, c);
+  return warp_sum_ff(ff{hi, __fsub_rn(c, __fsub_rn(hi, s))});
+}
+
+// Greedy argmax of target row r with ties to the smallest id.  Only entries
+// whose fp32 logit is within eps of the row maximum can be the argmax (the
+// fp32 logits are far more accurate than eps); the row CTA listed the
+// subtiles holding such entries, and those entries are re-ranked here with
+// the exact dot product.  If the list overflowed, every subtile is scanned.
+__device__ __forceinline__ float greedy_eps(float M) { return 1e-3f + 1e-5f * fabsf(M); }
+
+__device__ int exact_argmax(const TailParams &P, int64_t r, float M, int lane) {
+  const int nsub = P.dims.nsub;
+  const int64_t V = P.dims.V;
+  const float2 *part = P.w.part_p + r * nsub;
+  const float thr = M - greedy_eps(M);
+  const int *cand = P.w.cand + r * (1 + kMaxCand);
+  const int ncand = __ldcg(&cand[0]);
+  const bool listed = ncand <= kMaxCand;
+  const int n = listed ? ncand : nsub;
+  ff best = ff_make(-INFINITY);
+  int best_v = 0x7fffffff;
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const int i = i0 + lane;
+    int sub = -1;
+    if (i < n) sub = listed ? __ldcg(&cand[1 + i]) : i;
+    const bool ok = sub >= 0 && (listed || __ldcg(&part[sub].x) >= thr);
+    unsigned subs = __ballot_sync(0xffffffffu, ok);
+    while (subs) {
+      const int src = __ffs(subs) - 1;
+      subs &= subs - 1;
+      const int sc = __shfl_sync(0xffffffffu, sub, src);
+      const int64_t v = static_cast<int64_t>(sc) * kSub + lane;
+      unsigned hit =
+          __ballot_sync(0xffffffffu, v < V && __ldcg(&P.w.logits[r * V + v]) >= thr);
+      while (hit) {
+        const int64_t vv = static_cast<int64_t>(sc) * kSub + __ffs(hit) - 1;
+        hit &= hit - 1;
+        const ff e = dot_warp(P, r, vv, lane);
+        const bool same = e.hi == best.hi && e.lo == best.lo;
+        if (ff_lt(best, e) || (same && vv < best_v)) {
+          best = e;
+          best_v = static_cast<int>(vv);
+        }
+      }
+    }
+  }
+  return best_v == 0x7fffffff ? -1 : best_v;
+}
+
+// ---------------------------------------------------------------------------
+// Draw weights
+// ---------------------------------------------------------------------------
 
 // Weight of vocabulary entry v in the final draw: max(0, p - q) for a
 // residual, p for a bonus.  p(v) = exp(l / T - LSE) is evaluated as
-// exp(l * inv_t - M) * exp(M - LSE) with M the row maximum, so the fp32
-// argument stays small near the mass; the explicit _rn operations keep the
-// value bit-identical wherever it is recomputed.
+// exp(l * inv_t - M) * (1 / S) with M the row maximum, so the fp32 argument
+// stays small near the mass; the explicit _rn operations keep the value
+// bit-identical wherever it is recomputed.
 __device__ __forceinline__ float draw_weight(const SeqState &st, float l, float ql,
                                              float inv_t) {
   const float p = __fmul_rn(expf(fmaf(l, inv_t, -st.p_max)), st.p_corr);
@@ -158,7 +262,8 @@ __device__ __forceinline__ float draw_weight(const SeqState &st, float l, float 
   return fmaxf(__fsub_rn(p, q), 0.0f);
 }
 
-// The 8 consecutive weights of this thread in chunk `chunk`, and their sum.
+// The kChunkPerThread consecutive weights of this thread in chunk `chunk`,
+// and their sum (in index order).
 __device__ __forceinline__ float chunk_weights(const TailParams &P, const SeqState &st,
                                                int chunk, float (&r)[kChunkPerThread]) {
   const int64_t V = P.dims.V;
@@ -169,14 +274,18 @@ __device__ __forceinline__ float chunk_weights(const TailParams &P, const SeqSta
   float l[kChunkPerThread], q[kChunkPerThread];
   if ((V & 3) == 0 && v0 + kChunkPerThread <= V) {
     const float4 *l4 = reinterpret_cast<const float4 *>(lrow + v0);
-    const float4 a = l4[0], b = l4[1];
-    l[0] = a.x; l[1] = a.y; l[2] = a.z; l[3] = a.w;
-    l[4] = b.x; l[5] = b.y; l[6] = b.z; l[7] = b.w;
+#pragma unroll
+    for (int j = 0; j < kChunkPerThread / 4; ++j) {
+      const float4 a = __ldcg(&l4[j]);
+      l[4 * j] = a.x; l[4 * j + 1] = a.y; l[4 * j + 2] = a.z; l[4 * j + 3] = a.w;
+    }
     if (resid) {
       const float4 *q4 = reinterpret_cast<const float4 *>(qrow + v0);
-      const float4 c = q4[0], e = q4[1];
-      q[0] = c.x; q[1] = c.y; q[2] = c.z; q[3] = c.w;
-      q[4] = e.x; q[5] = e.y; q[6] = e.z; q[7] = e.w;
+#pragma unroll
+      for (int j = 0; j < kChunkPerThread / 4; ++j) {
+        const float4 a = q4[j];
+        q[4 * j] = a.x; q[4 * j + 1] = a.y; q[4 * j + 2] = a.z; q[4 * j + 3] = a.w;
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < kChunkPerThread; ++j) q[j] = 0.0f;
@@ -185,7 +294,7 @@ __device__ __forceinline__ float chunk_weights(const TailParams &P, const SeqSta
 #pragma unroll
     for (int j = 0; j < kChunkPerThread; ++j) {
       const bool in = v0 + j < V;
-      l[j] = in ? lrow[v0 + j] : 0.0f;
+      l[j] = in ? __ldcg(&lrow[v0 + j]) : 0.0f;
       q[j] = (in && resid) ? qrow[v0 + j] : 0.0f;
     }
   }
@@ -193,216 +302,207 @@ __device__ __forceinline__ float chunk_weights(const TailParams &P, const SeqSta
 #pragma unroll
   for (int j = 0; j < kChunkPerThread; ++j) {
     r[j] = v0 + j < V ? draw_weight(st, l[j], q[j], P.inv_t) : 0.0f;
-    sum += r[j];
+    sum = __fadd_rn(sum, r[j]);
   }
   return sum;
 }
 
 // ---------------------------------------------------------------------------
-// (b1) decision pass
+// The accept threshold p / q from row statistics (see the file comment).
+// lp = l / T - M_p and lq = ql / T - M_q as float-floats, ratio = S_q / S_p.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kTailThreads) decide_kernel(const TailParams P) {
-  pdl_wait();
-  pdl_launch_dependents();
-  const int b = blockIdx.x;
+__device__ __forceinline__ float accept_threshold(ff lp, ff lq, float ratio) {
+  if (lq.hi == -INFINITY) return lp.hi == -INFINITY ? 0.0f : INFINITY;  // q(x) == 0
+  const ff delta = ff_add(lp, ff_neg(lq));
+  if (!(delta.hi < 80.0f)) return INFINITY;  // far above 1: accepted for any u
+  if (delta.hi < -120.0f) return 0.0f;       // below every uniform on the 2^-24 grid
+  return __fmul_rn(__fmul_rn(expf(delta.hi), __fadd_rn(1.0f, delta.lo)), ratio);
+}
+
+// ---------------------------------------------------------------------------
+// Decider (one CTA, the last row CTA of sequence b)
+// ---------------------------------------------------------------------------
+__device__ void decide(const TailParams &P, int b) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
   const int K = P.dims.K, rows = K + 1;
   const int64_t V = P.dims.V;
-  const int nsub = P.dims.nsub;
+  const int R = P.dims.R;
   const int64_t out0 = static_cast<int64_t>(b) * rows;
-  __shared__ double s_lse[2 * SV_MAX_K + 1];
-  __shared__ float s_max[2 * SV_MAX_K + 1];
-  __shared__ double s_lx[SV_MAX_K];
-  __shared__ int s_arg[SV_MAX_K + 1];
+  __shared__ ff s_l[SV_MAX_K];           // draft-token logits
+  __shared__ ff s_part[kTailWarps];
+  __shared__ float s_lp_m[SV_MAX_K + 1], s_lq_m[SV_MAX_K];    // row maxima
+  __shared__ ff s_lp_s[SV_MAX_K + 1], s_lq_s[SV_MAX_K];       // row sums
+  __shared__ float s_ql[SV_MAX_K], s_u[SV_MAX_K + 1];
+  __shared__ int s_x[SV_MAX_K], s_arg[SV_MAX_K + 1];
   __shared__ int s_err;
 
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0) s_err = 0;
+  __syncthreads();
+  // everything the walk needs, loaded in parallel
+  if (threadIdx.x < rows) {
+    const int i = threadIdx.x;
+    s_lp_m[i] = __ldcg(&P.w.row_m[out0 + i]);
+    s_lp_s[i] = ld_ff(&P.w.row_s[out0 + i]);
+    if (!P.greedy) s_u[i] = P.u[out0 + i];
+    const bool fin = isfinite(s_lp_m[i]) &&
+                     (P.greedy || (s_lp_s[i].hi > 0.0f && s_lp_s[i].hi < INFINITY));
+    if (!fin) atomicCAS(&s_err, 0, SV_ERR_NONFINITE);
+  }
+  if (threadIdx.x >= 32 && threadIdx.x < 32 + K) {
+    const int i = threadIdx.x - 32;
+    const int x = P.draft[static_cast<int64_t>(b) * K + i];
+    s_x[i] = x;
+    if (x < 0 || static_cast<int64_t>(x) >= V) {
+      atomicExch(&s_err, SV_ERR_TOKEN);
+    } else if (!P.greedy) {
+      const int64_t rq = static_cast<int64_t>(R) + static_cast<int64_t>(b) * K + i;
+      s_lq_m[i] = __ldcg(&P.w.row_m[rq]);
+      s_lq_s[i] = ld_ff(&P.w.row_s[rq]);
+      s_ql[i] = P.q_logits[(static_cast<int64_t>(b) * K + i) * V + x];
+      const bool fin = isfinite(s_lq_m[i]) && s_lq_s[i].hi > 0.0f && s_lq_s[i].hi < INFINITY;
+      if (!fin) atomicCAS(&s_err, 0, SV_ERR_NONFINITE);
+    }
+  }
+  if (threadIdx.x == 64 &&
+      *reinterpret_cast<volatile unsigned *>(P.w.abort_epoch) == P.epoch) {
     // a contraction that gave up in this run leaves the partials undefined
-    s_err = *reinterpret_cast<volatile unsigned *>(P.w.abort_epoch) == P.epoch ? SV_ERR_TIMEOUT
-                                                                               : 0;
+    atomicExch(&s_err, SV_ERR_TIMEOUT);
   }
   __syncthreads();
   if (s_err == SV_ERR_TIMEOUT && b == 0) {
     // the aborted contraction may have left split-tile counters half-used
-    for (int i = threadIdx.x; i < P.split_cnt_n; i += blockDim.x) P.w.split_cnt[i] = 0;
+    for (int i = threadIdx.x; i < P.split_cnt_n; i += kTailThreads) P.w.split_cnt[i] = 0;
   }
-  if (threadIdx.x < K) {
-    const int x = P.draft[static_cast<int64_t>(b) * K + threadIdx.x];
-    if (x < 0 || static_cast<int64_t>(x) >= V) atomicCAS(&s_err, 0, SV_ERR_TOKEN);
-  }
-  __syncthreads();
-
   if (s_err == 0) {
     if (!P.greedy) {
-      const int nrow = 2 * K + 1;
-      for (int r = warp; r < nrow; r += nwarps) {
-        const float2 *part =
-            r < rows ? P.w.part_p + (out0 + r) * nsub
-                     : P.w.part_q + (static_cast<int64_t>(b) * K + (r - rows)) * nsub;
-        float M = -INFINITY;
-        for (int s = lane; s < nsub; s += 32) M = fmaxf(M, part[s].x);
-        M = warp_max(M);
-        double S = 0.0;
-        for (int s = lane; s < nsub; s += 32) {
-          const float2 pm = part[s];
-          S += static_cast<double>(pm.y * expf(pm.x - M));
+      // the K draft-token logits, each split over wpr warps
+      const int wpr = K > 0 ? (kTailWarps / K > 0 ? kTailWarps / K : 1) : 1;
+      const int per = kTailWarps / wpr;
+      for (int i0 = 0; i0 < K; i0 += per) {
+        const int i = i0 + warp / wpr;
+        if (i < K && warp / wpr < per) {
+          const ff l = dot_warp(P, out0 + i, s_x[i], lane, warp % wpr, wpr);
+          if (lane == 0) s_part[warp] = l;
         }
-        S = warp_sum_d(S);
-        if (lane == 0) {
-          s_max[r] = M;
-          s_lse[r] = static_cast<double>(M) + log(S);
-          const int64_t dst = r < rows ? out0 + r
-                                       : static_cast<int64_t>(P.dims.R) +
-                                             static_cast<int64_t>(b) * K + (r - rows);
-          P.w.lse[dst] = s_lse[r];
+        __syncthreads();
+        if (threadIdx.x < per && i0 + static_cast<int>(threadIdx.x) < K) {
+          ff l = s_part[threadIdx.x * wpr];
+          for (int p = 1; p < wpr; ++p) l = ff_add(l, s_part[threadIdx.x * wpr + p]);
+          s_l[i0 + threadIdx.x] = l;
         }
-      }
-      for (int i = warp; i < K; i += nwarps) {
-        const int x = P.draft[static_cast<int64_t>(b) * K + i];
-        const double l = dot_warp(P, out0 + i, x, lane);
-        if (lane == 0) s_lx[i] = l;
+        __syncthreads();
       }
     } else {
-      for (int i = warp; i < rows; i += nwarps) {
-        const int a = exact_argmax(P, out0 + i, lane);
+      for (int i = warp; i < rows; i += kTailWarps) {
+        const int a = exact_argmax(P, out0 + i, s_lp_m[i], lane);
         if (lane == 0) s_arg[i] = a;
       }
     }
   }
   __syncthreads();
-
-  if (threadIdx.x != 0) return;
-  int err = s_err;
-  SeqState st = {};
-  st.mode = kModeSkip;
-  if (err == 0 && !P.greedy) {
-    bool finite = true;
-    for (int r = 0; r < 2 * K + 1; ++r) finite = finite && isfinite(s_lse[r]);
-    for (int i = 0; i < K; ++i) finite = finite && isfinite(s_lx[i]);
-    if (!finite) {
-      err = SV_ERR_NONFINITE;
-    } else {
+  if (threadIdx.x == 0) {
+    int err = s_err;
+    SeqState st = {};
+    st.mode = kModeSkip;
+    if (err == 0 && !P.greedy) {
       int n = K, mode = kModeP;
+      const float T = static_cast<float>(P.T);
       for (int i = 0; i < K; ++i) {
-        const int x = P.draft[static_cast<int64_t>(b) * K + i];
-        const double p = exp(s_lx[i] / P.T - s_lse[i]);
-        const double ql = static_cast<double>(
-            P.q_logits[(static_cast<int64_t>(b) * K + i) * V + x]);
-        const double q = exp(ql / P.T - s_lse[rows + i]);
-        const double u = static_cast<double>(P.u[out0 + i]);
-        const bool accept = q > 0.0 ? (u < p / q) : (p > 0.0);
-        if (accept) {
-          P.out_tokens[out0 + i] = x;
+        if (!isfinite(s_l[i].hi)) {
+          err = SV_ERR_NONFINITE;
+          break;
+        }
+        const ff lp = ff_add(ff_div_f(s_l[i], T), ff_make(-s_lp_m[i]));
+        const ff lq = ff_add(ff_div_f(ff_make(s_ql[i]), T), ff_make(-s_lq_m[i]));
+        const float ratio = ff_to_f(ff_div(s_lq_s[i], s_lp_s[i]));
+        const float t = accept_threshold(lp, lq, ratio);
+        if (s_u[i] < t) {
+          P.out_tokens[out0 + i] = s_x[i];
         } else {
           n = i;
           mode = kModeResidual;
           break;
         }
       }
-      for (int i = n + 1; i < rows; ++i) P.out_tokens[out0 + i] = -1;
-      P.out_n[b] = n;
-      st.mode = mode;
-      st.n_acc = n;
-      st.p_row = static_cast<int>(out0 + n);
-      st.p_max = s_max[n];
-      st.p_corr = static_cast<float>(exp(static_cast<double>(s_max[n]) - s_lse[n]));
-      if (mode == kModeResidual) {
-        st.q_row = b * K + n;
-        st.q_max = s_max[rows + n];
-        st.q_corr = static_cast<float>(exp(static_cast<double>(s_max[rows + n]) - s_lse[rows + n]));
-      }
-      st.u_final = P.u[out0 + K];
-    }
-  } else if (err == 0) {
-    bool ok = true;
-    for (int i = 0; i < rows; ++i) ok = ok && s_arg[i] >= 0;
-    if (!ok) {
-      err = SV_ERR_NONFINITE;
-    } else {
-      int n = K;
-      for (int i = 0; i < K; ++i) {
-        const int x = P.draft[static_cast<int64_t>(b) * K + i];
-        if (x == s_arg[i]) {
-          P.out_tokens[out0 + i] = x;
-        } else {
-          P.out_tokens[out0 + i] = s_arg[i];
-          n = i;
-          break;
+      if (err == 0) {
+        for (int i = n + 1; i < rows; ++i) P.out_tokens[out0 + i] = -1;
+        P.out_n[b] = n;
+        st.mode = mode;
+        st.n_acc = n;
+        st.p_row = static_cast<int>(out0 + n);
+        st.p_max = s_lp_m[n];
+        st.p_corr = __fdiv_rn(1.0f, ff_to_f(s_lp_s[n]));
+        if (mode == kModeResidual) {
+          st.q_row = b * K + n;
+          st.q_max = s_lq_m[n];
+          st.q_corr = __fdiv_rn(1.0f, ff_to_f(s_lq_s[n]));
         }
+        st.u_final = s_u[K];
       }
-      if (n == K) P.out_tokens[out0 + K] = s_arg[K];
-      for (int i = n + 1; i < rows; ++i) P.out_tokens[out0 + i] = -1;
-      P.out_n[b] = n;
+    } else if (err == 0) {
+      bool ok = true;
+      for (int i = 0; i < rows; ++i) ok = ok && s_arg[i] >= 0;
+      if (!ok) {
+        err = SV_ERR_NONFINITE;
+      } else {
+        int n = K;
+        for (int i = 0; i < K; ++i) {
+          if (s_x[i] == s_arg[i]) {
+            P.out_tokens[out0 + i] = s_x[i];
+          } else {
+            P.out_tokens[out0 + i] = s_arg[i];
+            n = i;
+            break;
+          }
+        }
+        if (n == K) P.out_tokens[out0 + K] = s_arg[K];
+        for (int i = n + 1; i < rows; ++i) P.out_tokens[out0 + i] = -1;
+        P.out_n[b] = n;
+      }
     }
+    if (err != 0) {
+      if (err != SV_ERR_TIMEOUT) set_status(P.w.status, err);
+      st.mode = kModeSkip;
+      for (int i = 0; i < rows; ++i) P.out_tokens[out0 + i] = -1;
+      P.out_n[b] = -1;
+    }
+    P.w.seq[b] = st;
+    __threadfence();
+    *reinterpret_cast<volatile unsigned *>(&P.w.seq_flag[b]) = P.epoch;
   }
-  if (err != 0) {
-    if (err != SV_ERR_TIMEOUT) set_status(P.w.status, err);
-    for (int i = 0; i < rows; ++i) P.out_tokens[out0 + i] = -1;
-    P.out_n[b] = -1;
-  }
-  P.w.seq[b] = st;
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
-// (b2) residual masses
+// Selection (one CTA, the last chunk CTA of sequence b)
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kTailThreads) residual_kernel(const TailParams P) {
-  pdl_wait();
-  pdl_launch_dependents();
-  __shared__ double s_warp[kTailThreads / 32];
-  const int c = blockIdx.x, b = blockIdx.y;
-  const SeqState st = P.w.seq[b];
-  double t = 0.0;
-  if (st.mode != kModeSkip) {
-    float r[kChunkPerThread];
-    t = static_cast<double>(chunk_weights(P, st, c, r));
-  }
-  const double m = block_sum_d(t, s_warp);
-  if (threadIdx.x == 0) P.w.chunk_mass[static_cast<int64_t>(b) * P.dims.nchunk + c] = m;
-}
-
-// ---------------------------------------------------------------------------
-// (c) selection
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kTailThreads) select_kernel(const TailParams P) {
-  pdl_wait();
-  pdl_launch_dependents();
-  __shared__ double s_warp[kTailThreads / 32];
-  __shared__ double s_total, s_base, s_target;
-  __shared__ int s_chunk;
-  __shared__ int s_found, s_last;
-  const int b = blockIdx.x;
-  SeqState st = P.w.seq[b];
-  if (st.mode == kModeSkip) return;
+__device__ void select_token(const TailParams &P, int b, SeqState st) {
+  __shared__ ff s_warp[kTailWarps];
+  __shared__ ff s_base, s_target;
+  __shared__ int s_chunk, s_found, s_last;
+  const int lane = threadIdx.x & 31;
   const int nchunk = P.dims.nchunk;
-  double *mass = P.w.chunk_mass + static_cast<int64_t>(b) * nchunk;
+  float2 *mass = P.w.chunk_mass + static_cast<int64_t>(b) * nchunk;
 
-  if (threadIdx.x == 0) {
-    double S = 0.0;
-    for (int c = 0; c < nchunk; ++c) S += mass[c];
-    s_total = S;
-  }
-  __syncthreads();
-  if (!(s_total > 0.0) && st.mode == kModeResidual) {
+  ff S = ff_make(0.0f);
+  for (int c = threadIdx.x; c < nchunk; c += kTailThreads) S = ff_add(S, ld_ff(&mass[c]));
+  S = block_sum_ff(S, s_warp);
+  if (!(S.hi > 0.0f) && st.mode == kModeResidual) {
     // p_j == q_j on this row: draw from p_j instead
     st.mode = kModeP;
     for (int c = 0; c < nchunk; ++c) {
       float r[kChunkPerThread];
-      const double m = block_sum_d(static_cast<double>(chunk_weights(P, st, c, r)), s_warp);
-      if (threadIdx.x == 0) mass[c] = m;
+      const ff m = block_sum_ff(ff_make(chunk_weights(P, st, c, r)), s_warp);
+      if (threadIdx.x == 0) st_ff(&mass[c], m);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      double S = 0.0;
-      for (int c = 0; c < nchunk; ++c) S += mass[c];
-      s_total = S;
-    }
-    __syncthreads();
+    S = ff_make(0.0f);
+    for (int c = threadIdx.x; c < nchunk; c += kTailThreads) S = ff_add(S, ld_ff(&mass[c]));
+    S = block_sum_ff(S, s_warp);
   }
   const int64_t rows = P.dims.K + 1;
   int32_t *out = P.out_tokens + static_cast<int64_t>(b) * rows + st.n_acc;
-  if (!(s_total > 0.0)) {
+  if (!(S.hi > 0.0f)) {
     if (threadIdx.x == 0) {
       set_status(P.w.status, SV_ERR_NONFINITE);
       *out = -1;
@@ -410,46 +510,62 @@ __global__ void __launch_bounds__(kTailThreads) select_kernel(const TailParams P
     }
     return;
   }
-  if (threadIdx.x == 0) {
-    const double target = static_cast<double>(st.u_final) * s_total;
-    double acc = 0.0;
+  if (threadIdx.x < 32) {
+    // locate the chunk holding u * S: warp-level scan of the chunk masses
+    const ff target = ff_mul_f(S, st.u_final);
+    ff carry = ff_make(0.0f), base = ff_make(0.0f), base_last = ff_make(0.0f);
     int chunk = -1, last = -1;
-    double acc_last = 0.0;
-    for (int c = 0; c < nchunk; ++c) {
-      const double m = mass[c];
-      if (m > 0.0) {
-        last = c;
-        acc_last = acc;
+    for (int c0 = 0; c0 < nchunk && chunk < 0; c0 += 32) {
+      const int c = c0 + lane;
+      const ff m = c < nchunk ? ld_ff(&mass[c]) : ff_make(0.0f);
+      ff inc = m;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const ff y = ff_shfl_up(inc, o);
+        if (lane >= o) inc = ff_add(y, inc);
       }
-      if (target < acc + m) {
-        chunk = c;
-        break;
+      const ff incl = ff_add(carry, inc);
+      const ff excl = ff_add(incl, ff_neg(m));
+      const unsigned hit = __ballot_sync(0xffffffffu, c < nchunk && ff_lt(target, incl));
+      const unsigned pos = __ballot_sync(0xffffffffu, c < nchunk && m.hi > 0.0f);
+      if (pos) {
+        const int lp = 31 - __clz(pos);
+        last = c0 + lp;
+        base_last = ff_shfl(excl, lp);
       }
-      acc += m;
+      if (hit) {
+        const int lh = __ffs(hit) - 1;
+        chunk = c0 + lh;
+        base = ff_shfl(excl, lh);
+      }
+      carry = ff_shfl(incl, 31);
     }
-    if (chunk < 0) {  // rounding pushed the target past the end
-      chunk = last;
-      acc = acc_last;
+    if (lane == 0) {
+      if (chunk < 0) {  // rounding pushed the target past the end
+        chunk = last;
+        base = base_last;
+      }
+      s_chunk = chunk;
+      s_base = base;
+      s_target = target;
+      s_found = 0x7fffffff;
+      s_last = -1;
     }
-    s_chunk = chunk;
-    s_base = acc;
-    s_target = target;
-    s_found = 0x7fffffff;
-    s_last = -1;
   }
   __syncthreads();
   const int chunk = s_chunk;
   float r[kChunkPerThread];
   const float tsum = chunk_weights(P, st, chunk, r);
-  double run = s_base + block_excl_scan_d(static_cast<double>(tsum), s_warp);
+  ff run = ff_add(s_base, block_excl_scan_ff(ff_make(tsum), s_warp));
   const int64_t v0 = static_cast<int64_t>(chunk) * kChunk + threadIdx.x * kChunkPerThread;
+  const ff target = s_target;
   int found = 0x7fffffff, last = -1;
 #pragma unroll
   for (int j = 0; j < kChunkPerThread; ++j) {
-    run += static_cast<double>(r[j]);
+    run = ff_add(run, ff_make(r[j]));
     if (r[j] > 0.0f) {
       last = static_cast<int>(v0 + j);
-      if (found == 0x7fffffff && s_target < run) found = static_cast<int>(v0 + j);
+      if (found == 0x7fffffff && ff_lt(target, run)) found = static_cast<int>(v0 + j);
     }
   }
   if (found != 0x7fffffff) atomicMin(&s_found, found);
@@ -459,7 +575,158 @@ __global__ void __launch_bounds__(kTailThreads) select_kernel(const TailParams P
 }
 
 // ---------------------------------------------------------------------------
-// Launchers
+// The fused tail kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailParams P) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ unsigned s_ticket;
+  __shared__ float s_wf[kTailWarps];
+  __shared__ ff s_wff[kTailWarps];
+  __shared__ int s_last;
+  const int K = P.dims.K;
+  const int R = P.dims.R;
+  const int nrow = P.greedy ? R : R + P.dims.RQ;
+  if (threadIdx.x == 0) s_ticket = atomicAdd(P.w.ticket, 1u);
+  __syncthreads();
+  const int t = static_cast<int>(s_ticket);
+
+  if (t < nrow) {
+    // ---- row statistics ----
+    const bool qrow = t >= R;
+    const int b = qrow ? (t - R) / (K > 0 ? K : 1) : t / (K + 1);
+    const float2 *part = qrow ? P.w.part_q + static_cast<int64_t>(t - R) * P.dims.nsub
+                              : P.w.part_p + static_cast<int64_t>(t) * P.dims.nsub;
+    // one pass, 8 loads in flight per thread: running (max, sum) with
+    // rescaling whenever the running maximum grows
+    float m = -INFINITY, acc = 0.0f;
+    int bad = 0;
+    for (int s0 = threadIdx.x; s0 < P.dims.nsub; s0 += kTailThreads * 8) {
+      float2 pm[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int s = s0 + j * kTailThreads;
+        pm[j] = s < P.dims.nsub ? __ldcg(&part[s]) : make_float2(-INFINITY, 0.0f);
+      }
+      float mn = m;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        bad |= (isnan(pm[j].x) || pm[j].x == INFINITY) ? 1 : 0;
+        mn = fmaxf(mn, pm[j].x);
+      }
+      if (!P.greedy && mn > -INFINITY) {
+        acc = m > -INFINITY ? acc * expf(m - mn) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (pm[j].x > -INFINITY) acc += pm[j].y * expf(pm[j].x - mn);
+      }
+      m = mn;
+    }
+    bad = __syncthreads_or(bad);
+    float M = block_max_f(m, s_wf);
+    ff S = ff_make(0.0f);
+    if (!P.greedy && !bad) {
+      const float mine = m > -INFINITY ? acc * expf(m - M) : 0.0f;
+      S = block_sum_ff(ff_make(mine), s_wff);
+    }
+    if (bad) M = NAN;
+    if (P.greedy && !bad) {
+      // list the subtiles that may hold the argmax (see exact_argmax)
+      __shared__ int s_nc;
+      __shared__ int s_cand[kMaxCand];
+      if (threadIdx.x == 0) s_nc = 0;
+      __syncthreads();
+      const float thr = M - greedy_eps(M);
+      for (int s0 = threadIdx.x; s0 < P.dims.nsub; s0 += kTailThreads * 8) {
+        float x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int s = s0 + j * kTailThreads;
+          x[j] = s < P.dims.nsub ? __ldcg(&part[s].x) : -INFINITY;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (x[j] >= thr) {
+            const int k = atomicAdd(&s_nc, 1);
+            if (k < kMaxCand) s_cand[k] = s0 + j * kTailThreads;
+          }
+      }
+      __syncthreads();
+      int *cand = P.w.cand + static_cast<int64_t>(t) * (1 + kMaxCand);
+      const int nc = s_nc;
+      for (int k = threadIdx.x; k < nc && k < kMaxCand; k += kTailThreads) cand[1 + k] = s_cand[k];
+      if (threadIdx.x == 0) cand[0] = nc;
+    }
+    if (threadIdx.x == 0) {
+      P.w.row_m[t] = M;
+      st_ff(&P.w.row_s[t], S);
+      __threadfence();
+      const int need = P.greedy ? K + 1 : 2 * K + 1;
+      s_last = atomicAdd(&P.w.row_count[b], 1) == need - 1;
+      if (s_last) {
+        P.w.row_count[b] = 0;
+        __threadfence();
+      }
+    }
+    __syncthreads();
+    if (s_last) decide(P, b);
+  } else {
+    // ---- residual chunk ----
+    const int idx = t - nrow;
+    const int b = idx / P.dims.nchunk, c = idx % P.dims.nchunk;
+    if (threadIdx.x == 0) {
+      if (!wait_flag(&P.w.seq_flag[b], P.epoch, P.wait_limit_ns))
+        set_status(P.w.status, SV_ERR_TIMEOUT);
+      __threadfence();
+    }
+    __syncthreads();
+    SeqState st;
+    {
+      const int *src = reinterpret_cast<const int *>(&P.w.seq[b]);
+      int *dst = reinterpret_cast<int *>(&st);
+#pragma unroll
+      for (int i = 0; i < static_cast<int>(sizeof(SeqState) / 4); ++i) dst[i] = __ldcg(&src[i]);
+    }
+    if (*reinterpret_cast<const volatile unsigned *>(&P.w.seq_flag[b]) != P.epoch)
+      st.mode = kModeSkip;
+    float m = 0.0f;
+    if (st.mode != kModeSkip) {
+      float r[kChunkPerThread];
+      m = chunk_weights(P, st, c, r);
+    }
+    const ff mass = block_sum_ff(ff_make(m), s_wff);
+    if (threadIdx.x == 0) {
+      st_ff(&P.w.chunk_mass[static_cast<int64_t>(b) * P.dims.nchunk + c], mass);
+      __threadfence();
+      s_last = atomicAdd(&P.w.chunk_count[b], 1) == P.dims.nchunk - 1;
+      if (s_last) {
+        P.w.chunk_count[b] = 0;
+        __threadfence();
+      }
+    }
+    __syncthreads();
+    if (s_last && st.mode != kModeSkip) select_token(P, b, st);
+  }
+
+  // the last CTA to finish rewinds the ticket counter for the next launch
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(P.w.finished, 1u) == gridDim.x - 1) {
+      *P.w.ticket = 0;
+      *P.w.finished = 0;
+    }
+  }
+}
+
+cudaError_t launch_tail(const TailParams &P, cudaStream_t stream) {
+  const int nrow = P.greedy ? P.dims.R : P.dims.R + P.dims.RQ;
+  const int nchunk_ctas = P.greedy ? 0 : P.dims.B * P.dims.nchunk;
+  void *args[] = {const_cast<TailParams *>(&P)};
+  return launch_pdl(reinterpret_cast<const void *>(&tail_kernel), dim3(nrow + nchunk_ctas),
+                    dim3(kTailThreads), 0, stream, args);
+}
+
 // ---------------------------------------------------------------------------
 cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem,
                        cudaStream_t stream, void **args) {
@@ -474,24 +741,6 @@ cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelExC(&cfg, fn, args);
-}
-
-cudaError_t launch_decide(const TailParams &P, cudaStream_t stream) {
-  void *args[] = {const_cast<TailParams *>(&P)};
-  return launch_pdl(reinterpret_cast<const void *>(&decide_kernel), dim3(P.dims.B),
-                    dim3(kTailThreads), 0, stream, args);
-}
-
-cudaError_t launch_residual(const TailParams &P, cudaStream_t stream) {
-  void *args[] = {const_cast<TailParams *>(&P)};
-  return launch_pdl(reinterpret_cast<const void *>(&residual_kernel),
-                    dim3(P.dims.nchunk, P.dims.B), dim3(kTailThreads), 0, stream, args);
-}
-
-cudaError_t launch_select(const TailParams &P, cudaStream_t stream) {
-  void *args[] = {const_cast<TailParams *>(&P)};
-  return launch_pdl(reinterpret_cast<const void *>(&select_kernel), dim3(P.dims.B),
-                    dim3(kTailThreads), 0, stream, args);
 }
 
 }  // namespace sv

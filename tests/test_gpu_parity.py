@@ -178,3 +178,30 @@ def test_repeated_runs_are_bitwise_identical(dev):
                 assert torch.equal(a, b)
     assert eng.status() == sv.SV_OK
     eng.close()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_masked_draft_logits(dev, dtype):
+    # draft logits of -inf (tokens the draft can never propose) are valid
+    # inputs: q = 0 there, and those tokens reach the output only through
+    # the residual
+    over = dict(B=4, K=4, V=2000, d=256) if dtype == "bf16" else dict(B=4, K=4)
+    wl = si.workload("tiny", dtype=dtype, **over)
+    W = si.make_weights(wl, seed=31, device=dev)
+    W_np = si.to_oracle(W)
+    inp = si.make_round(wl, W, seed=32)
+    q = inp["q_logits"].clone()
+    mask = torch.rand(q.shape, generator=torch.Generator(device=dev).manual_seed(3),
+                      device=dev) < 0.3
+    drafted = torch.zeros_like(mask)
+    drafted.scatter_(2, inp["draft"].long().unsqueeze(-1), True)
+    q[mask & ~drafted] = float("-inf")
+    inp["q_logits"] = q
+    eng = sv.SpecVerify(wl.V, wl.d, wl.B, wl.K, wl.dtype, device=dev)
+    got = gpu_verify(eng, W, inp, 1.0)
+    assert got["status"] == sv.SV_OK
+    ref = oracle_verify(inp["hidden"], W_np, inp["draft"], inp["q_logits"], inp["uniforms"],
+                        1.0, want_logits=True)
+    check_numerics(eng, ref, wl, 1.0)
+    assert compare_tokens(got, ref, 1.0)[0] == 0
+    eng.close()

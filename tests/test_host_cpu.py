@@ -94,6 +94,9 @@ def test_parse_clocks():
             "0, 345 MHz, 2070 MHz, 150.0 W, 0x0001, Not Active, Not Active, Not Active, Not Active\n")
     c = bench.parse_clocks(text)
     assert c["sm_max_mhz"] == 2070
+    # nvidia-smi labels the queried clocks.sm column clocks.current.sm
+    c2 = bench.parse_clocks(text.replace("clocks.sm [MHz]", "clocks.current.sm [MHz]", 1))
+    assert c2 == c
     assert c["sm_mhz"] == pytest.approx((1965 + 1800) / 2)
     assert c["reasons"] == ["sw_power_cap"]
 
