@@ -176,6 +176,32 @@ const char *spec_verify_strerror(int code);
 /* Frees the handle and its workspace.  NULL is ignored. */
 void spec_verify_destroy(spec_verify_t *h);
 
+/* The same step as spec_verify_run for callers that cannot allocate device
+ * memory when they call in -- a serving runtime that plans every device
+ * buffer in advance and forbids cudaMalloc at run time (it can synchronise
+ * the device and fragment a caching allocator), or a plugin host that only
+ * passes input and output pointers.  No handle is needed and nothing is
+ * allocated: the scratch lives in one fixed device array of 32 MiB inside
+ * the library, which every GPU that loads the library holds until the
+ * process exits.  (The pages describe no such mode; this is a property of
+ * the library, not of the method.)
+ *   cfg            shape, dtype and stream, as for spec_verify_create
+ *   other arguments as for spec_verify_run
+ * The first call on a device looks up that device's copy of the array
+ * (cudaGetSymbolAddress); make it before any stream capture.  Every call
+ * reuses the same array and clears the counters it needs at its start, so
+ * calls that may overlap on the GPU (different streams, or different host
+ * threads on the same device) race and must be serialised by the caller.
+ * Errors (returned): as spec_verify_run, and SV_ERR_SHAPE if the scratch
+ * for this shape exceeds the array (about R*V*4 bytes of logits plus small
+ * tables; the Llama-8B-shaped step needs about 5.5 MiB).  Errors found on
+ * the device are not reported through a status word: the affected
+ * sequences get out_n_accepted = -1 and out_tokens = -1. */
+int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidden, const void *W_lm,
+                            const int32_t *draft_tokens, const float *q_logits,
+                            const float *uniforms, float temperature, int32_t *out_tokens,
+                            int32_t *out_n_accepted);
+
 #ifdef __cplusplus
 }
 #endif

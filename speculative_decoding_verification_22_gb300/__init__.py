@@ -38,7 +38,8 @@ EXPORTS = ("spec_verify_create", "spec_verify_run", "spec_verify_run_host",
            "spec_verify_debug_logits", "spec_verify_debug_lse",
            "spec_verify_set_wait_limit", "spec_verify_timing",
            "spec_verify_timing_read", "spec_verify_launches_per_run",
-           "spec_verify_strerror", "spec_verify_destroy")
+           "spec_verify_strerror", "spec_verify_destroy",
+           "spec_verify_run_noalloc")
 
 
 class SpecVerifyError(RuntimeError):
@@ -84,6 +85,8 @@ def load_library():
         lib.spec_verify_strerror.restype = ctypes.c_char_p
         lib.spec_verify_destroy.argtypes = [vp]
         lib.spec_verify_destroy.restype = None
+        lib.spec_verify_run_noalloc.argtypes = [ctypes.POINTER(sv_config_t), vp, vp, vp, vp,
+                                                vp, f32, vp, vp]
         for name in EXPORTS:
             if name not in ("spec_verify_strerror", "spec_verify_destroy"):
                 getattr(lib, name).restype = ctypes.c_int
@@ -188,6 +191,20 @@ def spec_verify_launches_per_run(h, temperature: float) -> int:
     if n < 0:
         raise SpecVerifyError(n, "spec_verify_launches_per_run")
     return n
+
+
+def spec_verify_run_noalloc(V, d, B, K, dtype, hidden, W_lm, draft_tokens, q_logits,
+                            uniforms, temperature: float, out_tokens, out_n_accepted,
+                            stream=None) -> None:
+    """The step without a handle or any allocation (scratch in a fixed
+    device array inside the library); for callers that cannot allocate
+    device memory at call time.  Calls that overlap on the GPU race."""
+    code = {"bf16": SV_BF16, "fp32": SV_FP32}.get(dtype, dtype)
+    cfg = sv_config_t(int(V), int(d), int(B), int(K), int(code), _stream_handle(stream))
+    _check(load_library().spec_verify_run_noalloc(
+        ctypes.byref(cfg), _ptr(hidden), _ptr(W_lm), _ptr(draft_tokens), _ptr(q_logits),
+        _ptr(uniforms), float(temperature), _ptr(out_tokens), _ptr(out_n_accepted)),
+        "spec_verify_run_noalloc")
 
 
 def spec_verify_destroy(h) -> None:

@@ -1,0 +1,72 @@
+"""The allocation-free entry point, spec_verify_run_noalloc.
+
+Some callers cannot allocate device memory at the moment they call in: a
+serving runtime that plans every device buffer up front and forbids
+cudaMalloc on its request path (cudaMalloc may synchronise the device and
+fragments a caching allocator), or a plugin host that passes the library
+nothing but input and output pointers.  For them the library offers an
+entry point without a handle whose scratch lives in a fixed device array
+inside the library.  These tests call it through the C ABI and require its
+outputs to equal those of the handle-based spec_verify_run on the same
+inputs, for two calls in a row (the second call finds the first call's data
+still in the array).  This file is collected last on purpose.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import spec_inputs as si
+import speculative_decoding_verification_22_gb300 as sv
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc_call(wl, inp, W, T, out_t, out_n):
+    cfg = sv.sv_config_t(wl.V, wl.d, wl.B, wl.K, sv.SV_BF16 if wl.dtype == "bf16" else sv.SV_FP32,
+                         torch.cuda.current_stream().cuda_stream)
+    p = lambda t: None if t is None else t.data_ptr()
+    return sv.load_library().spec_verify_run_noalloc(
+        ctypes.byref(cfg), p(inp["hidden"]), p(W), p(inp["draft"]), p(inp["q_logits"]),
+        p(inp["uniforms"]), float(T), p(out_t), p(out_n))
+
+
+@pytest.mark.parametrize("name,over,T", [
+    ("llama8b", {}, 1.0),
+    ("llama8b", {}, 0.0),
+    ("tiny", {}, 1.0),
+    ("tiny", dict(dtype="bf16", B=8, K=3, V=5000, d=1024, w_std=1 / 32), 0.7),
+])
+def test_noalloc_matches_the_handle_path_twice_in_a_row(name, over, T):
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    wl = si.workload(name, **over)
+    W = si.make_weights(wl, seed=77, device=dev)
+    eng = sv.SpecVerify(wl.V, wl.d, wl.B, wl.K, wl.dtype, device=dev)
+    for call in range(2):
+        inp = si.make_round(wl, W, seed=500 + call, T=T)
+        ref_t, ref_n = eng.run(inp["hidden"], W, inp["draft"], inp["q_logits"],
+                               inp["uniforms"], T)
+        assert eng.status() == sv.SV_OK
+        out_t = torch.full((wl.B, wl.K + 1), -7, dtype=torch.int32, device=dev)
+        out_n = torch.full((wl.B,), -7, dtype=torch.int32, device=dev)
+        assert _noalloc_call(wl, inp, W, T, out_t, out_n) == sv.SV_OK
+        torch.cuda.synchronize()
+        # token ids and accept counts are compared exactly, as everywhere
+        assert torch.equal(out_t, ref_t), (call, out_t, ref_t)
+        assert torch.equal(out_n, ref_n), (call, out_n, ref_n)
+        assert bool((out_n >= 0).all())
+    eng.close()
+
+
+def test_noalloc_rejects_shapes_beyond_its_array():
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    wl = si.workload("sweep", B=64, K=5)   # 384 rows of 128256 fp32 logits
+    small = si.workload("tiny", dtype="bf16", B=1, K=1, V=1000, d=64)
+    W = si.make_weights(small, seed=1, device=dev)
+    inp = si.make_round(small, W, seed=2)
+    out_t = torch.empty((wl.B, wl.K + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((wl.B,), dtype=torch.int32, device=dev)
+    # the shape check comes before any pointer is touched
+    assert _noalloc_call(wl, inp, W, 1.0, out_t, out_n) == sv.SV_ERR_SHAPE
