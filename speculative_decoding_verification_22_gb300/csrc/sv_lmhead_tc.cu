@@ -31,19 +31,33 @@
 namespace sv {
 namespace tc {
 
+// Ring depth and TMEM drain-ring length (tuning parameters).
+#ifndef SV_TC_MAX_STAGES
+#define SV_TC_MAX_STAGES 8
+#endif
+#ifndef SV_TC_DRAIN_SLOTS
+#define SV_TC_DRAIN_SLOTS 32
+#endif
+
 constexpr int kBK = 64;                            // k per stage (128 bytes)
 constexpr int kWSlabBytes = kTileM * kBK * 2;      // 16 KB
-constexpr int kMaxStages = 12;
+constexpr int kMaxStages = SV_TC_MAX_STAGES;
 constexpr int kNumEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * kNumEpiWarps;   // 192
-constexpr int kDrainSlots = 8;
+constexpr int kNumQWarps = 4;
+constexpr int kThreads = 64 + 32 * (kNumEpiWarps + kNumQWarps);  // 320
+constexpr int kMaxDrainSlots = 32;
+// TMEM slots of the drain ring for a column capacity NCOL (<= 512 columns)
+template <int NCOL>
+constexpr int drain_slots() {
+  return NCOL == 0 ? 1 : (512 / NCOL < SV_TC_DRAIN_SLOTS ? 512 / NCOL : SV_TC_DRAIN_SLOTS);
+}
 constexpr uint64_t kCleanupLimitNs = 2000000000ull;
 
 struct Ctl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t tfull[kDrainSlots];
-  uint64_t tempty[kDrainSlots];
+  uint64_t tfull[kMaxDrainSlots];
+  uint64_t tempty[kMaxDrainSlots];
   uint64_t teardown;
   uint32_t tmem_base;
   int abort_flag;
@@ -65,7 +79,7 @@ __device__ __forceinline__ void raise_abort(Ctl *ctl, const TcParams &P) {
 }
 
 // Streams the draft logits of one 32-entry subtile for every draft row and
-// writes their (max, sum-exp) partials of q / T.
+// writes their (max, sum-exp) partials of q / T (8 rows in flight per lane).
 __device__ __forceinline__ void q_partials(const TcParams &P, int64_t v, bool valid,
                                            int sub, int lane) {
   const int RQ = P.dims.RQ;
@@ -74,7 +88,8 @@ __device__ __forceinline__ void q_partials(const TcParams &P, int64_t v, bool va
     float x[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      x[j] = (r0 + j < RQ && valid) ? P.q_logits[static_cast<int64_t>(r0 + j) * V + v] : 0.0f;
+      x[j] = (r0 + j < RQ && valid) ? __ldg(&P.q_logits[static_cast<int64_t>(r0 + j) * V + v])
+                                    : 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (r0 + j < RQ) {
@@ -145,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
-    for (int s = 0; s < kDrainSlots; ++s) {
+    for (int s = 0; s < drain_slots<NCOL>(); ++s) {
       mbar_init(smem_u32(&ctl->tfull[s]), 1);
       mbar_init(smem_u32(&ctl->tempty[s]), kNumEpiWarps);
     }
@@ -271,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(smem_u32(&ctl->empty[stage]));
           if constexpr (NCOL != 0) {
             umma_commit(smem_u32(&ctl->tfull[slot]));
-            if (++slot == kDrainSlots) {
+            if (++slot == drain_slots<NCOL>()) {
               slot = 0;
               tphase ^= 1u;
             }
@@ -295,6 +310,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(smem_u32(&ctl->teardown), 0u, kCleanupLimitNs, &never);
     }
     __syncwarp();
+  } else if (warp >= 2 + kNumEpiWarps) {
+    // ---------------- draft-logit partials (independent of the GEMM) -------
+    if (!P.greedy && P.dims.RQ > 0) {
+      const int quad = (warp - 2 - kNumEpiWarps) & 3;
+      for (int t = t_first; t <= t_last; ++t) {
+        int kb0, kb1;
+        tile_range(t, u0, u1, nkb, kb0, kb1);
+        if (kb0 != 0) continue;  // the CTA holding a tile's first k block does it
+        const int64_t v = static_cast<int64_t>(t) * kTileM + quad * 32 + lane;
+        q_partials(P, v, v < P.dims.V, t * (kTileM / kSub) + quad, lane);
+      }
+    }
   } else {
     // ---------------- epilogue warps ----------------
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
@@ -308,7 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t v = static_cast<int64_t>(t) * kTileM + row_in_tile;
       const bool valid = v < P.dims.V;
       const int sub = t * (kTileM / kSub) + quad;
-      if (!P.greedy && kb0 == 0 && P.dims.RQ > 0) q_partials(P, v, valid, sub, lane);
       const bool split = kb0 != 0 || kb1 != nkb;
       const int bidx = kb0 == 0 ? c : c - 1;
       const int part = kb0 == 0 ? 0 : 1;
@@ -317,12 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           P.w.split_buf + (static_cast<int64_t>(bidx) * 2 + (1 - part)) * (kTileM * P.npad);
 
       if constexpr (NCOL != 0) {
-        float acc[NCOL], cmp[NCOL];
+        float acc[NCOL];
 #pragma unroll
-        for (int n = 0; n < NCOL; ++n) {
-          acc[n] = 0.0f;
-          cmp[n] = 0.0f;
-        }
+        for (int n = 0; n < NCOL; ++n) acc[n] = 0.0f;
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->tfull[slot]), tphase,
@@ -332,23 +355,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          uint32_t xr[NCOL / 16][16];
 #pragma unroll
-          for (int g = 0; g < NCOL / 16; ++g) {
-            float x[16];
-            tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(slot * NCOL + g * 16), x);
-            tmem_ld_wait();
+          for (int g = 0; g < NCOL / 16; ++g)
+            tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(slot * NCOL + g * 16), xr[g]);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {  // Kahan: acc + x with carried error
-              const float y = x[i] - cmp[g * 16 + i];
-              const float s = acc[g * 16 + i] + y;
-              cmp[g * 16 + i] = (s - acc[g * 16 + i]) - y;
-              acc[g * 16 + i] = s;
-            }
-          }
+          for (int g = 0; g < NCOL / 16; ++g) tmem_reg_fence(xr[g]);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[slot]));
-          if (++slot == kDrainSlots) {
+          // one k block's exact-product chunk (4 MMAs); the running sum is
+          // rounded to nearest, so its errors are unbiased
+#pragma unroll
+          for (int n = 0; n < NCOL; ++n) acc[n] = __fadd_rn(acc[n], __uint_as_float(xr[n / 16][n % 16]));
+          if (++slot == drain_slots<NCOL>()) {
             slot = 0;
             tphase ^= 1u;
           }
@@ -356,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         float val[NCOL];
 #pragma unroll
-        for (int n = 0; n < NCOL; ++n) val[n] = acc[n] - cmp[n];
+        for (int n = 0; n < NCOL; ++n) val[n] = acc[n];
         if (split) {
 #pragma unroll
           for (int n = 0; n < NCOL; ++n)
@@ -389,11 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) x[i] = 0.0f;
           for (int s = s_lo; s <= s_hi; ++s) {
-            float y[16];
+            uint32_t y[16];
             tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(s * P.npad + g * 16), y);
             tmem_ld_wait();
+            tmem_reg_fence(y);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] += y[i];
+            for (int i = 0; i < 16; ++i) x[i] += __uint_as_float(y[i]);
           }
           if (split) {
 #pragma unroll
@@ -465,7 +487,11 @@ TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin) {
   pl.h_box_rows = pl.npad <= 256 ? pl.npad : pl.npad / 2;
   if (pl.ncol != 0) {
     pl.nslot = 1;
-    pl.tmem_cols = static_cast<uint32_t>(tc::kDrainSlots * pl.ncol);
+    const int slots = pl.ncol == 16 ? tc::drain_slots<16>()
+                      : pl.ncol == 32 ? tc::drain_slots<32>() : tc::drain_slots<64>();
+    int cols = 32;
+    while (cols < slots * pl.ncol) cols *= 2;  // TMEM allocations are powers of two
+    pl.tmem_cols = static_cast<uint32_t>(cols);
   } else {
     // contiguous k ranges, one per accumulator; never more accumulators
     // than k blocks, so every accumulator of a tile range receives a block
