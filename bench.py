@@ -36,8 +36,8 @@ METRIC = "spec-verify rounds/s and % of HBM roofline at V=128256, d=4096, K=4, B
 UNIT = "rounds/s"
 L2_BYTES = 129 * 1024 * 1024
 NOMINAL_HBM_GBS = 8000.0
-KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_22_gb300", "csrc",
-                          "sv_lmhead_tc.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "speculative_decoding_verification_22_gb300", "csrc", f)
+               for f in ("sv_lmhead_tc.cu", "sv_internal.cuh", "sv_kernels.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lmhead_tc_llama8b.md")
 
 
@@ -121,12 +121,21 @@ def parse_clocks(text: str):
             "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def kernel_source_hash():
+    """First 16 hex digits of the SHA-256 of the contraction kernel's sources."""
+    h = hashlib.sha256()
+    for f in KERNEL_SRCS:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic():
     """DRAM bytes per launch of the contraction kernel from the committed
     ncu summary, or None if the kernel source changed since the capture."""
     try:
         text = open(TRAFFIC_FILE).read()
-        src = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+        src = kernel_source_hash()
     except OSError:
         return None
     traffic, sha = None, None
