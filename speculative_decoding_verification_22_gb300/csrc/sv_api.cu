@@ -70,7 +70,7 @@ void free_all(spec_verify *h) {
                   h->w.row_s,     h->w.seq,         h->w.chunk_mass, h->w.split_buf,
                   h->w.split_cnt, h->w.status,      h->w.abort_epoch, h->w.ticket,
                   h->w.finished,  h->w.row_count,   h->w.chunk_count, h->w.seq_flag,
-                  h->w.cand,
+                  h->w.cand,      h->w.draft_logit,
                   h->st_hidden,   h->st_draft,      h->st_q,        h->st_u,
                   h->st_tokens,   h->st_n};
   for (void *p : ptrs)
@@ -185,6 +185,7 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
             dalloc(&h->w.row_count, D.B) && dalloc(&h->w.chunk_count, D.B) &&
             dalloc(&h->w.seq_flag, D.B) &&
             dalloc(&h->w.cand, static_cast<size_t>(R) * (1 + sv::kMaxCand)) &&
+            dalloc(&h->w.draft_logit, static_cast<size_t>(D.RQ)) &&
             dalloc(&h->w.chunk_mass, static_cast<size_t>(D.B) * D.nchunk) &&
             dalloc(&h->w.split_buf, split_floats) &&
             dalloc(&h->w.split_cnt, static_cast<size_t>(h->num_sms) * 4) &&
@@ -292,6 +293,9 @@ int spec_verify_run(spec_verify_t *h, const void *hidden, const void *W_lm,
     P.tmem_cols = pl.tmem_cols;
     P.wait_limit_ns = h->wait_limit_ns;
     P.epoch = epoch;
+    P.H = hidden;
+    P.W = W_lm;
+    P.draft = draft_tokens;
     e = sv::launch_tc(pl, P, h->tmW, h->tmH, st);
   } else {
     sv::SimtParams P{};
@@ -327,6 +331,7 @@ int spec_verify_run(spec_verify_t *h, const void *hidden, const void *W_lm,
   T.epoch = epoch;
   T.wait_limit_ns = h->wait_limit_ns;
   T.split_cnt_n = h->num_sms * 4;
+  T.draft_logits_ready = h->cfg.dtype == SV_BF16 ? 1 : 0;
   if (sv::launch_tail(T, st) != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
 }

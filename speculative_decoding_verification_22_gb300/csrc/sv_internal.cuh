@@ -69,6 +69,7 @@ struct Work {
   int *chunk_count;    // [B]   chunk CTAs finished per sequence
   unsigned *seq_flag;  // [B]   epoch of the sequence's published decision
   int *cand;           // [R, 1 + kMaxCand] greedy: count, then subtile ids
+  float2 *draft_logit; // [RQ]  exact logit of each draft token (float-float)
 };
 
 // ---------------------------------------------------------------------------
@@ -368,6 +369,51 @@ __device__ __forceinline__ ff warp_sum_ff(ff x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = ff_add(x, ff_shfl_xor(x, o));
   return x;
+}
+
+// Accumulates a * b exactly into the pair (s, c): the product's rounding
+// error comes from an FMA (zero when the product is exact, as for bf16) and
+// the sum's from TwoSum.
+__device__ __forceinline__ void acc_product(float a, float b, float &s, float &c) {
+  const float p = __fmul_rn(a, b);
+  const float pe = fmaf(a, b, -p);
+  float t, e;
+  two_sum(s, p, t, e);
+  s = t;
+  c = __fadd_rn(c, __fadd_rn(e, pe));
+}
+
+// Exact-product, TwoSum-compensated dot product of two bf16 rows of length
+// d (a multiple of 8; 16-byte aligned) by one warp, over the 16-byte vectors
+// [lo, hi) of the rows, 4 vectors in flight per lane.  Returns a float-float
+// (every lane the same value).
+__device__ __forceinline__ ff dot_bf16_warp(const uint4 *h, const uint4 *w, int64_t lo,
+                                            int64_t hi, int lane) {
+  float s = 0.0f, c = 0.0f;
+  constexpr int kBatch = 4;
+  for (int64_t k0 = lo; k0 < hi; k0 += 32 * kBatch) {
+    uint4 hv[kBatch], wv[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int64_t k = k0 + j * 32 + lane;
+      hv[j] = k < hi ? __ldg(&h[k]) : make_uint4(0, 0, 0, 0);
+      wv[j] = k < hi ? __ldg(&w[k]) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const uint32_t hw[4] = {hv[j].x, hv[j].y, hv[j].z, hv[j].w};
+      const uint32_t ww[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // a bf16 value is the top half of an fp32; the widening is exact
+        acc_product(__uint_as_float(hw[e] << 16), __uint_as_float(ww[e] << 16), s, c);
+        acc_product(__uint_as_float(hw[e] & 0xffff0000u), __uint_as_float(ww[e] & 0xffff0000u),
+                    s, c);
+      }
+    }
+  }
+  const float hi2 = __fadd_rn(s, c);
+  return warp_sum_ff(ff{hi2, __fsub_rn(c, __fsub_rn(hi2, s))});
 }
 
 }  // namespace sv

@@ -23,6 +23,9 @@ struct TcParams {
   uint32_t tmem_cols;      // TMEM columns allocated per CTA
   uint64_t wait_limit_ns;  // bound of every device-side wait
   unsigned epoch;          // run counter (stamps an abort)
+  const void *H;           // [R, d] bf16 hidden states (draft-token logits)
+  const void *W;           // [V, d] bf16 LM head
+  const int32_t *draft;    // [B, K]
 };
 
 struct TcPlan {
@@ -66,6 +69,7 @@ struct TailParams {
   unsigned epoch;          // run counter
   uint64_t wait_limit_ns;  // bound of the wait for a sequence's decision
   int split_cnt_n;         // entries of w.split_cnt
+  int draft_logits_ready;  // w.draft_logit was written by the contraction
 };
 cudaError_t launch_tail(const TailParams &P, cudaStream_t stream);
 

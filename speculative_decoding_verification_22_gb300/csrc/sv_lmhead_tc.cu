@@ -321,6 +321,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t v = static_cast<int64_t>(t) * kTileM + quad * 32 + lane;
         q_partials(P, v, v < P.dims.V, t * (kTileM / kSub) + quad, lane);
       }
+      // the exact logit of every draft token (one warp each, spread over
+      // the grid); the decision pass reads them instead of recomputing
+      const int K = P.dims.K;
+      const int64_t n16 = P.dims.d / 8;
+      for (int idx = c * kNumQWarps + quad; idx < P.dims.RQ; idx += G * kNumQWarps) {
+        const int b = idx / K, i = idx - b * K;
+        const int x = P.draft[idx];
+        ff l = ff_make(NAN);
+        if (x >= 0 && static_cast<int64_t>(x) < P.dims.V) {
+          const uint4 *h = static_cast<const uint4 *>(P.H) +
+                           (static_cast<int64_t>(b) * (K + 1) + i) * n16;
+          const uint4 *w = static_cast<const uint4 *>(P.W) + static_cast<int64_t>(x) * n16;
+          l = dot_bf16_warp(h, w, 0, n16, lane);
+        }
+        if (lane == 0) P.w.draft_logit[idx] = make_float2(l.hi, l.lo);
+      }
     }
   } else {
     // ---------------- epilogue warps ----------------

@@ -156,6 +156,7 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
   w.seq = c.take<sv::SeqState>(D.B);
   w.chunk_mass = c.take<float2>(static_cast<size_t>(D.B) * D.nchunk);
   w.cand = c.take<int>(static_cast<size_t>(R) * (1 + sv::kMaxCand));
+  w.draft_logit = c.take<float2>(static_cast<size_t>(D.RQ));
   w.split_buf = c.take<float>(cfg->dtype == SV_BF16
                                   ? static_cast<size_t>(plan.grid) * 2 * sv::kTileM * plan.npad
                                   : 1);
@@ -191,6 +192,9 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
     P.tmem_cols = plan.tmem_cols;
     P.wait_limit_ns = wait_limit_ns;
     P.epoch = epoch;
+    P.H = hidden;
+    P.W = W_lm;
+    P.draft = draft_tokens;
     e = sv::launch_tc(plan, P, tmW, tmH, st);
   } else {
     sv::SimtParams P{};
@@ -221,5 +225,6 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
   T.epoch = epoch;
   T.wait_limit_ns = wait_limit_ns;
   T.split_cnt_n = sms * 4;
+  T.draft_logits_ready = cfg->dtype == SV_BF16 ? 1 : 0;
   return sv::launch_tail(T, st) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -6,9 +6,10 @@
 //
 //  row CTAs (tickets 0 .. R+RQ-1), one per target row (logits / T) and per
 //      draft row (q_logits / T): combine the per-32-entry softmax partials
-//      into the row maximum M and sum S = sum_v exp(x_v - M).  The last row
-//      CTA of a sequence becomes its decider: it recomputes the K
-//      draft-token logits with a compensated dot product and walks the
+//      into the row maximum M and sum S = sum_v exp(x_v - M); a draft-row
+//      CTA also recomputes its draft token's logit with a compensated dot
+//      product.  The last row CTA of a sequence becomes its decider: it
+//      evaluates the K accept thresholds in parallel and walks the
 //      draft left to right, x_{i+1} surviving iff u_i < p_{i+1}(x) /
 //      q_{i+1}(x) ("Speculative Decoding: Two Models, One Voice", "The idea"
 //      step 3; "Speculative Decoding" (library wiki), "One speculation
@@ -120,18 +121,6 @@ __device__ __forceinline__ void st_ff(float2 *p, ff v) { *p = make_float2(v.hi, 
 // Dot products and the greedy argmax
 // ---------------------------------------------------------------------------
 
-// Accumulates a * b exactly into the pair (s, c): the product's rounding
-// error comes from an FMA (zero when the product is exact, as for bf16) and
-// the sum's from TwoSum.
-__device__ __forceinline__ void acc_product(float a, float b, float &s, float &c) {
-  const float p = __fmul_rn(a, b);
-  const float pe = fmaf(a, b, -p);
-  float t, e;
-  two_sum(s, p, t, e);
-  s = t;
-  c = __fadd_rn(c, __fadd_rn(e, pe));
-}
-
 // Part `part` of `nparts` (contiguous ranges of 16-byte vectors) of the dot
 // product of hidden row `hrow` with W row `wrow`, by one warp with 16-byte
 // loads (rows are 16-byte aligned: d is a multiple of 8 for bf16, of 4 for
@@ -150,28 +139,7 @@ __device__ ff dot_warp(const TailParams &P, int64_t hrow, int64_t wrow, int lane
     const uint4 *w =
         reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.W) + wrow * d);
     const int64_t n = d / 8;
-    const int64_t lo = n * part / nparts, hi = n * (part + 1) / nparts;
-    for (int64_t k0 = lo; k0 < hi; k0 += 32 * kBatch) {
-      uint4 hv[kBatch], wv[kBatch];
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int64_t k = k0 + j * 32 + lane;
-        hv[j] = k < hi ? __ldg(&h[k]) : make_uint4(0, 0, 0, 0);
-        wv[j] = k < hi ? __ldg(&w[k]) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const __nv_bfloat162 *hb = reinterpret_cast<const __nv_bfloat162 *>(&hv[j]);
-        const __nv_bfloat162 *wb = reinterpret_cast<const __nv_bfloat162 *>(&wv[j]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 hf = __bfloat1622float2(hb[e]);
-          const float2 wf = __bfloat1622float2(wb[e]);
-          acc_product(hf.x, wf.x, s, c);
-          acc_product(hf.y, wf.y, s, c);
-        }
-      }
-    }
+    return dot_bf16_warp(h, w, n * part / nparts, n * (part + 1) / nparts, lane);
   } else {
     const float4 *h = reinterpret_cast<const float4 *>(static_cast<const float *>(P.H) + hrow * d);
     const float4 *w = reinterpret_cast<const float4 *>(static_cast<const float *>(P.W) + wrow * d);
@@ -329,7 +297,7 @@ __device__ void decide(const TailParams &P, int b) {
   const int R = P.dims.R;
   const int64_t out0 = static_cast<int64_t>(b) * rows;
   __shared__ ff s_l[SV_MAX_K];           // draft-token logits
-  __shared__ ff s_part[kTailWarps];
+  __shared__ int s_acc[SV_MAX_K];        // 1 accept, 0 reject, -1 non-finite
   __shared__ float s_lp_m[SV_MAX_K + 1], s_lq_m[SV_MAX_K];    // row maxima
   __shared__ ff s_lp_s[SV_MAX_K + 1], s_lq_s[SV_MAX_K];       // row sums
   __shared__ float s_ql[SV_MAX_K], s_u[SV_MAX_K + 1];
@@ -359,6 +327,7 @@ __device__ void decide(const TailParams &P, int b) {
       s_lq_m[i] = __ldcg(&P.w.row_m[rq]);
       s_lq_s[i] = ld_ff(&P.w.row_s[rq]);
       s_ql[i] = P.q_logits[(static_cast<int64_t>(b) * K + i) * V + x];
+      s_l[i] = ld_ff(&P.w.draft_logit[static_cast<int64_t>(b) * K + i]);
       const bool fin = isfinite(s_lq_m[i]) && s_lq_s[i].hi > 0.0f && s_lq_s[i].hi < INFINITY;
       if (!fin) atomicCAS(&s_err, 0, SV_ERR_NONFINITE);
     }
@@ -375,22 +344,15 @@ __device__ void decide(const TailParams &P, int b) {
   }
   if (s_err == 0) {
     if (!P.greedy) {
-      // the K draft-token logits, each split over wpr warps
-      const int wpr = K > 0 ? (kTailWarps / K > 0 ? kTailWarps / K : 1) : 1;
-      const int per = kTailWarps / wpr;
-      for (int i0 = 0; i0 < K; i0 += per) {
-        const int i = i0 + warp / wpr;
-        if (i < K && warp / wpr < per) {
-          const ff l = dot_warp(P, out0 + i, s_x[i], lane, warp % wpr, wpr);
-          if (lane == 0) s_part[warp] = l;
-        }
-        __syncthreads();
-        if (threadIdx.x < per && i0 + static_cast<int>(threadIdx.x) < K) {
-          ff l = s_part[threadIdx.x * wpr];
-          for (int p = 1; p < wpr; ++p) l = ff_add(l, s_part[threadIdx.x * wpr + p]);
-          s_l[i0 + threadIdx.x] = l;
-        }
-        __syncthreads();
+      // accept thresholds of the K positions, one thread each
+      if (threadIdx.x < K) {
+        const int i = threadIdx.x;
+        const float T = static_cast<float>(P.T);
+        const ff l = s_l[i];
+        const ff lp = ff_add(ff_div_f(l, T), ff_make(-s_lp_m[i]));
+        const ff lq = ff_add(ff_div_f(ff_make(s_ql[i]), T), ff_make(-s_lq_m[i]));
+        const float ratio = ff_to_f(ff_div(s_lq_s[i], s_lp_s[i]));
+        s_acc[i] = isfinite(l.hi) ? (s_u[i] < accept_threshold(lp, lq, ratio) ? 1 : 0) : -1;
       }
     } else {
       for (int i = warp; i < rows; i += kTailWarps) {
@@ -406,17 +368,12 @@ __device__ void decide(const TailParams &P, int b) {
     st.mode = kModeSkip;
     if (err == 0 && !P.greedy) {
       int n = K, mode = kModeP;
-      const float T = static_cast<float>(P.T);
       for (int i = 0; i < K; ++i) {
-        if (!isfinite(s_l[i].hi)) {
+        if (s_acc[i] < 0) {
           err = SV_ERR_NONFINITE;
           break;
         }
-        const ff lp = ff_add(ff_div_f(s_l[i], T), ff_make(-s_lp_m[i]));
-        const ff lq = ff_add(ff_div_f(ff_make(s_ql[i]), T), ff_make(-s_lq_m[i]));
-        const float ratio = ff_to_f(ff_div(s_lq_s[i], s_lp_s[i]));
-        const float t = accept_threshold(lp, lq, ratio);
-        if (s_u[i] < t) {
+        if (s_acc[i]) {
           P.out_tokens[out0 + i] = s_x[i];
         } else {
           n = i;
@@ -656,6 +613,25 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailParams P) 
       const int nc = s_nc;
       for (int k = threadIdx.x; k < nc && k < kMaxCand; k += kTailThreads) cand[1 + k] = s_cand[k];
       if (threadIdx.x == 0) cand[0] = nc;
+    }
+    if (qrow && !P.greedy && !P.draft_logits_ready) {
+      // the exact logit of this position's draft token, split over the
+      // CTA's warps (fixed order), so the decider only reads it (the
+      // tensor-core contraction computes these itself)
+      const int i = (t - R) - b * K;
+      const int x = P.draft[static_cast<int64_t>(b) * K + i];
+      if (x >= 0 && static_cast<int64_t>(x) < P.dims.V) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const ff part = dot_warp(P, static_cast<int64_t>(b) * (K + 1) + i, x, lane, warp,
+                                 kTailWarps);
+        if (lane == 0) s_wff[warp] = part;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          ff l = s_wff[0];
+          for (int w2 = 1; w2 < kTailWarps; ++w2) l = ff_add(l, s_wff[w2]);
+          st_ff(&P.w.draft_logit[t - R], l);
+        }
+      }
     }
     if (threadIdx.x == 0) {
       P.w.row_m[t] = M;
