@@ -70,6 +70,7 @@ void free_all(spec_verify *h) {
                   h->w.row_s,     h->w.seq,         h->w.chunk_mass, h->w.split_buf,
                   h->w.split_cnt, h->w.status,      h->w.abort_epoch, h->w.ticket,
                   h->w.finished,  h->w.row_count,   h->w.chunk_count, h->w.seq_flag,
+                  h->w.seq_final,
                   h->w.cand,      h->w.draft_logit,
                   h->st_hidden,   h->st_draft,      h->st_q,        h->st_u,
                   h->st_tokens,   h->st_n};
@@ -85,17 +86,32 @@ bool dalloc(T **p, size_t count) {
   return cudaMalloc(reinterpret_cast<void **>(p), count * sizeof(T)) == cudaSuccess;
 }
 
-int encode_2d(CUtensorMap *map, const void *base, int64_t inner, int64_t outer,
-              uint32_t box_inner, uint32_t box_outer) {
+// TMA map of a bf16 [outer, inner] row-major matrix.  chunks == 1: 2-D,
+// box {64, box_rows}.  chunks > 1: 3-D view {64, outer, inner / 64} (the
+// k-chunk dimension has a 128-byte stride), box {64, box_rows, chunks}, so
+// one copy brings `chunks` consecutive 64-wide k blocks of box_rows rows.
+int encode_w(CUtensorMap *map, const void *base, int64_t inner, int64_t outer,
+             uint32_t box_rows, int chunks) {
   auto fn = encode_fn();
   if (!fn) return SV_ERR_CUDA;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (chunks > 1) {
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(outer), static_cast<cuuint64_t>(inner / 64)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, static_cast<cuuint32_t>(chunks)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -184,6 +200,7 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
             dalloc(&h->w.ticket, 1) && dalloc(&h->w.finished, 1) &&
             dalloc(&h->w.row_count, D.B) && dalloc(&h->w.chunk_count, D.B) &&
             dalloc(&h->w.seq_flag, D.B) &&
+            dalloc(&h->w.seq_final, D.B) &&
             dalloc(&h->w.cand, static_cast<size_t>(R) * (1 + sv::kMaxCand)) &&
             dalloc(&h->w.draft_logit, static_cast<size_t>(D.RQ)) &&
             dalloc(&h->w.chunk_mass, static_cast<size_t>(D.B) * D.nchunk) &&
@@ -205,6 +222,7 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
          cudaMemset(h->w.row_count, 0, sizeof(int) * D.B) == cudaSuccess &&
          cudaMemset(h->w.chunk_count, 0, sizeof(int) * D.B) == cudaSuccess &&
          cudaMemset(h->w.seq_flag, 0, sizeof(unsigned) * D.B) == cudaSuccess &&
+         cudaMemset(h->w.seq_final, 0, sizeof(int) * D.B) == cudaSuccess &&
          cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     free_all(h);
@@ -269,11 +287,12 @@ int spec_verify_run(spec_verify_t *h, const void *hidden, const void *W_lm,
   if (h->cfg.dtype == SV_BF16) {
     const sv::TcPlan &pl = h->plan;
     if (h->tmW_ptr != W_lm) {
-      if (encode_2d(&h->tmW, W_lm, D.d, D.V, 64, sv::kTileM) != SV_OK) return SV_ERR_CUDA;
+      if (encode_w(&h->tmW, W_lm, D.d, D.V, sv::kTileM, pl.chunks) != SV_OK) return SV_ERR_CUDA;
       h->tmW_ptr = W_lm;
     }
     if (h->tmH_ptr != hidden) {
-      if (encode_2d(&h->tmH, hidden, D.d, D.R, 64, static_cast<uint32_t>(pl.h_box_rows)) != SV_OK)
+      if (encode_w(&h->tmH, hidden, D.d, D.R, static_cast<uint32_t>(pl.h_box_rows), pl.chunks) !=
+          SV_OK)
         return SV_ERR_CUDA;
       h->tmH_ptr = hidden;
     }
@@ -285,6 +304,7 @@ int spec_verify_run(spec_verify_t *h, const void *hidden, const void *W_lm,
     P.greedy = greedy ? 1 : 0;
     P.npad = pl.npad;
     P.nkb = pl.nkb;
+    P.chunks = pl.chunks;
     P.stages = pl.stages;
     P.stage_bytes = pl.stage_bytes;
     P.h_boxes = pl.h_boxes;

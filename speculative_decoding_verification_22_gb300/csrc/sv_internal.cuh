@@ -68,6 +68,7 @@ struct Work {
   int *row_count;      // [B]   row CTAs finished per sequence
   int *chunk_count;    // [B]   chunk CTAs finished per sequence
   unsigned *seq_flag;  // [B]   epoch of the sequence's published decision
+  int *seq_final;      // [B]   decision + chunk-phase arrivals, poison bit
   int *cand;           // [R, 1 + kMaxCand] greedy: count, then subtile ids
   float2 *draft_logit; // [RQ]  exact logit of each draft token (float-float)
 };
@@ -173,6 +174,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m,
       : "memory");
 }
 
+// 3-D tiled load: box {c0.., c1.., c2..}; same alignment rule on c0.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, int32_t c0,
+                                            int32_t c1, int32_t c2, uint32_t bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05 (TMEM + tensor cores), cta_group::1
 // ---------------------------------------------------------------------------
@@ -209,6 +221,17 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc,
 }
 // Arrives once on `bar` when all tcgen05.mma issued so far by this thread
 // have completed.
+// One lane of the (converged) warp; the same lane every time.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

@@ -15,6 +15,7 @@ struct TcParams {
   int greedy;              // T == 0
   int npad;                // MMA N = R rounded up to 16
   int nkb;                 // 64-wide k blocks per tile
+  int chunks;              // k blocks per stage (one 3-D TMA box when > 1)
   int stages;              // shared-memory ring depth
   int stage_bytes;         // W slab + H slab, multiple of 1024
   int h_boxes;             // TMA boxes per H slab (1 or 2)
@@ -29,7 +30,7 @@ struct TcParams {
 };
 
 struct TcPlan {
-  int npad, ncol, nkb, stage_bytes, stages, smem, h_boxes, h_box_rows, nslot;
+  int npad, ncol, nkb, chunks, stage_bytes, stages, smem, h_boxes, h_box_rows, nslot;
   uint32_t tmem_cols;
   int grid, threads;
   bool valid;

@@ -38,6 +38,15 @@ namespace tc {
 #ifndef SV_TC_DRAIN_SLOTS
 #define SV_TC_DRAIN_SLOTS 32
 #endif
+#ifndef SV_TC_STAGES_C2
+#define SV_TC_STAGES_C2 5
+#endif
+#ifndef SV_TC_STAGES_C4
+#define SV_TC_STAGES_C4 2
+#endif
+#ifndef SV_TC_MAX_CHUNKS
+#define SV_TC_MAX_CHUNKS 2
+#endif
 
 constexpr int kBK = 64;                            // k per stage (128 bytes)
 constexpr int kWSlabBytes = kTileM * kBK * 2;      // 16 KB
@@ -65,11 +74,13 @@ struct Ctl {
   int consumed;
 };
 
-__device__ __forceinline__ void tile_range(int t, int64_t u0, int64_t u1, int nkb,
+// The k-block range [kb0, kb1) of tile t inside this CTA's unit range
+// [u0, u1); a unit is a group of `chunks` k blocks (ngr groups per tile).
+__device__ __forceinline__ void tile_range(int t, int64_t u0, int64_t u1, int ngr, int chunks,
                                            int &kb0, int &kb1) {
-  const int64_t tb = static_cast<int64_t>(t) * nkb;
-  kb0 = static_cast<int>((u0 > tb ? u0 : tb) - tb);
-  kb1 = static_cast<int>((u1 < tb + nkb ? u1 : tb + nkb) - tb);
+  const int64_t tb = static_cast<int64_t>(t) * ngr;
+  kb0 = static_cast<int>((u0 > tb ? u0 : tb) - tb) * chunks;
+  kb1 = static_cast<int>((u1 < tb + ngr ? u1 : tb + ngr) - tb) * chunks;
 }
 
 __device__ __forceinline__ void raise_abort(Ctl *ctl, const TcParams &P) {
@@ -149,11 +160,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int nkb = P.nkb;
-  const int64_t U = static_cast<int64_t>(P.dims.ntile) * nkb;
+  const int C = P.chunks;
+  const int ngr = nkb / C;
+  const int64_t U = static_cast<int64_t>(P.dims.ntile) * ngr;
   const int G = gridDim.x, c = blockIdx.x;
   const int64_t u0 = U * c / G, u1 = U * (c + 1) / G;
-  const int t_first = static_cast<int>(u0 / nkb);
-  const int t_last = static_cast<int>((u1 - 1) / nkb);
+  const int t_first = static_cast<int>(u0 / ngr);
+  const int t_last = static_cast<int>((u1 - 1) / ngr);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.stages; ++s) {
@@ -194,14 +207,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_h = policy_evict_last();
-      const uint32_t tx = static_cast<uint32_t>(kWSlabBytes + P.npad * 128);
+      const uint32_t tx = static_cast<uint32_t>(C * (kWSlabBytes + P.npad * 128));
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       for (int t = t_first; t <= t_last; ++t) {
         int kb0, kb1;
-        tile_range(t, u0, u1, nkb, kb0, kb1);
+        tile_range(t, u0, u1, ngr, C, kb0, kb1);
         bool ok = true;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; kb += C) {
           if (!mbar_wait(smem_u32(&ctl->empty[stage]), phase ^ 1u, P.wait_limit_ns, abort)) {
             raise_abort(ctl, P);
             ok = false;
@@ -210,10 +223,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sbase = base + static_cast<uint32_t>(stage * P.stage_bytes);
           const uint32_t full = smem_u32(&ctl->full[stage]);
           mbar_arrive_expect_tx(full, tx);
-          tma_load_2d(sbase, &tmW, kb * kBK, t * kTileM, full, pol_w);
-          for (int hb = 0; hb < P.h_boxes; ++hb)
-            tma_load_2d(sbase + kWSlabBytes + static_cast<uint32_t>(hb * P.h_box_rows * 128),
-                        &tmH, kb * kBK, hb * P.h_box_rows, full, pol_h);
+          if (C > 1) {
+            // C consecutive k blocks in one 3-D box: 128 rows x (C x 128 B)
+            // contiguous runs; in shared memory C [128 x 64] swizzled tiles
+            tma_load_3d(sbase, &tmW, 0, t * kTileM, kb, full, pol_w);
+            tma_load_3d(sbase + static_cast<uint32_t>(C * kWSlabBytes), &tmH, 0, 0, kb, full,
+                        pol_h);
+          } else {
+            tma_load_2d(sbase, &tmW, kb * kBK, t * kTileM, full, pol_w);
+            for (int hb = 0; hb < P.h_boxes; ++hb)
+              tma_load_2d(sbase + kWSlabBytes + static_cast<uint32_t>(hb * P.h_box_rows * 128),
+                          &tmH, kb * kBK, hb * P.h_box_rows, full, pol_h);
+          }
           ++issued;
           if (++stage == P.stages) {
             stage = 0;
@@ -227,84 +248,114 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      int stage = 0, consumed = 0;
-      uint32_t sphase = 0;
-      int slot = 0;
-      uint32_t tphase = 0;
-      bool ok = true;
-      for (int t = t_first; t <= t_last && ok; ++t) {
-        int kb0, kb1;
-        tile_range(t, u0, u1, nkb, kb0, kb1);
-        if constexpr (NCOL == 0) {
-          if (!mbar_wait(smem_u32(&ctl->tempty[0]), tphase ^ 1u, P.wait_limit_ns, abort)) {
-            raise_abort(ctl, P);
+    // The whole warp runs the loop and waits together, so the stage/slot
+    // state and the descriptors stay warp-uniform; one elected lane issues
+    // the MMAs and commits.  (Issued from a single-lane branch the same
+    // sequence costs several times more per k block, which made the issuer,
+    // not HBM, the limit for small N.)
+    int stage = 0, consumed = 0;
+    uint32_t sphase = 0;
+    int slot = 0;
+    uint32_t tphase = 0;
+    bool ok = true;
+    // descriptor address fields are (addr >> 4); shared addresses stay
+    // below 256 KB, so offsets add without carrying out of the field
+    const uint64_t adesc0 = sw128_desc(base);
+    const uint64_t bdesc0 = sw128_desc(base + static_cast<uint32_t>(C * kWSlabBytes));
+    const uint32_t stage16 = static_cast<uint32_t>(P.stage_bytes >> 4);
+    const uint32_t bchunk16 = static_cast<uint32_t>((P.npad * 128) >> 4);
+    const uint32_t idesc = idesc_bf16(kTileM, NCOL != 0 ? P.npad : (P.npad <= 256 ? P.npad : 256));
+    const uint32_t idesc2 = idesc_bf16(kTileM, P.npad > 256 ? P.npad - 256 : 16);
+    for (int t = t_first; t <= t_last && ok; ++t) {
+      int kb0, kb1;
+      tile_range(t, u0, u1, ngr, C, kb0, kb1);
+      if constexpr (NCOL == 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->tempty[0]), tphase ^ 1u,
+                                               P.wait_limit_ns, abort))) {
+          if (lane == 0) raise_abort(ctl, P);
+          break;
+        }
+        tc_fence_after();
+      }
+      uint64_t adesc = 0, bdesc = 0;
+      int j = 0;  // chunk within the current stage (kb0 is a multiple of C)
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if constexpr (NCOL != 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->tempty[slot]), tphase ^ 1u,
+                                                 P.wait_limit_ns, abort))) {
+            if (lane == 0) raise_abort(ctl, P);
+            ok = false;
             break;
           }
-          tc_fence_after();
         }
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if constexpr (NCOL != 0) {
-            if (!mbar_wait(smem_u32(&ctl->tempty[slot]), tphase ^ 1u, P.wait_limit_ns, abort)) {
-              raise_abort(ctl, P);
-              ok = false;
-              break;
-            }
-          }
-          if (!mbar_wait(smem_u32(&ctl->full[stage]), sphase, P.wait_limit_ns, abort)) {
-            raise_abort(ctl, P);
+        if (j == 0) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->full[stage]), sphase,
+                                                 P.wait_limit_ns, abort))) {
+            if (lane == 0) raise_abort(ctl, P);
             ok = false;
             break;
           }
           ++consumed;
-          tc_fence_after();
-          const uint32_t sbase = base + static_cast<uint32_t>(stage * P.stage_bytes);
-          const uint64_t adesc = sw128_desc(sbase);
-          const uint64_t bdesc = sw128_desc(sbase + kWSlabBytes);
-          if constexpr (NCOL != 0) {
-            const uint32_t d = tmem + static_cast<uint32_t>(slot * NCOL);
-            const uint32_t idesc = idesc_bf16(kTileM, P.npad);
+          adesc = adesc0 + static_cast<uint64_t>(stage) * stage16;
+          bdesc = bdesc0 + static_cast<uint64_t>(stage) * stage16;
+        }
+        tc_fence_after();
+        if constexpr (NCOL != 0) {
+          const uint32_t d = tmem + static_cast<uint32_t>(slot * NCOL);
+          if (elect_one()) {
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
               umma_bf16(d, adesc + 2u * k, bdesc + 2u * k, idesc, k > 0 ? 1u : 0u);
-          } else {
-            const int s = static_cast<int>(static_cast<int64_t>(kb) * P.nslot / nkb);
-            const bool first =
-                kb == kb0 || static_cast<int>(static_cast<int64_t>(kb - 1) * P.nslot / nkb) != s;
-            const uint32_t d = tmem + static_cast<uint32_t>(s * P.npad);
-            const int n1 = P.npad <= 256 ? P.npad : 256;
-            const uint32_t idesc1 = idesc_bf16(kTileM, n1);
-            const uint32_t idesc2 = idesc_bf16(kTileM, P.npad > 256 ? P.npad - 256 : 16);
-            const uint64_t bdesc2 = sw128_desc(sbase + kWSlabBytes + 256u * 128u);
+            // release the stage first: the producer's refill is on the
+            // critical path, the drain of this slot is not
+            if (j == C - 1) umma_commit(smem_u32(&ctl->empty[stage]));
+            umma_commit(smem_u32(&ctl->tfull[slot]));
+          }
+          __syncwarp();
+          if (++slot == drain_slots<NCOL>()) {
+            slot = 0;
+            tphase ^= 1u;
+          }
+        } else {
+          const int s = static_cast<int>(static_cast<int64_t>(kb) * P.nslot / nkb);
+          const bool first =
+              kb == kb0 || static_cast<int>(static_cast<int64_t>(kb - 1) * P.nslot / nkb) != s;
+          const uint32_t d = tmem + static_cast<uint32_t>(s * P.npad);
+          // npad > 256 only with single-chunk stages
+          const uint64_t bdesc2 = bdesc + ((256u * 128u) >> 4);
+          if (elect_one()) {
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
               const uint32_t acc = (k > 0 || !first) ? 1u : 0u;
-              umma_bf16(d, adesc + 2u * k, bdesc + 2u * k, idesc1, acc);
+              umma_bf16(d, adesc + 2u * k, bdesc + 2u * k, idesc, acc);
               if (P.npad > 256) umma_bf16(d + 256u, adesc + 2u * k, bdesc2 + 2u * k, idesc2, acc);
             }
+            if (j == C - 1) umma_commit(smem_u32(&ctl->empty[stage]));
           }
-          umma_commit(smem_u32(&ctl->empty[stage]));
-          if constexpr (NCOL != 0) {
-            umma_commit(smem_u32(&ctl->tfull[slot]));
-            if (++slot == drain_slots<NCOL>()) {
-              slot = 0;
-              tphase ^= 1u;
-            }
-          }
+          __syncwarp();
+        }
+        adesc += kWSlabBytes >> 4;
+        bdesc += bchunk16;
+        if (++j == C) {
+          j = 0;
           if (++stage == P.stages) {
             stage = 0;
             sphase ^= 1u;
           }
         }
-        if constexpr (NCOL == 0) {
-          if (ok) {
-            umma_commit(smem_u32(&ctl->tfull[0]));
-            tphase ^= 1u;
-          }
+      }
+      if constexpr (NCOL == 0) {
+        if (ok) {
+          if (elect_one()) umma_commit(smem_u32(&ctl->tfull[0]));
+          __syncwarp();
+          tphase ^= 1u;
         }
       }
-      ctl->consumed = consumed;
-      // every MMA issued by this thread must finish before TMEM is freed
+    }
+    if (lane == 0) ctl->consumed = consumed;
+    // every MMA issued by the elected lane must finish before TMEM is
+    // freed; a commit tracks the MMAs of the thread that issues it
+    if (elect_one()) {
       umma_commit(smem_u32(&ctl->teardown));
       const int never = 0;
       mbar_wait(smem_u32(&ctl->teardown), 0u, kCleanupLimitNs, &never);
@@ -316,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int quad = (warp - 2 - kNumEpiWarps) & 3;
       for (int t = t_first; t <= t_last; ++t) {
         int kb0, kb1;
-        tile_range(t, u0, u1, nkb, kb0, kb1);
+        tile_range(t, u0, u1, ngr, C, kb0, kb1);
         if (kb0 != 0) continue;  // the CTA holding a tile's first k block does it
         const int64_t v = static_cast<int64_t>(t) * kTileM + quad * 32 + lane;
         q_partials(P, v, v < P.dims.V, t * (kTileM / kSub) + quad, lane);
@@ -347,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tphase = 0;
     for (int t = t_first; t <= t_last; ++t) {
       int kb0, kb1;
-      tile_range(t, u0, u1, nkb, kb0, kb1);
+      tile_range(t, u0, u1, ngr, C, kb0, kb1);
       const int64_t v = static_cast<int64_t>(t) * kTileM + row_in_tile;
       const bool valid = v < P.dims.V;
       const int sub = t * (kTileM / kSub) + quad;
@@ -490,10 +541,26 @@ TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin) {
   pl.npad = ((dims.R + 15) / 16) * 16;
   pl.ncol = pl.npad <= 16 ? 16 : pl.npad <= 32 ? 32 : pl.npad <= 64 ? 64 : 0;
   pl.nkb = static_cast<int>((dims.d + tc::kBK - 1) / tc::kBK);
-  pl.stage_bytes = ((tc::kWSlabBytes + pl.npad * 128 + 1023) / 1024) * 1024;
   const int ctl_bytes = static_cast<int>(sizeof(tc::Ctl));
-  int stages = (smem_optin - 1024 - ctl_bytes) / pl.stage_bytes;
-  if (stages > tc::kMaxStages) stages = tc::kMaxStages;
+  const int budget = smem_optin - 1024 - ctl_bytes;
+  // Stages of C consecutive k blocks, loaded as one 3-D box (longer
+  // contiguous DRAM runs per W row); needs d a multiple of 64 * C and the
+  // hidden slab in one box (npad <= 256).
+  pl.chunks = 1;
+  if (dims.d % tc::kBK == 0 && pl.npad <= 256) {
+    for (int cand = SV_TC_MAX_CHUNKS; cand >= 2; cand /= 2) {
+      const int sb = ((cand * (tc::kWSlabBytes + pl.npad * 128) + 1023) / 1024) * 1024;
+      if (pl.nkb % cand == 0 && 2 * sb <= budget) {
+        pl.chunks = cand;
+        break;
+      }
+    }
+  }
+  const int max_stages = pl.chunks == 4 ? SV_TC_STAGES_C4
+                         : pl.chunks == 2 ? SV_TC_STAGES_C2 : tc::kMaxStages;
+  pl.stage_bytes = ((pl.chunks * (tc::kWSlabBytes + pl.npad * 128) + 1023) / 1024) * 1024;
+  int stages = budget / pl.stage_bytes;
+  if (stages > max_stages) stages = max_stages;
   pl.stages = stages;
   pl.smem = stages * pl.stage_bytes + ctl_bytes + 1024;
   // above half of the SM's shared memory: exactly one CTA per SM, so the

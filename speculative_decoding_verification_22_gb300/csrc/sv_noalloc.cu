@@ -62,8 +62,8 @@ struct Carver {
   }
 };
 
-int encode_2d_local(CUtensorMap *map, const void *ptr, int64_t inner, int64_t outer,
-                    uint32_t box_inner, uint32_t box_outer) {
+int encode_w_local(CUtensorMap *map, const void *ptr, int64_t inner, int64_t outer,
+                   uint32_t box_rows, int chunks) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
     void *p = nullptr;
@@ -74,15 +74,25 @@ int encode_2d_local(CUtensorMap *map, const void *ptr, int64_t inner, int64_t ou
       return SV_ERR_CUDA;
     fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   }
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
-             ? SV_OK
-             : SV_ERR_CUDA;
+  CUresult r;
+  if (chunks > 1) {  // same 3-D view as the handle path
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(outer), static_cast<cuuint64_t>(inner / 64)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, static_cast<cuuint32_t>(chunks)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS ? SV_OK : SV_ERR_CUDA;
 }
 
 }  // namespace
@@ -147,6 +157,7 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
   w.row_count = c.take<int>(D.B);
   w.chunk_count = c.take<int>(D.B);
   w.seq_flag = c.take<unsigned>(D.B);
+  w.seq_final = c.take<int>(D.B);
   const size_t zero_bytes = c.off;
   w.logits = c.take<float>(static_cast<size_t>(R) * D.V);
   w.part_p = c.take<float2>(static_cast<size_t>(R) * D.nsub);
@@ -172,9 +183,9 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
   cudaError_t e;
   if (cfg->dtype == SV_BF16) {
     CUtensorMap tmW, tmH;
-    if (encode_2d_local(&tmW, W_lm, D.d, D.V, 64, sv::kTileM) != SV_OK ||
-        encode_2d_local(&tmH, hidden, D.d, D.R, 64, static_cast<uint32_t>(plan.h_box_rows)) !=
-            SV_OK)
+    if (encode_w_local(&tmW, W_lm, D.d, D.V, sv::kTileM, plan.chunks) != SV_OK ||
+        encode_w_local(&tmH, hidden, D.d, D.R, static_cast<uint32_t>(plan.h_box_rows),
+                       plan.chunks) != SV_OK)
       return SV_ERR_CUDA;
     sv::TcParams P{};
     P.dims = D;
@@ -184,6 +195,7 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
     P.greedy = greedy ? 1 : 0;
     P.npad = plan.npad;
     P.nkb = plan.nkb;
+    P.chunks = plan.chunks;
     P.stages = plan.stages;
     P.stage_bytes = plan.stage_bytes;
     P.h_boxes = plan.h_boxes;

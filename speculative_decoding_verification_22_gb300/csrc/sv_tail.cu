@@ -290,7 +290,26 @@ __device__ __forceinline__ float accept_threshold(ff lp, ff lq, float ratio) {
 // ---------------------------------------------------------------------------
 // Decider (one CTA, the last row CTA of sequence b)
 // ---------------------------------------------------------------------------
-__device__ void decide(const TailParams &P, int b) {
+// Per-sequence finalisation.  The decision (row phase) and the last chunk
+// CTA of the residual-mass phase both arrive on seq_final[b]; the second to
+// arrive finalises the sequence.  A chunk CTA whose wait for the decision
+// ran out contributed no mass, so it sets the poison bit and the sequence
+// is reported as -1 instead of drawing from an incomplete distribution.
+constexpr int kArrivalMask = 0xffff;
+constexpr int kPoisoned = 1 << 16;
+enum : int { kFinNone = 0, kFinSelect = 1, kFinPoison = 2 };
+
+// thread 0 only
+__device__ __forceinline__ int arrive_final(const TailParams &P, int b) {
+  const int prev = atomicAdd(&P.w.seq_final[b], 1);
+  if ((prev & kArrivalMask) != 1) return kFinNone;
+  P.w.seq_final[b] = 0;  // both arrived: rewind for the next launch
+  __threadfence();
+  return (prev & kPoisoned) ? kFinPoison : kFinSelect;
+}
+
+// Returns (to every thread of the block) what this CTA must finalise.
+__device__ int decide(const TailParams &P, int b) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = P.dims.K, rows = K + 1;
   const int64_t V = P.dims.V;
@@ -302,7 +321,7 @@ __device__ void decide(const TailParams &P, int b) {
   __shared__ ff s_lp_s[SV_MAX_K + 1], s_lq_s[SV_MAX_K];       // row sums
   __shared__ float s_ql[SV_MAX_K], s_u[SV_MAX_K + 1];
   __shared__ int s_x[SV_MAX_K], s_arg[SV_MAX_K + 1];
-  __shared__ int s_err;
+  __shared__ int s_err, s_fin;
 
   if (threadIdx.x == 0) s_err = 0;
   __syncthreads();
@@ -426,8 +445,14 @@ __device__ void decide(const TailParams &P, int b) {
     P.w.seq[b] = st;
     __threadfence();
     *reinterpret_cast<volatile unsigned *>(&P.w.seq_flag[b]) = P.epoch;
+    s_fin = kFinNone;
+    if (!P.greedy) {
+      __threadfence();
+      s_fin = arrive_final(P, b);
+    }
   }
-  __syncwarp();
+  __syncthreads();
+  return s_fin;
 }
 
 // ---------------------------------------------------------------------------
@@ -534,6 +559,24 @@ __device__ void select_token(const TailParams &P, int b, SeqState st) {
 // ---------------------------------------------------------------------------
 // The fused tail kernel
 // ---------------------------------------------------------------------------
+// Carries out what arrive_final decided (block-wide).
+__device__ void finalize_sequence(const TailParams &P, int b, int fin) {
+  if (fin == kFinPoison) {
+    if (threadIdx.x == 0) {
+      const int rows = P.dims.K + 1;
+      for (int i = 0; i < rows; ++i) P.out_tokens[static_cast<int64_t>(b) * rows + i] = -1;
+      P.out_n[b] = -1;
+    }
+  } else if (fin == kFinSelect) {
+    SeqState st;
+    const int *src = reinterpret_cast<const int *>(&P.w.seq[b]);
+    int *dst = reinterpret_cast<int *>(&st);
+#pragma unroll
+    for (int i = 0; i < static_cast<int>(sizeof(SeqState) / 4); ++i) dst[i] = __ldcg(&src[i]);
+    if (st.mode != kModeSkip) select_token(P, b, st);
+  }
+}
+
 __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailParams P) {
   pdl_wait();
   pdl_launch_dependents();
@@ -645,14 +688,17 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailParams P) 
       }
     }
     __syncthreads();
-    if (s_last) decide(P, b);
+    if (s_last) finalize_sequence(P, b, decide(P, b));
   } else {
     // ---- residual chunk ----
     const int idx = t - nrow;
     const int b = idx / P.dims.nchunk, c = idx % P.dims.nchunk;
+    __shared__ int s_seen, s_fin;
     if (threadIdx.x == 0) {
       if (!wait_flag(&P.w.seq_flag[b], P.epoch, P.wait_limit_ns))
         set_status(P.w.status, SV_ERR_TIMEOUT);
+      // one read of the flag decides for the whole CTA
+      s_seen = *reinterpret_cast<const volatile unsigned *>(&P.w.seq_flag[b]) == P.epoch;
       __threadfence();
     }
     __syncthreads();
@@ -663,8 +709,7 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailParams P) 
 #pragma unroll
       for (int i = 0; i < static_cast<int>(sizeof(SeqState) / 4); ++i) dst[i] = __ldcg(&src[i]);
     }
-    if (*reinterpret_cast<const volatile unsigned *>(&P.w.seq_flag[b]) != P.epoch)
-      st.mode = kModeSkip;
+    if (!s_seen) st.mode = kModeSkip;
     float m = 0.0f;
     if (st.mode != kModeSkip) {
       float r[kChunkPerThread];
@@ -673,15 +718,17 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailParams P) 
     const ff mass = block_sum_ff(ff_make(m), s_wff);
     if (threadIdx.x == 0) {
       st_ff(&P.w.chunk_mass[static_cast<int64_t>(b) * P.dims.nchunk + c], mass);
+      if (!s_seen) atomicOr(&P.w.seq_final[b], kPoisoned);
       __threadfence();
-      s_last = atomicAdd(&P.w.chunk_count[b], 1) == P.dims.nchunk - 1;
-      if (s_last) {
+      s_fin = kFinNone;
+      if (atomicAdd(&P.w.chunk_count[b], 1) == P.dims.nchunk - 1) {
         P.w.chunk_count[b] = 0;
         __threadfence();
+        s_fin = arrive_final(P, b);
       }
     }
     __syncthreads();
-    if (s_last && st.mode != kModeSkip) select_token(P, b, st);
+    finalize_sequence(P, b, s_fin);
   }
 
   // the last CTA to finish rewinds the ticket counter for the next launch
