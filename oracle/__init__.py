@@ -74,6 +74,9 @@ def _load():
             lib.sv_oracle_rule_batch.restype = ctypes.c_int
             lib.sv_oracle_emitted_law.argtypes = [i64, vp, vp, vp]
             lib.sv_oracle_emitted_law.restype = dbl
+            lib.sv_oracle_ngram_draft.argtypes = [vp, i64, vp, i32, i32, i32,
+                                                  i32, vp, vp]
+            lib.sv_oracle_ngram_draft.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -135,7 +138,9 @@ def verify(hidden, W, draft, q_logits, uniforms, temperature: float,
     """The whole verify-and-sample step for B sequences.
 
     hidden [B, K+1, d] and W [V, d] as uint16 (bf16 bits) or float32;
-    draft [B, K] int32; q_logits [B, K, V] float32; uniforms [B, K+1] float32.
+    draft [B, K] int32; q_logits [B, K, V] float32, or None for drafts
+    proposed with certainty (point-mass q; a -1 then ends a draft early);
+    uniforms [B, K+1] float32.
     Returns tokens [B, K+1], n_accepted [B], dist [B], lse_p, lse_q, status
     and (optionally) fp64 logits [B*(K+1), V].
     """
@@ -148,7 +153,7 @@ def verify(hidden, W, draft, q_logits, uniforms, temperature: float,
     V = W.shape[0]
     draft = _c(draft, np.int32).reshape(B, K)
     T = float(temperature)
-    q = None if (T == 0.0 or K == 0) else _c(q_logits, np.float32).reshape(B, K, V)
+    q = None if (K == 0 or q_logits is None) else _c(q_logits, np.float32).reshape(B, K, V)
     u = None if T == 0.0 else _c(uniforms, np.float32).reshape(B, rows)
     tokens = np.empty((B, rows), dtype=np.int32)
     n_acc = np.empty((B,), dtype=np.int32)
@@ -168,11 +173,13 @@ def verify(hidden, W, draft, q_logits, uniforms, temperature: float,
 
 def rule_batch(p, q, x, u):
     """The accept / residual / bonus rule for n independent rounds that
-    share p [K+1, V] and q [K, V] (probabilities); x [n, K], u [n, K+1]."""
+    share p [K+1, V] and q [K, V] (probabilities; None for point-mass
+    drafts, where a -1 ends a draft early); x [n, K], u [n, K+1]."""
     p = _c(p, np.float64)
     K1, V = p.shape
     K = K1 - 1
-    q = _c(q, np.float64).reshape(K, V) if K > 0 else np.zeros((1, V))
+    if q is not None:
+        q = _c(q, np.float64).reshape(K, V) if K > 0 else np.zeros((1, V))
     x = _c(x, np.int32).reshape(-1, K) if K > 0 else np.zeros((len(u), 1), np.int32)
     u = _c(u, np.float64).reshape(-1, K1)
     n = u.shape[0]
@@ -211,3 +218,21 @@ def expected_tokens_positions(alphas) -> float:
         prod *= float(a)
         total += prod
     return total
+
+
+def ngram_draft(tokens, lengths, K: int, n_min: int = 2, n_max: int = 5):
+    """Prompt-lookup drafts (reading R10 in sv_oracle.c): tokens [B, L]
+    int32 contexts (row b holds lengths[b] tokens), K draft slots.
+    Returns draft [B, K] (-1 after the proposal) and its length [B]."""
+    tokens = _c(tokens, np.int32)
+    if tokens.ndim == 1:
+        tokens = tokens.reshape(1, -1)
+    B, L = tokens.shape
+    lengths = _c(lengths, np.int32).reshape(B)
+    draft = np.empty((B, K), dtype=np.int32)
+    n = np.empty((B,), dtype=np.int32)
+    rc = _load().sv_oracle_ngram_draft(_ptr(tokens), L, _ptr(lengths), B, K,
+                                       n_min, n_max, _ptr(draft), _ptr(n))
+    if rc != OK:
+        raise ValueError(f"sv_oracle_ngram_draft failed ({rc})")
+    return draft, n

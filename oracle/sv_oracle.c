@@ -45,6 +45,22 @@
  *       the bonus a_{K+1} ([P1] first remark, [P3] Step 2).
  *   R7  Token ids outside [0, V) make that sequence's result invalid: its
  *       outputs are -1 and the function reports it.
+ *   R8  A draft that comes without a distribution (no q_logits: a prompt
+ *       lookup match, a user-supplied prediction) was proposed with
+ *       certainty, so q_i is the point mass at x_i ([P3] "Drafts without a
+ *       model"; [P4] "Where it breaks": q is the distribution that actually
+ *       generated the proposal).  Then t_i = p_i(x_i), and the residual
+ *       max(0, p_j - q_j) is p_j with the entry at x_j removed.
+ *   R9  Such a draft may be shorter than K: the first -1 ends it (every
+ *       later entry must be -1 too).  With K_b proposed tokens the round
+ *       walks positions 1..K_b and, if all survive, draws the bonus from
+ *       target row K_b (greedy: emits its argmax).
+ *   R10 Prompt lookup ([P3] "Drafts without a model"; [P1] "No model at
+ *       all"): for n from n_max down to n_min, take the last n context
+ *       tokens and look for an earlier occurrence followed by at least one
+ *       token; the first n that has one wins, and of its occurrences the
+ *       latest (the one starting closest to the end).  The draft is the up
+ *       to K tokens that follow it in the context.
  */
 #include <math.h>
 #include <stdint.h>
@@ -180,22 +196,39 @@ static int32_t inverse_cdf(int64_t V, const double *w, double S, double u,
  * draw its inverse-CDF interval edges).
  * `scratch` must hold V doubles.
  * ---------------------------------------------------------------------- */
+/* Number of proposed tokens of a draft x[0..K-1] (R7, R9): K if every id
+ * is in [0, V); with point_mass, the position of the first -1 if every
+ * later entry is -1 too.  Returns -1 for an invalid draft. */
+static int32_t draft_length(int64_t V, int32_t K, const int32_t *x, int point_mass) {
+  int32_t kb = K;
+  for (int32_t i = 0; i < K; ++i) {
+    if (point_mass && x[i] == -1 && kb == K) kb = i;
+    if (i >= kb) {
+      if (x[i] != -1) return -1;
+    } else if (x[i] < 0 || (int64_t)x[i] >= V) {
+      return -1;
+    }
+  }
+  return kb;
+}
+
 static int32_t rule_one_sequence(int64_t V, int32_t K, const double *p,
                                  const double *q, const int32_t *x,
                                  const double *u, int32_t *tokens,
                                  double *dist, double *scratch) {
   double best = INFINITY;
   for (int32_t i = 0; i <= K; ++i) tokens[i] = -1;
-  for (int32_t i = 0; i < K; ++i)
-    if (x[i] < 0 || (int64_t)x[i] >= V) {
-      *dist = INFINITY;
-      return SV_ORACLE_ETOKEN;
-    }
-  int32_t j = K; /* row of the final draw */
+  /* q == NULL: the draft was proposed with certainty (R8, R9) */
+  const int32_t kb = draft_length(V, K, x, q == NULL);
+  if (kb < 0) {
+    *dist = INFINITY;
+    return SV_ORACLE_ETOKEN;
+  }
+  int32_t j = kb; /* row of the final draw */
   int residual = 0;
-  for (int32_t i = 0; i < K; ++i) {
+  for (int32_t i = 0; i < kb; ++i) {
     const double px = p[(int64_t)i * V + x[i]];
-    const double qx = q[(int64_t)i * V + x[i]];
+    const double qx = q ? q[(int64_t)i * V + x[i]] : 1.0;
     int accept;
     double t;
     if (qx > 0.0) {
@@ -221,9 +254,10 @@ static int32_t rule_one_sequence(int64_t V, int32_t K, const double *p,
   int32_t tok;
   double dfinal;
   if (residual) {
-    const double *qj = q + (int64_t)j * V;
+    const double *qj = q ? q + (int64_t)j * V : NULL;
     for (int64_t v = 0; v < V; ++v) {
-      const double r = pj[v] - qj[v];
+      const double qv = qj ? qj[v] : (v == (int64_t)x[j] ? 1.0 : 0.0);
+      const double r = pj[v] - qv;
       scratch[v] = r > 0.0 ? r : 0.0;
       S += scratch[v];
     }
@@ -249,15 +283,16 @@ static int32_t rule_one_sequence(int64_t V, int32_t K, const double *p,
  * decided something this round.
  * ---------------------------------------------------------------------- */
 static int32_t greedy_one_sequence(int64_t V, int32_t K, const double *L,
-                                   const int32_t *x, int32_t *tokens,
-                                   double *gap) {
+                                   const int32_t *x, int point_mass,
+                                   int32_t *tokens, double *gap) {
   double best = INFINITY;
   for (int32_t i = 0; i <= K; ++i) tokens[i] = -1;
-  for (int32_t i = 0; i < K; ++i)
-    if (x[i] < 0 || (int64_t)x[i] >= V) {
-      *gap = INFINITY;
-      return SV_ORACLE_ETOKEN;
-    }
+  const int32_t kb = draft_length(V, K, x, point_mass);
+  if (kb < 0) {
+    *gap = INFINITY;
+    return SV_ORACLE_ETOKEN;
+  }
+  K = kb; /* R9: a shorter draft ends the walk earlier */
   for (int32_t i = 0; i <= K; ++i) {
     const double *row = L + (int64_t)i * V;
     int64_t a = 0;
@@ -308,7 +343,8 @@ int sv_oracle_verify(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
       !hidden || !W || !out_tokens || !out_n || !(T >= 0.0) || T == INFINITY)
     return SV_ORACLE_EARG;
   if (K > 0 && !draft) return SV_ORACLE_EARG;
-  if (T > 0.0 && (!u || (K > 0 && !q_logits))) return SV_ORACLE_EARG;
+  if (T > 0.0 && !u) return SV_ORACLE_EARG;
+  const int point_mass = q_logits == NULL; /* R8, R9 */
   const int64_t rows = (int64_t)K + 1;
   const size_t esz = dtype == 0 ? 2 : 4;
   double *L = (double *)malloc(sizeof(double) * (size_t)(rows * V));
@@ -334,14 +370,14 @@ int sv_oracle_verify(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
     double dd;
     int32_t n;
     if (T == 0.0) {
-      n = greedy_one_sequence(V, K, L, xb, tb, &dd);
+      n = greedy_one_sequence(V, K, L, xb, point_mass, tb, &dd);
     } else {
       for (int64_t i = 0; i < rows; ++i) {
         const double lse = sv_oracle_lse(V, L + i * V, T);
         if (lse_p) lse_p[(int64_t)b * rows + i] = lse;
         for (int64_t v = 0; v < V; ++v) p[i * V + v] = exp(L[i * V + v] / T - lse);
       }
-      for (int64_t i = 0; i < K; ++i) {
+      for (int64_t i = 0; i < K && !point_mass; ++i) {
         const float *ql = q_logits + ((int64_t)b * K + i) * V;
         for (int64_t v = 0; v < V; ++v) qrow[v] = (double)ql[v];
         const double lse = sv_oracle_lse(V, qrow, T);
@@ -349,7 +385,7 @@ int sv_oracle_verify(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
         for (int64_t v = 0; v < V; ++v) q[i * V + v] = exp(qrow[v] / T - lse);
       }
       for (int64_t i = 0; i < rows; ++i) ud[i] = (double)u[(int64_t)b * rows + i];
-      n = rule_one_sequence(V, K, p, q, xb, ud, tb, &dd, scratch);
+      n = rule_one_sequence(V, K, p, point_mass ? NULL : q, xb, ud, tb, &dd, scratch);
     }
     if (n == SV_ORACLE_ETOKEN) {
       status = SV_ORACLE_ETOKEN;
@@ -368,13 +404,14 @@ int sv_oracle_verify(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
  * The rule alone, for many independent rounds that share the same p and q
  * (the i.i.d.-position setting of the pages' simulations, [P1] "Checking
  * the math honestly", [P3] three-token example):
- *   p [K+1, V], q [K, V] probabilities; x [n, K]; u [n, K+1]
+ *   p [K+1, V], q [K, V] probabilities (q == NULL: point-mass drafts, R8,
+ *   R9); x [n, K]; u [n, K+1]
  * Outputs tokens [n, K+1], n_accepted [n], dist [n] (may be NULL).
  * ---------------------------------------------------------------------- */
 int sv_oracle_rule_batch(int64_t V, int32_t K, const double *p, const double *q,
                          int64_t n, const int32_t *x, const double *u,
                          int32_t *out_tokens, int32_t *out_n, double *dist) {
-  if (V < 1 || K < 0 || n < 0 || !p || (K > 0 && (!q || !x)) || !u ||
+  if (V < 1 || K < 0 || n < 0 || !p || (K > 0 && !x) || !u ||
       !out_tokens || !out_n)
     return SV_ORACLE_EARG;
   double *scratch = (double *)malloc(sizeof(double) * (size_t)V);
@@ -421,4 +458,46 @@ double sv_oracle_emitted_law(int64_t V, const double *p, const double *q,
     }
   }
   return alpha;
+}
+
+/* ------------------------------------------------------------------------
+ * Prompt-lookup drafting (reading R10), B contexts of lengths[b] tokens,
+ * row b starting at tokens + b * ld.  For n = n_max down to n_min: the
+ * pattern is the last n tokens; an occurrence starts at j with
+ * j + n <= len - 1 (at least one token follows it) and matches the pattern
+ * token for token; the first n with an occurrence wins, with its largest j.
+ * out_draft [B, K]: the up to K tokens following that occurrence, then -1;
+ * out_len [B]: their number (0 when no n matched).
+ * ---------------------------------------------------------------------- */
+int sv_oracle_ngram_draft(const int32_t *tokens, int64_t ld, const int32_t *lengths,
+                          int32_t B, int32_t K, int32_t n_min, int32_t n_max,
+                          int32_t *out_draft, int32_t *out_len) {
+  if (!tokens || !lengths || !out_draft || !out_len || B < 0 || K < 0 || n_min < 1 ||
+      n_max < n_min)
+    return SV_ORACLE_EARG;
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t *t = tokens + (int64_t)b * ld;
+    const int64_t len = lengths[b];
+    int32_t *out = out_draft + (int64_t)b * K;
+    for (int32_t i = 0; i < K; ++i) out[i] = -1;
+    out_len[b] = 0;
+    if (len < 0 || len > ld) return SV_ORACLE_EARG;
+    for (int32_t n = n_max; n >= n_min; --n) {
+      if ((int64_t)n >= len) continue; /* needs n + 1 tokens at least */
+      const int32_t *pat = t + (len - n);
+      int64_t found = -1;
+      for (int64_t j = 0; j + n <= len - 1; ++j) {
+        int match = 1;
+        for (int32_t k = 0; k < n && match; ++k) match = t[j + k] == pat[k];
+        if (match) found = j; /* keep the latest */
+      }
+      if (found >= 0) {
+        int32_t m = 0;
+        for (int64_t v = found + n; v < len && m < K; ++v) out[m++] = t[v];
+        out_len[b] = m;
+        break;
+      }
+    }
+  }
+  return SV_ORACLE_OK;
 }
