@@ -102,7 +102,17 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out);
  *                  scores the bonus position K+1)
  *   W_lm           device, [V, d] of dtype (the LM-head matrix, read once)
  *   draft_tokens   device, int32 [B, K], each in [0, V); may be NULL if K == 0
- *   q_logits       device, fp32 [B, K, V] draft logits; unused if T == 0
+ *   q_logits       device, fp32 [B, K, V] draft logits; not read if T == 0.
+ *                  NULL: the drafts came without a distribution (prompt
+ *                  lookup, a supplied prediction), so q is the point mass at
+ *                  each proposed token ("Speculative Decoding: The Algebra
+ *                  and the Proof", "Where it breaks": q is the distribution
+ *                  that actually generated the proposal).  The accept test
+ *                  becomes u < p(x), the residual is p without x, and a draft
+ *                  may end early: the first -1 in draft_tokens[b] ends it
+ *                  (later entries must be -1 too) and, if every proposed
+ *                  token survives, the bonus comes from target row K_b, the
+ *                  draft's length.  Applies at T == 0 as well (greedy).
  *   uniforms       device, fp32 [B, K+1] in [0, 1): u[b, i] for the accept
  *                  test of position i+1, u[b, K] for the final draw;
  *                  unused if T == 0
@@ -201,6 +211,36 @@ int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidden, const vo
                             const int32_t *draft_tokens, const float *q_logits,
                             const float *uniforms, float temperature, int32_t *out_tokens,
                             int32_t *out_n_accepted);
+
+/* ---------------------------------------------------------------------------
+ * Prompt-lookup drafting ("Speculative Decoding: Guess Several Tokens, Check
+ * Them in One Pass", "Drafts without a model"; "Speculative Decoding: Two
+ * Models, One Voice", "No model at all"): propose the tokens that followed
+ * an earlier occurrence of the last few context tokens.  For each sequence
+ * b with context tokens[b * ld .. b * ld + lengths[b] - 1]:
+ *   for n = n_max down to n_min, the pattern is the last n tokens; an
+ *   occurrence starts at j with j + n <= lengths[b] - 1 (at least one token
+ *   follows it) and equals the pattern token for token.  The first n with
+ *   an occurrence wins, and of its occurrences the latest (largest j).
+ * (Longest n first and the latest occurrence are this library's reading;
+ * the pages leave both open.)
+ *   tokens         device, int32 [B, ld] row-major contexts
+ *   lengths        device, int32 [B]; a length outside [0, ld] counts as 0
+ *   K              draft slots, 1..SV_MAX_K
+ *   n_min, n_max   1 <= n_min <= n_max <= SV_NGRAM_MAX
+ *   out_draft      device, int32 [B, K]: the up to K tokens following the
+ *                  chosen occurrence, then -1 (ready for spec_verify_run
+ *                  with q_logits == NULL)
+ *   out_len        device, int32 [B]: the draft's length, 0 if no n matched
+ *   stream         cudaStream_t (NULL: the default stream)
+ * Asynchronous; allocates nothing; graph-capturable.  All pointers 4-byte
+ * aligned.  Errors (returned): SV_ERR_ARG (null pointer, B < 1, ld < 1, K or
+ * the n bounds out of range), SV_ERR_ALIGN, SV_ERR_ARCH (not compute
+ * capability 10.3), SV_ERR_CUDA (launch failed). */
+#define SV_NGRAM_MAX 16
+int spec_ngram_draft(const int32_t *tokens, int64_t ld, const int32_t *lengths, int32_t B,
+                     int32_t K, int32_t n_min, int32_t n_max, int32_t *out_draft,
+                     int32_t *out_len, void *stream);
 
 #ifdef __cplusplus
 }

@@ -31,6 +31,7 @@ SV_FP32 = 1
 SV_MAX_K = 16
 SV_MAX_B = 4096
 SV_MAX_ROWS_BF16 = 384
+SV_NGRAM_MAX = 16
 
 # every symbol of include/spec_verify.h
 EXPORTS = ("spec_verify_create", "spec_verify_run", "spec_verify_run_host",
@@ -39,7 +40,7 @@ EXPORTS = ("spec_verify_create", "spec_verify_run", "spec_verify_run_host",
            "spec_verify_set_wait_limit", "spec_verify_timing",
            "spec_verify_timing_read", "spec_verify_launches_per_run",
            "spec_verify_strerror", "spec_verify_destroy",
-           "spec_verify_run_noalloc")
+           "spec_verify_run_noalloc", "spec_ngram_draft")
 
 
 class SpecVerifyError(RuntimeError):
@@ -87,6 +88,9 @@ def load_library():
         lib.spec_verify_destroy.restype = None
         lib.spec_verify_run_noalloc.argtypes = [ctypes.POINTER(sv_config_t), vp, vp, vp, vp,
                                                 vp, f32, vp, vp]
+        i32 = ctypes.c_int32
+        lib.spec_ngram_draft.argtypes = [vp, ctypes.c_int64, vp, i32, i32, i32, i32, vp, vp,
+                                         vp]
         for name in EXPORTS:
             if name not in ("spec_verify_strerror", "spec_verify_destroy"):
                 getattr(lib, name).restype = ctypes.c_int
@@ -205,6 +209,24 @@ def spec_verify_run_noalloc(V, d, B, K, dtype, hidden, W_lm, draft_tokens, q_log
         ctypes.byref(cfg), _ptr(hidden), _ptr(W_lm), _ptr(draft_tokens), _ptr(q_logits),
         _ptr(uniforms), float(temperature), _ptr(out_tokens), _ptr(out_n_accepted)),
         "spec_verify_run_noalloc")
+
+
+def spec_ngram_draft(tokens, lengths, K: int, n_min: int = 2, n_max: int = 5,
+                     out_draft=None, out_len=None, stream=None):
+    """Prompt-lookup drafts for B contexts (tokens [B, L] int32 on the GPU,
+    lengths [B] int32): the up to K tokens that followed the latest earlier
+    occurrence of the longest recurring suffix of n_max..n_min tokens.
+    Returns (draft [B, K] with -1 after the proposal, length [B]); the
+    draft feeds spec_verify_run with q_logits=None."""
+    B, L = tokens.shape
+    if out_draft is None:
+        out_draft = torch.empty((B, K), dtype=torch.int32, device=tokens.device)
+    if out_len is None:
+        out_len = torch.empty((B,), dtype=torch.int32, device=tokens.device)
+    _check(load_library().spec_ngram_draft(
+        _ptr(tokens), int(L), _ptr(lengths), int(B), int(K), int(n_min), int(n_max),
+        _ptr(out_draft), _ptr(out_len), _stream_handle(stream)), "spec_ngram_draft")
+    return out_draft, out_len
 
 
 def spec_verify_destroy(h) -> None:

@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspec_verify.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["sv_api.cu", "sv_lmhead_tc.cu", "sv_lmhead_simt.cu", "sv_tail.cu", "sv_noalloc.cu"]
+SOURCES = ["sv_api.cu", "sv_lmhead_tc.cu", "sv_lmhead_simt.cu", "sv_tail.cu", "sv_noalloc.cu",
+           "sv_ngram.cu"]
 HEADERS = ["sv_internal.cuh", "sv_kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

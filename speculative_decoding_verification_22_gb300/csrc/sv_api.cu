@@ -266,7 +266,9 @@ int spec_verify_run(spec_verify_t *h, const void *hidden, const void *W_lm,
   const sv::Dims &D = h->dims;
   const bool greedy = temperature == 0.0f;
   if (D.K > 0 && !draft_tokens) return SV_ERR_ARG;
-  if (!greedy && ((D.K > 0 && !q_logits) || !uniforms)) return SV_ERR_ARG;
+  // q_logits == NULL: point-mass drafts (q = the proposed token with
+  // certainty); a -1 draft token then ends that sequence's draft
+  if (!greedy && !uniforms) return SV_ERR_ARG;
   const void *ptrs[] = {hidden, W_lm, draft_tokens, q_logits, uniforms, out_tokens,
                         out_n_accepted};
   for (const void *p : ptrs)
@@ -381,7 +383,7 @@ int spec_verify_run_host(spec_verify_t *h, const void *hidden_host, const void *
   const sv::Dims &D = h->dims;
   const bool greedy = temperature == 0.0f;
   if (D.K > 0 && !draft_tokens_host) return SV_ERR_ARG;
-  if (!greedy && ((D.K > 0 && !q_logits_host) || !uniforms_host)) return SV_ERR_ARG;
+  if (!greedy && !uniforms_host) return SV_ERR_ARG;
   cudaStream_t st = h->stream;
   const size_t es = esize(h->cfg.dtype);
   if (cudaMemcpyAsync(h->st_hidden, hidden_host, static_cast<size_t>(D.R) * D.d * es,
@@ -391,7 +393,7 @@ int spec_verify_run_host(spec_verify_t *h, const void *hidden_host, const void *
                                  cudaMemcpyHostToDevice, st) != cudaSuccess)
     return SV_ERR_CUDA;
   if (!greedy) {
-    if (D.K > 0 &&
+    if (D.K > 0 && q_logits_host &&
         cudaMemcpyAsync(h->st_q, q_logits_host, sizeof(float) * static_cast<size_t>(D.RQ) * D.V,
                         cudaMemcpyHostToDevice, st) != cudaSuccess)
       return SV_ERR_CUDA;
@@ -399,9 +401,11 @@ int spec_verify_run_host(spec_verify_t *h, const void *hidden_host, const void *
                         st) != cudaSuccess)
       return SV_ERR_CUDA;
   }
+  // the staging q buffer stands in for the caller's only if one was given
+  // (no q_logits: point-mass drafts; at T == 0 q is not read)
   int rc = spec_verify_run(h, h->st_hidden, W_lm, D.K > 0 ? h->st_draft : nullptr,
-                           greedy ? nullptr : h->st_q, greedy ? nullptr : h->st_u, temperature,
-                           h->st_tokens, h->st_n);
+                           q_logits_host ? h->st_q : nullptr, greedy ? nullptr : h->st_u,
+                           temperature, h->st_tokens, h->st_n);
   if (rc != SV_OK) return rc;
   if (cudaMemcpyAsync(out_tokens_host, h->st_tokens, sizeof(int32_t) * D.R,
                       cudaMemcpyDeviceToHost, st) != cudaSuccess ||

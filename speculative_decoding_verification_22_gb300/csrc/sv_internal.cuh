@@ -24,7 +24,10 @@ constexpr int kMaxCand = 64;    // greedy: near-maximal subtiles listed per row
 
 // Per-sequence state handed from the decision pass to the residual and
 // selection passes.
-enum : int { kModeSkip = 0, kModeResidual = 1, kModeP = 2 };
+// kModeResidualPoint: the residual of a draft proposed with certainty (q =
+// the point mass at the proposed token): p without that token, whose id
+// is held in q_row.
+enum : int { kModeSkip = 0, kModeResidual = 1, kModeP = 2, kModeResidualPoint = 3 };
 
 struct SeqState {
   int mode;      // kModeSkip: nothing to draw (greedy, invalid, error)

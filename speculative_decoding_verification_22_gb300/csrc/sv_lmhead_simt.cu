@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) lmhead_simt_kernel(const Simt
     if (valid) P.w.logits[static_cast<int64_t>(row) * V + v] = l;
     const float2 pm = subtile_partial(l, valid, P.inv_t, P.greedy != 0);
     if (lane == 0) P.w.part_p[static_cast<int64_t>(row) * P.dims.nsub + sub] = pm;
-  } else if (!P.greedy && row - P.dims.R < P.dims.RQ) {
+  } else if (!P.greedy && P.q_logits != nullptr && row - P.dims.R < P.dims.RQ) {
     const int rq = row - P.dims.R;
     const float x = valid ? P.q_logits[static_cast<int64_t>(rq) * V + v] : 0.0f;
     const float2 pm = subtile_partial(x, valid, P.inv_t, false);
@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) lmhead_simt_kernel(const Simt
 }
 
 cudaError_t launch_simt(const SimtParams &P, cudaStream_t stream) {
-  const int rows = P.dims.R + (P.greedy ? 0 : P.dims.RQ);
+  const int rows = P.dims.R + ((P.greedy || P.q_logits == nullptr) ? 0 : P.dims.RQ);
   dim3 grid(P.dims.nsub, (rows + kSimtWarps - 1) / kSimtWarps);
   void *args[] = {const_cast<SimtParams *>(&P)};
   return launch_pdl(reinterpret_cast<const void *>(&lmhead_simt_kernel), grid,

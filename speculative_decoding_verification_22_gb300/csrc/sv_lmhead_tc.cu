@@ -365,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- draft-logit partials (independent of the GEMM) -------
     if (!P.greedy && P.dims.RQ > 0) {
       const int quad = (warp - 2 - kNumEpiWarps) & 3;
-      for (int t = t_first; t <= t_last; ++t) {
+      // no draft distribution (point-mass drafts): nothing to normalise
+      for (int t = t_first; t <= t_last && P.q_logits != nullptr; ++t) {
         int kb0, kb1;
         tile_range(t, u0, u1, ngr, C, kb0, kb1);
         if (kb0 != 0) continue;  // the CTA holding a tile's first k block does it

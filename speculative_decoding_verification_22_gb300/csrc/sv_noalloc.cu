@@ -113,7 +113,7 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
   if (cfg->dtype == SV_BF16 && R > SV_MAX_ROWS_BF16) return SV_ERR_SHAPE;
   const bool greedy = temperature == 0.0f;
   if (cfg->K > 0 && !draft_tokens) return SV_ERR_ARG;
-  if (!greedy && ((cfg->K > 0 && !q_logits) || !uniforms)) return SV_ERR_ARG;
+  if (!greedy && !uniforms) return SV_ERR_ARG;  // q_logits == NULL: point-mass drafts
   const void *ptrs[] = {hidden, W_lm, draft_tokens, q_logits, uniforms, out_tokens,
                         out_n_accepted};
   for (const void *p : ptrs)

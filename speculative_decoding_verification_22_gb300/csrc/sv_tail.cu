@@ -218,16 +218,21 @@ __device__ int exact_argmax(const TailParams &P, int64_t r, float M, int lane) {
 // ---------------------------------------------------------------------------
 
 // Weight of vocabulary entry v in the final draw: max(0, p - q) for a
-// residual, p for a bonus.  p(v) = exp(l / T - LSE) is evaluated as
-// exp(l * inv_t - M) * (1 / S) with M the row maximum, so the fp32 argument
-// stays small near the mass; the explicit _rn operations keep the value
-// bit-identical wherever it is recomputed.
-__device__ __forceinline__ float draw_weight(const SeqState &st, float l, float ql,
+// residual, p for a bonus; for a point-mass draft's residual, p with the
+// proposed token's entry removed (max(0, p - 1) = 0 there).
+// p(v) = exp(l / T - LSE) is evaluated as exp(l * inv_t - M) * (1 / S) with M
+// the row maximum, so the fp32 argument stays small near the mass; the
+// explicit _rn operations keep the value bit-identical wherever it is
+// recomputed.
+__device__ __forceinline__ float draw_weight(const SeqState &st, int64_t v, float l, float ql,
                                              float inv_t) {
   const float p = __fmul_rn(expf(fmaf(l, inv_t, -st.p_max)), st.p_corr);
-  if (st.mode != kModeResidual) return p;
-  const float q = __fmul_rn(expf(fmaf(ql, inv_t, -st.q_max)), st.q_corr);
-  return fmaxf(__fsub_rn(p, q), 0.0f);
+  if (st.mode == kModeResidual) {
+    const float q = __fmul_rn(expf(fmaf(ql, inv_t, -st.q_max)), st.q_corr);
+    return fmaxf(__fsub_rn(p, q), 0.0f);
+  }
+  if (st.mode == kModeResidualPoint && v == st.q_row) return 0.0f;
+  return p;
 }
 
 // The kChunkPerThread consecutive weights of this thread in chunk `chunk`,
@@ -269,7 +274,7 @@ __device__ __forceinline__ float chunk_weights(const TailParams &P, const SeqSta
   float sum = 0.0f;
 #pragma unroll
   for (int j = 0; j < kChunkPerThread; ++j) {
-    r[j] = v0 + j < V ? draw_weight(st, l[j], q[j], P.inv_t) : 0.0f;
+    r[j] = v0 + j < V ? draw_weight(st, v0 + j, l[j], q[j], P.inv_t) : 0.0f;
     sum = __fadd_rn(sum, r[j]);
   }
   return sum;
@@ -321,7 +326,10 @@ __device__ int decide(const TailParams &P, int b) {
   __shared__ ff s_lp_s[SV_MAX_K + 1], s_lq_s[SV_MAX_K];       // row sums
   __shared__ float s_ql[SV_MAX_K], s_u[SV_MAX_K + 1];
   __shared__ int s_x[SV_MAX_K], s_arg[SV_MAX_K + 1];
-  __shared__ int s_err, s_fin;
+  __shared__ int s_err, s_fin, s_kb;
+  // no draft distribution: the draft was proposed with certainty (q is a
+  // point mass at each proposed token) and a -1 ends it early
+  const bool point = P.q_logits == nullptr;
 
   if (threadIdx.x == 0) s_err = 0;
   __syncthreads();
@@ -339,13 +347,17 @@ __device__ int decide(const TailParams &P, int b) {
     const int i = threadIdx.x - 32;
     const int x = P.draft[static_cast<int64_t>(b) * K + i];
     s_x[i] = x;
-    if (x < 0 || static_cast<int64_t>(x) >= V) {
+    if (point && x == -1) {
+      // end of a short draft (checked below)
+    } else if (x < 0 || static_cast<int64_t>(x) >= V) {
       atomicExch(&s_err, SV_ERR_TOKEN);
     } else if (!P.greedy) {
+      // a point-mass draft row holds M = 0, S = 1 and q_logits(x) counts
+      // as 0, so the threshold below is p(x) / 1
       const int64_t rq = static_cast<int64_t>(R) + static_cast<int64_t>(b) * K + i;
       s_lq_m[i] = __ldcg(&P.w.row_m[rq]);
       s_lq_s[i] = ld_ff(&P.w.row_s[rq]);
-      s_ql[i] = P.q_logits[(static_cast<int64_t>(b) * K + i) * V + x];
+      s_ql[i] = point ? 0.0f : P.q_logits[(static_cast<int64_t>(b) * K + i) * V + x];
       s_l[i] = ld_ff(&P.w.draft_logit[static_cast<int64_t>(b) * K + i]);
       const bool fin = isfinite(s_lq_m[i]) && s_lq_s[i].hi > 0.0f && s_lq_s[i].hi < INFINITY;
       if (!fin) atomicCAS(&s_err, 0, SV_ERR_NONFINITE);
@@ -357,14 +369,27 @@ __device__ int decide(const TailParams &P, int b) {
     atomicExch(&s_err, SV_ERR_TIMEOUT);
   }
   __syncthreads();
+  if (threadIdx.x == 0) {
+    // proposed tokens of this sequence: K, or the position of the first -1
+    // of a point-mass draft, after which every entry must be -1 too
+    int kb = K;
+    if (point)
+      for (int i = 0; i < K && kb == K; ++i)
+        if (s_x[i] == -1) kb = i;
+    for (int i = kb; i < K; ++i)
+      if (s_x[i] != -1) atomicExch(&s_err, SV_ERR_TOKEN);
+    s_kb = kb;
+  }
+  __syncthreads();
+  const int kb = s_kb;
   if (s_err == SV_ERR_TIMEOUT && b == 0) {
     // the aborted contraction may have left split-tile counters half-used
     for (int i = threadIdx.x; i < P.split_cnt_n; i += kTailThreads) P.w.split_cnt[i] = 0;
   }
   if (s_err == 0) {
     if (!P.greedy) {
-      // accept thresholds of the K positions, one thread each
-      if (threadIdx.x < K) {
+      // accept thresholds of the proposed positions, one thread each
+      if (threadIdx.x < kb) {
         const int i = threadIdx.x;
         const float T = static_cast<float>(P.T);
         const ff l = s_l[i];
@@ -374,7 +399,7 @@ __device__ int decide(const TailParams &P, int b) {
         s_acc[i] = isfinite(l.hi) ? (s_u[i] < accept_threshold(lp, lq, ratio) ? 1 : 0) : -1;
       }
     } else {
-      for (int i = warp; i < rows; i += kTailWarps) {
+      for (int i = warp; i <= kb; i += kTailWarps) {
         const int a = exact_argmax(P, out0 + i, s_lp_m[i], lane);
         if (lane == 0) s_arg[i] = a;
       }
@@ -386,8 +411,8 @@ __device__ int decide(const TailParams &P, int b) {
     SeqState st = {};
     st.mode = kModeSkip;
     if (err == 0 && !P.greedy) {
-      int n = K, mode = kModeP;
-      for (int i = 0; i < K; ++i) {
+      int n = kb, mode = kModeP;
+      for (int i = 0; i < kb; ++i) {
         if (s_acc[i] < 0) {
           err = SV_ERR_NONFINITE;
           break;
@@ -396,7 +421,7 @@ __device__ int decide(const TailParams &P, int b) {
           P.out_tokens[out0 + i] = s_x[i];
         } else {
           n = i;
-          mode = kModeResidual;
+          mode = point ? kModeResidualPoint : kModeResidual;
           break;
         }
       }
@@ -412,17 +437,19 @@ __device__ int decide(const TailParams &P, int b) {
           st.q_row = b * K + n;
           st.q_max = s_lq_m[n];
           st.q_corr = __fdiv_rn(1.0f, ff_to_f(s_lq_s[n]));
+        } else if (mode == kModeResidualPoint) {
+          st.q_row = s_x[n];  // the token whose entry the residual drops
         }
         st.u_final = s_u[K];
       }
     } else if (err == 0) {
       bool ok = true;
-      for (int i = 0; i < rows; ++i) ok = ok && s_arg[i] >= 0;
+      for (int i = 0; i <= kb; ++i) ok = ok && s_arg[i] >= 0;
       if (!ok) {
         err = SV_ERR_NONFINITE;
       } else {
-        int n = K;
-        for (int i = 0; i < K; ++i) {
+        int n = kb;
+        for (int i = 0; i < kb; ++i) {
           if (s_x[i] == s_arg[i]) {
             P.out_tokens[out0 + i] = s_x[i];
           } else {
@@ -431,7 +458,7 @@ __device__ int decide(const TailParams &P, int b) {
             break;
           }
         }
-        if (n == K) P.out_tokens[out0 + K] = s_arg[K];
+        if (n == kb) P.out_tokens[out0 + kb] = s_arg[kb];
         for (int i = n + 1; i < rows; ++i) P.out_tokens[out0 + i] = -1;
         P.out_n[b] = n;
       }
@@ -469,7 +496,7 @@ __device__ void select_token(const TailParams &P, int b, SeqState st) {
   ff S = ff_make(0.0f);
   for (int c = threadIdx.x; c < nchunk; c += kTailThreads) S = ff_add(S, ld_ff(&mass[c]));
   S = block_sum_ff(S, s_warp);
-  if (!(S.hi > 0.0f) && st.mode == kModeResidual) {
+  if (!(S.hi > 0.0f) && (st.mode == kModeResidual || st.mode == kModeResidualPoint)) {
     // p_j == q_j on this row: draw from p_j instead
     st.mode = kModeP;
     for (int c = 0; c < nchunk; ++c) {
@@ -598,10 +625,12 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailParams P) 
     const float2 *part = qrow ? P.w.part_q + static_cast<int64_t>(t - R) * P.dims.nsub
                               : P.w.part_p + static_cast<int64_t>(t) * P.dims.nsub;
     // one pass, 8 loads in flight per thread: running (max, sum) with
-    // rescaling whenever the running maximum grows
+    // rescaling whenever the running maximum grows.  A point-mass draft
+    // row has no partials: it is published as M = 0, S = 1.
+    const bool neutral = qrow && P.q_logits == nullptr;
     float m = -INFINITY, acc = 0.0f;
     int bad = 0;
-    for (int s0 = threadIdx.x; s0 < P.dims.nsub; s0 += kTailThreads * 8) {
+    for (int s0 = threadIdx.x; s0 < P.dims.nsub && !neutral; s0 += kTailThreads * 8) {
       float2 pm[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -628,6 +657,10 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailParams P) 
     if (!P.greedy && !bad) {
       const float mine = m > -INFINITY ? acc * expf(m - M) : 0.0f;
       S = block_sum_ff(ff_make(mine), s_wff);
+    }
+    if (neutral) {
+      M = 0.0f;
+      S = ff_make(1.0f);
     }
     if (bad) M = NAN;
     if (P.greedy && !bad) {

@@ -26,13 +26,14 @@ def oracle_verify(hidden, W_np, draft, q_logits, uniforms, T, want_logits=False,
     C oracle releases the GIL).  `rows` restricts it to some sequences."""
     H = si.to_oracle(hidden)
     X = si.to_oracle(draft)
-    Q = si.to_oracle(q_logits)
+    Q = None if q_logits is None else si.to_oracle(q_logits)
     U = si.to_oracle(uniforms)
     B = H.shape[0]
     seqs = list(range(B)) if rows is None else list(rows)
 
     def one(b):
-        return oracle.verify(H[b:b + 1], W_np, X[b:b + 1], Q[b:b + 1] if Q.size else Q,
+        q = None if q_logits is None else (Q[b:b + 1] if Q.size else Q)
+        return oracle.verify(H[b:b + 1], W_np, X[b:b + 1], q,
                              U[b:b + 1], T, want_logits=want_logits)
 
     res = list(_POOL.map(one, seqs))

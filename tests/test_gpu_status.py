@@ -63,8 +63,9 @@ def test_misaligned_and_bad_arguments_are_rejected_on_the_host(setup):
             sv.spec_verify_run(eng.h, inp["hidden"], W, inp["draft"], inp["q_logits"],
                                inp["uniforms"], T, out_t, out_n)
         assert e.value.code == sv.SV_ERR_ARG
+    # sampling needs the uniforms (q_logits may be NULL: point-mass drafts)
     with pytest.raises(sv.SpecVerifyError) as e:
-        sv.spec_verify_run(eng.h, inp["hidden"], W, inp["draft"], None, inp["uniforms"],
+        sv.spec_verify_run(eng.h, inp["hidden"], W, inp["draft"], inp["q_logits"], None,
                            1.0, out_t, out_n)
     assert e.value.code == sv.SV_ERR_ARG
     assert eng.status() == sv.SV_OK

@@ -20,7 +20,7 @@ def header_symbols():
     for fn in os.listdir(inc):
         if fn.endswith(".h"):
             text = open(os.path.join(inc, fn)).read()
-            names.update(re.findall(r"^[\w\s\*]*?\b(spec_verify_\w+)\s*\(", text, re.M))
+            names.update(re.findall(r"^[\w\s\*]*?\b(spec_\w+)\s*\(", text, re.M))
     return names
 
 
@@ -130,3 +130,17 @@ def test_rank_aggregation_over_gloo():
         assert p.exitcode == 0
     for r in (0, 1):
         assert results[r] == (1.5, 201)
+
+
+def test_ngram_draft_rejects_bad_arguments_before_cuda(lib):
+    f = lib.spec_ngram_draft
+    good = 1 << 12  # aligned fake addresses: the checks never dereference
+    assert f(None, 8, good, 1, 4, 2, 5, good, good, None) == sv.SV_ERR_ARG
+    assert f(good, 8, good, 0, 4, 2, 5, good, good, None) == sv.SV_ERR_ARG    # B
+    assert f(good, 0, good, 1, 4, 2, 5, good, good, None) == sv.SV_ERR_ARG    # ld
+    assert f(good, 8, good, 1, 0, 2, 5, good, good, None) == sv.SV_ERR_ARG    # K
+    assert f(good, 8, good, 1, 17, 2, 5, good, good, None) == sv.SV_ERR_ARG   # K > 16
+    assert f(good, 8, good, 1, 4, 0, 5, good, good, None) == sv.SV_ERR_ARG    # n_min
+    assert f(good, 8, good, 1, 4, 3, 2, good, good, None) == sv.SV_ERR_ARG    # n_max < n_min
+    assert f(good, 8, good, 1, 4, 2, 17, good, good, None) == sv.SV_ERR_ARG   # n_max > 16
+    assert f(good + 2, 8, good, 1, 4, 2, 5, good, good, None) == sv.SV_ERR_ALIGN
