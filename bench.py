@@ -6,6 +6,11 @@ bonus draw) for the Llama-3.1-8B-shaped LM head (V=128256, d=4096, B=1,
 K=4, T=1) on synthetic inputs, through the C ABI.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--drafts model|ngram]
+
+``--drafts ngram`` times the prompt-lookup variant instead: each step runs
+the GPU n-gram drafter over a synthetic 4096-token context and verifies its
+drafts as point masses (no draft logits are streamed).
 
 Prints one JSON line (rank 0).  Metric: verify rounds/s; ``roofline`` is
 the LM-head contraction kernel's algorithmic bytes over its CUDA-event
@@ -45,20 +50,50 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lmhead_tc_llama8b.md")
 # host-side helpers (no GPU needed; covered by the CPU tests)
 # ---------------------------------------------------------------------------
 
-def algorithmic_bytes(V, d, B, K, greedy=False, elt=2):
+def algorithmic_bytes(V, d, B, K, greedy=False, elt=2, point_mass=False, ctx_tokens=0):
     """Bytes one verify round must move: W_lm + q_logits + hidden + draft
-    tokens + uniforms + outputs (q and uniforms are not read when greedy)."""
+    tokens + uniforms + outputs (q and uniforms are not read when greedy; q
+    is absent for point-mass drafts, whose drafter reads ctx_tokens int32
+    context tokens per sequence)."""
     w = elt * V * d
-    q = 0 if greedy else 4 * B * K * V
+    q = 0 if (greedy or point_mass) else 4 * B * K * V
+    w += 4 * B * ctx_tokens
     h = elt * B * (K + 1) * d
     small = 4 * B * K + (0 if greedy else 4 * B * (K + 1)) + 4 * B * (K + 1) + 4 * B
     return w + q + h + small
 
 
-def contraction_bytes(V, d, B, K, greedy=False, elt=2):
+def contraction_bytes(V, d, B, K, greedy=False, elt=2, point_mass=False):
     """Algorithmic bytes of the contraction kernel alone: W_lm, hidden and
-    (sampling) the draft logits it streams for the softmax partials."""
-    return elt * V * d + elt * B * (K + 1) * d + (0 if greedy else 4 * B * K * V)
+    (sampling with draft logits) the draft logits it streams for the softmax
+    partials."""
+    q = 0 if (greedy or point_mass) else 4 * B * K * V
+    return elt * V * d + elt * B * (K + 1) * d + q
+
+
+CTX_TOKENS = 4096
+
+
+def make_contexts(B, V, seed, device, length=CTX_TOKENS, doc=3072):
+    """Synthetic prompt-lookup contexts: a random `doc`-token document, then
+    spans of 8-32 tokens copied from random places in it, up to `length`
+    tokens, so the last tokens recur earlier (as when an answer quotes its
+    input).  Returns tokens [B, length] int32 and lengths [B]."""
+    import torch
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    ctx = torch.empty((B, length), dtype=torch.int32)
+    for b in range(B):
+        ctx[b, :doc] = torch.randint(0, V, (doc,), generator=g, dtype=torch.int32)
+        pos = doc
+        while pos < length:
+            n = int(torch.randint(8, 33, (1,), generator=g))
+            s0 = int(torch.randint(0, doc - n, (1,), generator=g))
+            n = min(n, length - pos)
+            ctx[b, pos:pos + n] = ctx[b, s0:s0 + n]
+            pos += n
+    lens = torch.full((B,), length, dtype=torch.int32)
+    return ctx.to(device), lens.to(device)
 
 
 def n_input_sets(set_bytes, minimum=4, cap=256):
@@ -204,8 +239,9 @@ def oracle_rate(wl, W_np, inputs, budget_s):
     per_row = (time.perf_counter() - t0) / rows
     round_est = per_row * wl.V
     if round_est <= budget_s / 2:
+        q = inputs.get("q_logits")
         args = (si.to_oracle(inputs["hidden"]), W_np, si.to_oracle(inputs["draft"]),
-                si.to_oracle(inputs["q_logits"]), si.to_oracle(inputs["uniforms"]), wl.T)
+                None if q is None else si.to_oracle(q), si.to_oracle(inputs["uniforms"]), wl.T)
         n, t0 = 0, time.perf_counter()
         while True:
             oracle.verify(*args)
@@ -270,9 +306,12 @@ def reference_arm(args, wl, dev):
                     "d2h_bytes_per_step": 0}}
 
 
-def workload_config(wl, extra=None):
+def workload_config(wl, extra=None, drafts="model"):
+    what = (f"draft acceptance ~{wl.alpha}" if drafts == "model" else
+            f"prompt-lookup drafts (n-gram 5..2) over a {CTX_TOKENS}-token synthetic context, "
+            "verified as point masses")
     cfg = {"workload": f"Llama-3.1-8B-shaped LM-head verify round, V={wl.V}, d={wl.d}, "
-                       f"B={wl.B}, K={wl.K}, T={wl.T}, draft acceptance ~{wl.alpha}",
+                       f"B={wl.B}, K={wl.K}, T={wl.T}, {what}",
            "V": wl.V, "d": wl.d, "B": wl.B, "K": wl.K, "T": wl.T,
            "weights": "bf16 N(0, 0.02^2)", "alpha_target": wl.alpha}
     if extra:
@@ -291,6 +330,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--drafts", default="model", choices=["model", "ngram"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--clock-log", default=None)
@@ -321,11 +361,19 @@ def main():
     import speculative_decoding_verification_22_gb300 as sv
 
     T = wl.T
+    ngram = args.drafts == "ngram"
     W = si.make_weights(wl, seed=1 + 1000 * rank, device=dev)
-    set_bytes = (2 * wl.B * (wl.K + 1) * wl.d + 4 * wl.B * wl.K * wl.V
-                 + 4 * wl.B * wl.K + 4 * wl.B * (wl.K + 1))
+    set_bytes = (2 * wl.B * (wl.K + 1) * wl.d + 4 * wl.B * wl.K
+                 + (4 * wl.B * CTX_TOKENS if ngram else 4 * wl.B * wl.K * wl.V)
+                 + 4 * wl.B * (wl.K + 1))
     nsets = n_input_sets(set_bytes)
     sets = [si.make_round(wl, W, seed=10_000 + 1000 * rank + i) for i in range(nsets)]
+    if ngram:
+        for i, s in enumerate(sets):
+            s["q_logits"] = None
+            s["ctx"], s["lens"] = make_contexts(wl.B, wl.V, 20_000 + 1000 * rank + i, dev)
+            s["draft"] = torch.empty((wl.B, wl.K), dtype=torch.int32, device=dev)
+            s["dlen"] = torch.empty((wl.B,), dtype=torch.int32, device=dev)
     eng = sv.SpecVerify(wl.V, wl.d, wl.B, wl.K, "bf16", device=dev)
     stream = torch.cuda.Stream(device=dev)
     sv.spec_verify_set_stream(eng.h, stream)
@@ -337,10 +385,13 @@ def main():
 
     def run_set(i):
         s = sets[i]
+        if ngram:
+            sv.spec_ngram_draft(s["ctx"], s["lens"], wl.K, 2, 5, s["draft"], s["dlen"],
+                                stream=torch.cuda.current_stream())
         sv.spec_verify_run(eng.h, s["hidden"], W, s["draft"], s["q_logits"],
                            s["uniforms"], T, out_tok[i], out_n[i])
 
-    launches_per_run = sv.spec_verify_launches_per_run(eng.h, T)
+    launches_per_run = sv.spec_verify_launches_per_run(eng.h, T) + (1 if ngram else 0)
     # warm-up (also the first use of every input set)
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, nsets)):
@@ -414,7 +465,7 @@ def main():
     sv.spec_verify_timing(eng.h, False)
     k1_s = ms_k1 / 1e3 / n_k1
     peaks, peak_src = measured_peaks()
-    k1_bytes = contraction_bytes(wl.V, wl.d, wl.B, wl.K)
+    k1_bytes = contraction_bytes(wl.V, wl.d, wl.B, wl.K, point_mass=ngram)
     achieved = k1_bytes / k1_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
@@ -423,25 +474,48 @@ def main():
                 "kernel": "lmhead_tc_kernel (LM-head contraction + softmax partials)",
                 "kernel_us": k1_s * 1e6, "algorithmic_bytes_per_launch": k1_bytes,
                 "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
-                "step_frac_of_measured": algorithmic_bytes(wl.V, wl.d, wl.B, wl.K)
+                "step_frac_of_measured": algorithmic_bytes(
+                    wl.V, wl.d, wl.B, wl.K, point_mass=ngram,
+                    ctx_tokens=CTX_TOKENS if ngram else 0)
                 * value / world / 1e9 / peaks["hbm_gbs"]}
 
-    # end to end through the host-buffer entry point
+    # end to end through the host-buffer entry point (prompt lookup: the
+    # context, hidden states and uniforms copied in from pinned memory, the
+    # drafter and the verify call, the outputs copied back, every step)
     e2e_steps = min(steps, 1000)
-    pin = [{k: sets[i][k].cpu().pin_memory() for k in ("hidden", "draft", "q_logits", "uniforms")}
-           for i in range(min(nsets, 8))]
+    keys = ("hidden", "ctx", "lens", "uniforms") if ngram else (
+        "hidden", "draft", "q_logits", "uniforms")
+    pin = [{k: sets[i][k].cpu().pin_memory() for k in keys} for i in range(min(nsets, 8))]
     ht = torch.empty((wl.B, wl.K + 1), dtype=torch.int32).pin_memory()
     hn = torch.empty((wl.B,), dtype=torch.int32).pin_memory()
+    if ngram:
+        dbuf = {k: torch.empty_like(sets[0][k]) for k in keys}
+        dbuf.update(draft=torch.empty_like(sets[0]["draft"]),
+                    dlen=torch.empty_like(sets[0]["dlen"]))
+        dtok, dn = out_tok[0], out_n[0]
+
+    def e2e_step(p):
+        if not ngram:
+            sv.spec_verify_run_host(eng.h, p["hidden"], W, p["draft"], p["q_logits"],
+                                    p["uniforms"], T, ht, hn)
+            return
+        with torch.cuda.stream(stream):
+            for k in keys:
+                dbuf[k].copy_(p[k], non_blocking=True)
+            sv.spec_ngram_draft(dbuf["ctx"], dbuf["lens"], wl.K, 2, 5, dbuf["draft"],
+                                dbuf["dlen"], stream=stream)
+            sv.spec_verify_run(eng.h, dbuf["hidden"], W, dbuf["draft"], None,
+                               dbuf["uniforms"], T, dtok, dn)
+            ht.copy_(dtok, non_blocking=True)
+            hn.copy_(dn, non_blocking=True)
+        stream.synchronize()
+
     for i in range(3):
-        p = pin[i % len(pin)]
-        sv.spec_verify_run_host(eng.h, p["hidden"], W, p["draft"], p["q_logits"],
-                                p["uniforms"], T, ht, hn)
+        e2e_step(pin[i % len(pin)])
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(e2e_steps):
-        p = pin[i % len(pin)]
-        sv.spec_verify_run_host(eng.h, p["hidden"], W, p["draft"], p["q_logits"],
-                                p["uniforms"], T, ht, hn)
+        e2e_step(pin[i % len(pin)])
     e2e_el = time.perf_counter() - t0
     _, e2e_total = aggregate(e2e_el, e2e_steps)
     e2e_max, _ = aggregate(e2e_el, e2e_steps)
@@ -463,9 +537,10 @@ def main():
             "data": "synthetic",
             "config": workload_config(wl, {
                 "l2": f"inputs larger than L2: W_lm {2 * wl.V * wl.d} B per round plus "
-                      f"{nsets} rotating hidden/q/uniform sets ({nsets * set_bytes} B)",
+                      f"{nsets} rotating input sets ({nsets * set_bytes} B)",
                 "graph": graph is not None,
-                "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}),
+                "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+                drafts=args.drafts),
             "emitted_tokens_per_round": tokens_per_round,
             "emitted_tokens_per_s": value * tokens_per_round,
             "roofline": roofline,

@@ -44,7 +44,7 @@ def _drafter_case(dev, ctx, lens, K, n_min=2, n_max=5):
 
 
 @pytest.mark.parametrize("vocab,L,K", [(3, 300, 4), (8, 4000, 16), (50000, 2048, 4),
-                                       (2, 64, 1)])
+                                       (2, 64, 1), (6, 60000, 4)])  # last: beyond smem
 def test_drafter_matches_the_oracle(dev, vocab, L, K):
     rng = np.random.default_rng(vocab + L)
     B = 64
