@@ -77,6 +77,12 @@ def _load():
             lib.sv_oracle_ngram_draft.argtypes = [vp, i64, vp, i32, i32, i32,
                                                   i32, vp, vp]
             lib.sv_oracle_ngram_draft.restype = ctypes.c_int
+            lib.sv_oracle_truncate.argtypes = [i64, vp, dbl, i32, dbl, vp, vp, vp, vp]
+            lib.sv_oracle_truncate.restype = ctypes.c_int
+            lib.sv_oracle_verify_truncated.argtypes = [i64, i64, i32, i32, i32, vp, vp, vp,
+                                                       vp, vp, dbl, i32, dbl, i32, dbl, vp,
+                                                       vp, vp, vp, vp]
+            lib.sv_oracle_verify_truncated.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -236,3 +242,51 @@ def ngram_draft(tokens, lengths, K: int, n_min: int = 2, n_max: int = 5):
     if rc != OK:
         raise ValueError(f"sv_oracle_ngram_draft failed ({rc})")
     return draft, n
+
+
+def truncate(logits, T: float, top_k: int = 0, top_p: float = 1.0):
+    """Warped distribution of one row of logits (reading R11 in
+    sv_oracle.c): temperature, top-k (0: off), then top-p (1: off), both
+    cut by value with ties kept.  Returns (p, keep, gap, margin)."""
+    x = _c(logits, np.float64)
+    p = np.empty_like(x)
+    keep = np.empty(x.size, dtype=np.uint8)
+    gap, margin = ctypes.c_double(), ctypes.c_double()
+    rc = _load().sv_oracle_truncate(x.size, _ptr(x), float(T), int(top_k), float(top_p),
+                                    _ptr(p), _ptr(keep), ctypes.byref(gap),
+                                    ctypes.byref(margin))
+    if rc != OK:
+        raise ValueError(f"sv_oracle_truncate failed ({rc})")
+    return p, keep.astype(bool), gap.value, margin.value
+
+
+def verify_truncated(hidden, W, draft, q_logits, uniforms, temperature: float,
+                     p_top_k: int = 0, p_top_p: float = 1.0, q_top_k: int = 0,
+                     q_top_p: float = 1.0) -> dict:
+    """The verify step with truncated target and draft distributions (R11);
+    arguments as verify().  Adds trunc_gap [B] (smallest cut gap, logit
+    units) and trunc_margin [B] (smallest top-p mass margin)."""
+    hidden, dt = _matrix(hidden)
+    W, dt2 = _matrix(W)
+    if dt != dt2:
+        raise TypeError("hidden and W must share a dtype")
+    B, rows, d = hidden.shape
+    K = rows - 1
+    V = W.shape[0]
+    draft = _c(draft, np.int32).reshape(B, K)
+    T = float(temperature)
+    q = None if (K == 0 or q_logits is None) else _c(q_logits, np.float32).reshape(B, K, V)
+    u = None if T == 0.0 else _c(uniforms, np.float32).reshape(B, rows)
+    tokens = np.empty((B, rows), dtype=np.int32)
+    n_acc = np.empty((B,), dtype=np.int32)
+    dist = np.empty((B,), dtype=np.float64)
+    gap = np.full((B,), np.inf)
+    margin = np.full((B,), np.inf)
+    rc = _load().sv_oracle_verify_truncated(V, d, B, K, dt, _ptr(hidden), _ptr(W), _ptr(draft),
+                                            _ptr(q), _ptr(u), T, int(p_top_k), float(p_top_p),
+                                            int(q_top_k), float(q_top_p), _ptr(tokens),
+                                            _ptr(n_acc), _ptr(dist), _ptr(gap), _ptr(margin))
+    if rc not in (OK, ETOKEN):
+        raise ValueError(f"sv_oracle_verify_truncated failed ({rc})")
+    return {"tokens": tokens, "n_accepted": n_acc, "dist": dist, "trunc_gap": gap,
+            "trunc_margin": margin, "status": rc}

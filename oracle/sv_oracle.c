@@ -61,6 +61,18 @@
  *       token; the first n that has one wins, and of its occurrences the
  *       latest (the one starting closest to the end).  The draft is the up
  *       to K tokens that follow it in the context.
+ *   R11 Truncated sampling ([P1] "three remarks": warping by temperature,
+ *       top-k and top-p before forming p and q keeps the rule exact for
+ *       the warped target; [P4] "Where it breaks": p is the requested
+ *       distribution after temperature and truncation, q the distribution
+ *       that generated the proposal, each normalised over the vocabulary;
+ *       the two may use different settings).  Order: divide the logits by
+ *       T, keep the top_k largest (top_k = 0: all), renormalise, keep the
+ *       smallest most-probable set whose mass reaches top_p (top_p = 1:
+ *       all), renormalise.  Both cuts are by value: top-k keeps every x at
+ *       or above the k-th largest x (ties at the boundary kept), top-p
+ *       every x at or above the value of the first token, in descending
+ *       order, at which the cumulative mass reaches top_p.
  */
 #include <math.h>
 #include <stdint.h>
@@ -500,4 +512,185 @@ int sv_oracle_ngram_draft(const int32_t *tokens, int64_t ld, const int32_t *leng
     }
   }
   return SV_ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * Truncation of one row (reading R11).  x[0..V-1] are logits / T.  On
+ * return keep[v] = 1 for the kept tokens and *gap / *margin receive how
+ * close the cuts came to changing: *gap is the smallest distance, in x
+ * units, between a cut value and the nearest x on the other side of it;
+ * *margin the distance of top_p from the cumulative masses just before and
+ * at the top-p cut (INFINITY when a cut is off).  `order` must hold V
+ * int64 (scratch).
+ * ---------------------------------------------------------------------- */
+static const double *g_sort_x;
+static int cmp_desc(const void *a, const void *b) {
+  const double xa = g_sort_x[*(const int64_t *)a], xb = g_sort_x[*(const int64_t *)b];
+  if (xa > xb) return -1;
+  if (xa < xb) return 1;
+  const int64_t ia = *(const int64_t *)a, ib = *(const int64_t *)b;
+  return ia < ib ? -1 : (ia > ib);
+}
+
+static void truncate_row(int64_t V, const double *x, int32_t top_k, double top_p,
+                         unsigned char *keep, double *gap, double *margin, int64_t *order) {
+  *gap = INFINITY;
+  *margin = INFINITY;
+  for (int64_t v = 0; v < V; ++v) {
+    keep[v] = 1;
+    order[v] = v;
+  }
+  g_sort_x = x; /* the oracle is single-threaded per call */
+  qsort(order, (size_t)V, sizeof(int64_t), cmp_desc);
+  int64_t n_keep = V; /* kept tokens are order[0..n_keep-1] */
+  if (top_k > 0 && (int64_t)top_k < V) {
+    const double tk = x[order[top_k - 1]];
+    n_keep = top_k;
+    while (n_keep < V && x[order[n_keep]] >= tk) ++n_keep; /* ties kept */
+    if (n_keep < V) {
+      const double g = tk - x[order[n_keep]];
+      if (g < *gap) *gap = g;
+    }
+  }
+  if (top_p < 1.0) {
+    const double m = x[order[0]];
+    double S = 0.0;
+    for (int64_t i = 0; i < n_keep; ++i) S += exp(x[order[i]] - m);
+    double c = 0.0, c_prev = 0.0;
+    int64_t cut = n_keep - 1;
+    for (int64_t i = 0; i < n_keep; ++i) {
+      c_prev = c;
+      c += exp(x[order[i]] - m) / S;
+      if (c >= top_p) {
+        cut = i;
+        break;
+      }
+    }
+    const double tp = x[order[cut]];
+    const double mg0 = fabs(top_p - c_prev), mg1 = fabs(c - top_p);
+    *margin = mg0 < mg1 ? mg0 : mg1;
+    int64_t n2 = cut + 1;
+    while (n2 < n_keep && x[order[n2]] >= tp) ++n2; /* ties kept */
+    if (n2 < n_keep) {
+      const double g = tp - x[order[n2]];
+      if (g < *gap) *gap = g;
+    }
+    n_keep = n2;
+  }
+  for (int64_t i = n_keep; i < V; ++i) keep[order[i]] = 0;
+}
+
+/* Warped distribution of one row: softmax of x over the kept tokens. */
+static void warped_softmax(int64_t V, const double *x, const unsigned char *keep, double *p) {
+  double m = -INFINITY;
+  for (int64_t v = 0; v < V; ++v)
+    if (keep[v] && x[v] > m) m = x[v];
+  double S = 0.0;
+  for (int64_t v = 0; v < V; ++v) S += keep[v] ? exp(x[v] - m) : 0.0;
+  for (int64_t v = 0; v < V; ++v) p[v] = keep[v] ? exp(x[v] - m) / S : 0.0;
+}
+
+/* Truncates one row of logits (R11) and returns its warped distribution;
+ * keep_out [V] (may be NULL) marks the kept tokens, *gap (logit units) and
+ * *margin are the cut distances described at truncate_row. */
+int sv_oracle_truncate(int64_t V, const double *logits, double T, int32_t top_k, double top_p,
+                       double *p, unsigned char *keep_out, double *gap, double *margin) {
+  if (V < 1 || !logits || !p || !(T > 0.0) || top_k < 0 || !(top_p > 0.0) || top_p > 1.0)
+    return SV_ORACLE_EARG;
+  double *x = (double *)malloc(sizeof(double) * (size_t)V);
+  unsigned char *keep = (unsigned char *)malloc((size_t)V);
+  int64_t *order = (int64_t *)malloc(sizeof(int64_t) * (size_t)V);
+  if (!x || !keep || !order) {
+    free(x); free(keep); free(order);
+    return SV_ORACLE_ENOMEM;
+  }
+  for (int64_t v = 0; v < V; ++v) x[v] = logits[v] / T;
+  double g, mg;
+  truncate_row(V, x, top_k, top_p, keep, &g, &mg, order);
+  warped_softmax(V, x, keep, p);
+  if (keep_out) memcpy(keep_out, keep, (size_t)V);
+  if (gap) *gap = g * T;
+  if (margin) *margin = mg;
+  free(x); free(keep); free(order);
+  return SV_ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * The verify-and-sample step with truncated sampling (R11): as
+ * sv_oracle_verify at T > 0, with the target rows warped by (p_top_k,
+ * p_top_p) and the draft rows by (q_top_k, q_top_p).  trunc_gap [B]
+ * receives the smallest cut gap over the sequence's rows, in logit units,
+ * and trunc_margin [B] the smallest top-p mass margin (both may be NULL).
+ * T == 0 is greedy verification, which truncation does not change (the
+ * argmax is always kept).
+ * ---------------------------------------------------------------------- */
+int sv_oracle_verify_truncated(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
+                               const void *hidden, const void *W, const int32_t *draft,
+                               const float *q_logits, const float *u, double T,
+                               int32_t p_top_k, double p_top_p, int32_t q_top_k,
+                               double q_top_p, int32_t *out_tokens, int32_t *out_n,
+                               double *dist, double *trunc_gap, double *trunc_margin) {
+  if (T == 0.0)
+    return sv_oracle_verify(V, d, B, K, dtype, hidden, W, draft, q_logits, u, T, out_tokens,
+                            out_n, dist, NULL, NULL, NULL);
+  if (V < 1 || d < 1 || B < 1 || K < 0 || (dtype != 0 && dtype != 1) || !hidden || !W ||
+      !out_tokens || !out_n || !(T > 0.0) || T == INFINITY || !u || (K > 0 && !draft) ||
+      p_top_k < 0 || q_top_k < 0 || !(p_top_p > 0.0) || p_top_p > 1.0 ||
+      !(q_top_p > 0.0) || q_top_p > 1.0)
+    return SV_ORACLE_EARG;
+  const int point_mass = q_logits == NULL;
+  const int64_t rows = (int64_t)K + 1;
+  const size_t esz = dtype == 0 ? 2 : 4;
+  double *L = (double *)malloc(sizeof(double) * (size_t)(rows * V));
+  double *p = (double *)malloc(sizeof(double) * (size_t)(rows * V));
+  double *q = (double *)malloc(sizeof(double) * (size_t)((K > 0 ? K : 1) * V));
+  double *x = (double *)malloc(sizeof(double) * (size_t)V);
+  double *scratch = (double *)malloc(sizeof(double) * (size_t)V);
+  double *ud = (double *)malloc(sizeof(double) * (size_t)rows);
+  unsigned char *keep = (unsigned char *)malloc((size_t)V);
+  int64_t *order = (int64_t *)malloc(sizeof(int64_t) * (size_t)V);
+  if (!L || !p || !q || !x || !scratch || !ud || !keep || !order) {
+    free(L); free(p); free(q); free(x); free(scratch); free(ud); free(keep); free(order);
+    return SV_ORACLE_ENOMEM;
+  }
+  int status = SV_ORACLE_OK;
+  for (int32_t b = 0; b < B; ++b) {
+    const char *hb = (const char *)hidden + (size_t)b * (size_t)(rows * d) * esz;
+    int rc = sv_oracle_logits(V, d, rows, dtype, hb, W, 0, V, L);
+    if (rc != SV_ORACLE_OK) { status = rc; break; }
+    double gmin = INFINITY, mmin = INFINITY, g, mg;
+    for (int64_t i = 0; i < rows; ++i) {
+      for (int64_t v = 0; v < V; ++v) x[v] = L[i * V + v] / T;
+      truncate_row(V, x, p_top_k, p_top_p, keep, &g, &mg, order);
+      warped_softmax(V, x, keep, p + i * V);
+      if (g * T < gmin) gmin = g * T;
+      if (mg < mmin) mmin = mg;
+    }
+    for (int64_t i = 0; i < K && !point_mass; ++i) {
+      const float *ql = q_logits + ((int64_t)b * K + i) * V;
+      for (int64_t v = 0; v < V; ++v) x[v] = (double)ql[v] / T;
+      truncate_row(V, x, q_top_k, q_top_p, keep, &g, &mg, order);
+      warped_softmax(V, x, keep, q + i * V);
+      if (g * T < gmin) gmin = g * T;
+      if (mg < mmin) mmin = mg;
+    }
+    for (int64_t i = 0; i < rows; ++i) ud[i] = (double)u[(int64_t)b * rows + i];
+    const int32_t *xb = K > 0 ? draft + (int64_t)b * K : NULL;
+    int32_t *tb = out_tokens + (int64_t)b * rows;
+    double dd;
+    const int32_t n = rule_one_sequence(V, K, p, point_mass ? NULL : q, xb, ud, tb, &dd,
+                                        scratch);
+    if (n == SV_ORACLE_ETOKEN) {
+      status = SV_ORACLE_ETOKEN;
+      for (int64_t i = 0; i < rows; ++i) tb[i] = -1;
+      out_n[b] = -1;
+    } else {
+      out_n[b] = n;
+    }
+    if (dist) dist[b] = dd;
+    if (trunc_gap) trunc_gap[b] = gmin;
+    if (trunc_margin) trunc_margin[b] = mmin;
+  }
+  free(L); free(p); free(q); free(x); free(scratch); free(ud); free(keep); free(order);
+  return status;
 }
