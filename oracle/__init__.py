@@ -80,8 +80,8 @@ def _load():
             lib.sv_oracle_truncate.argtypes = [i64, vp, dbl, i32, dbl, vp, vp, vp, vp]
             lib.sv_oracle_truncate.restype = ctypes.c_int
             lib.sv_oracle_verify_truncated.argtypes = [i64, i64, i32, i32, i32, vp, vp, vp,
-                                                       vp, vp, dbl, i32, dbl, i32, dbl, vp,
-                                                       vp, vp, vp, vp]
+                                                       vp, vp, dbl, i32, dbl, i32, dbl, dbl,
+                                                       dbl, vp, vp, vp, vp, vp]
             lib.sv_oracle_verify_truncated.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -262,10 +262,11 @@ def truncate(logits, T: float, top_k: int = 0, top_p: float = 1.0):
 
 def verify_truncated(hidden, W, draft, q_logits, uniforms, temperature: float,
                      p_top_k: int = 0, p_top_p: float = 1.0, q_top_k: int = 0,
-                     q_top_p: float = 1.0) -> dict:
+                     q_top_p: float = 1.0, tol_gap: float = 0.0, tol_mass: float = 0.0) -> dict:
     """The verify step with truncated target and draft distributions (R11);
-    arguments as verify().  Adds trunc_gap [B] (smallest cut gap, logit
-    units) and trunc_margin [B] (smallest top-p mass margin)."""
+    arguments as verify().  Adds trunc_sens [B] (the largest warped mass of
+    a token next to a cut within tol_gap / tol_mass of flipping) and
+    trunc_xgap [B] (the smallest |logit(x_i) - cut|), see sv_oracle.c."""
     hidden, dt = _matrix(hidden)
     W, dt2 = _matrix(W)
     if dt != dt2:
@@ -280,13 +281,14 @@ def verify_truncated(hidden, W, draft, q_logits, uniforms, temperature: float,
     tokens = np.empty((B, rows), dtype=np.int32)
     n_acc = np.empty((B,), dtype=np.int32)
     dist = np.empty((B,), dtype=np.float64)
-    gap = np.full((B,), np.inf)
-    margin = np.full((B,), np.inf)
+    sens = np.zeros((B,))
+    xgap = np.full((B,), np.inf)
     rc = _load().sv_oracle_verify_truncated(V, d, B, K, dt, _ptr(hidden), _ptr(W), _ptr(draft),
                                             _ptr(q), _ptr(u), T, int(p_top_k), float(p_top_p),
-                                            int(q_top_k), float(q_top_p), _ptr(tokens),
-                                            _ptr(n_acc), _ptr(dist), _ptr(gap), _ptr(margin))
+                                            int(q_top_k), float(q_top_p), float(tol_gap),
+                                            float(tol_mass), _ptr(tokens), _ptr(n_acc),
+                                            _ptr(dist), _ptr(sens), _ptr(xgap))
     if rc not in (OK, ETOKEN):
         raise ValueError(f"sv_oracle_verify_truncated failed ({rc})")
-    return {"tokens": tokens, "n_accepted": n_acc, "dist": dist, "trunc_gap": gap,
-            "trunc_margin": margin, "status": rc}
+    return {"tokens": tokens, "n_accepted": n_acc, "dist": dist, "trunc_sens": sens,
+            "trunc_xgap": xgap, "status": rc}

@@ -533,9 +533,12 @@ static int cmp_desc(const void *a, const void *b) {
 }
 
 static void truncate_row(int64_t V, const double *x, int32_t top_k, double top_p,
-                         unsigned char *keep, double *gap, double *margin, int64_t *order) {
+                         unsigned char *keep, double *gap, double *margin, int64_t *order,
+                         double *cut, int64_t *adj0, int64_t *adj1) {
   *gap = INFINITY;
   *margin = INFINITY;
+  *cut = -INFINITY;
+  *adj0 = *adj1 = -1; /* last kept and first dropped token of the final cut */
   for (int64_t v = 0; v < V; ++v) {
     keep[v] = 1;
     order[v] = v;
@@ -578,6 +581,11 @@ static void truncate_row(int64_t V, const double *x, int32_t top_k, double top_p
     n_keep = n2;
   }
   for (int64_t i = n_keep; i < V; ++i) keep[order[i]] = 0;
+  if (n_keep < V) {
+    *cut = x[order[n_keep - 1]];
+    *adj0 = order[n_keep - 1];
+    *adj1 = order[n_keep];
+  }
 }
 
 /* Warped distribution of one row: softmax of x over the kept tokens. */
@@ -605,8 +613,9 @@ int sv_oracle_truncate(int64_t V, const double *logits, double T, int32_t top_k,
     return SV_ORACLE_ENOMEM;
   }
   for (int64_t v = 0; v < V; ++v) x[v] = logits[v] / T;
-  double g, mg;
-  truncate_row(V, x, top_k, top_p, keep, &g, &mg, order);
+  double g, mg, cut;
+  int64_t a0, a1;
+  truncate_row(V, x, top_k, top_p, keep, &g, &mg, order, &cut, &a0, &a1);
   warped_softmax(V, x, keep, p);
   if (keep_out) memcpy(keep_out, keep, (size_t)V);
   if (gap) *gap = g * T;
@@ -618,18 +627,27 @@ int sv_oracle_truncate(int64_t V, const double *logits, double T, int32_t top_k,
 /* ------------------------------------------------------------------------
  * The verify-and-sample step with truncated sampling (R11): as
  * sv_oracle_verify at T > 0, with the target rows warped by (p_top_k,
- * p_top_p) and the draft rows by (q_top_k, q_top_p).  trunc_gap [B]
- * receives the smallest cut gap over the sequence's rows, in logit units,
- * and trunc_margin [B] the smallest top-p mass margin (both may be NULL).
- * T == 0 is greedy verification, which truncation does not change (the
- * argmax is always kept).
+ * p_top_p) and the draft rows by (q_top_k, q_top_p).  T == 0 is greedy
+ * verification, which truncation does not change (the argmax is always
+ * kept).
+ * Two per-sequence outputs (may be NULL) say how far the round is from a
+ * membership decision that rounding could flip, for a caller whose logits
+ * carry an error of up to tol_gap (logit units) and whose cumulative
+ * masses carry up to tol_mass:
+ *   trunc_sens [B]  the largest warped probability of a token next to a
+ *                   cut that lies within those tolerances (0 if none):
+ *                   moving that token across the cut moves every threshold
+ *                   and CDF edge of the round by about that much;
+ *   trunc_xgap [B]  the smallest |logit(x_i) - cut| over the draft tokens
+ *                   and their rows' cuts (logit units; INFINITY if none).
  * ---------------------------------------------------------------------- */
 int sv_oracle_verify_truncated(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
                                const void *hidden, const void *W, const int32_t *draft,
                                const float *q_logits, const float *u, double T,
                                int32_t p_top_k, double p_top_p, int32_t q_top_k,
-                               double q_top_p, int32_t *out_tokens, int32_t *out_n,
-                               double *dist, double *trunc_gap, double *trunc_margin) {
+                               double q_top_p, double tol_gap, double tol_mass,
+                               int32_t *out_tokens, int32_t *out_n, double *dist,
+                               double *trunc_sens, double *trunc_xgap) {
   if (T == 0.0)
     return sv_oracle_verify(V, d, B, K, dtype, hidden, W, draft, q_logits, u, T, out_tokens,
                             out_n, dist, NULL, NULL, NULL);
@@ -658,21 +676,34 @@ int sv_oracle_verify_truncated(int64_t V, int64_t d, int32_t B, int32_t K, int32
     const char *hb = (const char *)hidden + (size_t)b * (size_t)(rows * d) * esz;
     int rc = sv_oracle_logits(V, d, rows, dtype, hb, W, 0, V, L);
     if (rc != SV_ORACLE_OK) { status = rc; break; }
-    double gmin = INFINITY, mmin = INFINITY, g, mg;
-    for (int64_t i = 0; i < rows; ++i) {
-      for (int64_t v = 0; v < V; ++v) x[v] = L[i * V + v] / T;
-      truncate_row(V, x, p_top_k, p_top_p, keep, &g, &mg, order);
-      warped_softmax(V, x, keep, p + i * V);
-      if (g * T < gmin) gmin = g * T;
-      if (mg < mmin) mmin = mg;
-    }
-    for (int64_t i = 0; i < K && !point_mass; ++i) {
-      const float *ql = q_logits + ((int64_t)b * K + i) * V;
-      for (int64_t v = 0; v < V; ++v) x[v] = (double)ql[v] / T;
-      truncate_row(V, x, q_top_k, q_top_p, keep, &g, &mg, order);
-      warped_softmax(V, x, keep, q + i * V);
-      if (g * T < gmin) gmin = g * T;
-      if (mg < mmin) mmin = mg;
+    const int32_t *xb0 = K > 0 ? draft + (int64_t)b * K : NULL;
+    double sens = 0.0, xgap = INFINITY, g, mg, cut;
+    int64_t a0, a1;
+    for (int64_t side = 0; side < 2; ++side) {
+      const int64_t nrow = side == 0 ? rows : (point_mass ? 0 : K);
+      for (int64_t i = 0; i < nrow; ++i) {
+        if (side == 0) {
+          for (int64_t v = 0; v < V; ++v) x[v] = L[i * V + v] / T;
+        } else {
+          const float *ql = q_logits + ((int64_t)b * K + i) * V;
+          for (int64_t v = 0; v < V; ++v) x[v] = (double)ql[v] / T;
+        }
+        double *dst = side == 0 ? p + i * V : q + i * V;
+        truncate_row(V, x, side == 0 ? p_top_k : q_top_k, side == 0 ? p_top_p : q_top_p,
+                     keep, &g, &mg, order, &cut, &a0, &a1);
+        warped_softmax(V, x, keep, dst);
+        if (a0 >= 0 && (g * T < tol_gap || mg < tol_mass)) {
+          /* the neighbours of the cut, as warped probabilities if kept */
+          const double w0 = dst[a0];
+          const double w1 = w0 * exp(x[a1] - x[a0]);
+          const double s = w0 > w1 ? w0 : w1;
+          if (s > sens) sens = s;
+        }
+        if (a0 >= 0 && i < K && xb0 && xb0[i] >= 0 && (int64_t)xb0[i] < V) {
+          const double dx = fabs(x[xb0[i]] - cut) * T;
+          if (dx < xgap) xgap = dx;
+        }
+      }
     }
     for (int64_t i = 0; i < rows; ++i) ud[i] = (double)u[(int64_t)b * rows + i];
     const int32_t *xb = K > 0 ? draft + (int64_t)b * K : NULL;
@@ -688,8 +719,8 @@ int sv_oracle_verify_truncated(int64_t V, int64_t d, int32_t B, int32_t K, int32
       out_n[b] = n;
     }
     if (dist) dist[b] = dd;
-    if (trunc_gap) trunc_gap[b] = gmin;
-    if (trunc_margin) trunc_margin[b] = mmin;
+    if (trunc_sens) trunc_sens[b] = sens;
+    if (trunc_xgap) trunc_xgap[b] = xgap;
   }
   free(L); free(p); free(q); free(x); free(scratch); free(ud); free(keep); free(order);
   return status;
