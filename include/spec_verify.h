@@ -212,6 +212,32 @@ int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidden, const vo
                             const float *uniforms, float temperature, int32_t *out_tokens,
                             int32_t *out_n_accepted);
 
+/* The step with truncated sampling: as spec_verify_run, with the target
+ * distributions warped by (target_top_k, target_top_p) and the draft
+ * distributions by (draft_top_k, draft_top_p) before the rule
+ * ("Speculative Decoding: Two Models, One Voice", three remarks: warping by
+ * temperature, top-k and top-p before forming p and q keeps the rule exact
+ * for the warped target; "Speculative Decoding: The Algebra and the Proof",
+ * "Where it breaks": p is the requested distribution after temperature and
+ * truncation, q the distribution that generated the proposal, and the two
+ * may use different settings).  Order: logits / T, then top-k, then top-p
+ * on the renormalised top-k distribution.  Both cuts are by value, ties
+ * kept: top-k keeps every token whose logit is at least the k-th largest
+ * (top_k = 0 or >= V: no cut), top-p every token whose logit is at least
+ * that of the first token, in descending order, at which the cumulative
+ * probability reaches top_p (top_p = 1: no cut).  Membership is decided on
+ * the fp32 logits the step computes.  At T == 0 (greedy) the cuts change
+ * nothing; with q_logits == NULL the draft settings are unused.  One more
+ * launch (the cut of every truncated row) runs between the contraction and
+ * the decision kernel.
+ * Errors: as spec_verify_run, and SV_ERR_ARG for top_k < 0 or top_p outside
+ * (0, 1]. */
+int spec_verify_run_truncated(spec_verify_t *h, const void *hidden, const void *W_lm,
+                              const int32_t *draft_tokens, const float *q_logits,
+                              const float *uniforms, float temperature, int32_t target_top_k,
+                              float target_top_p, int32_t draft_top_k, float draft_top_p,
+                              int32_t *out_tokens, int32_t *out_n_accepted);
+
 /* ---------------------------------------------------------------------------
  * Prompt-lookup drafting ("Speculative Decoding: Guess Several Tokens, Check
  * Them in One Pass", "Drafts without a model"; "Speculative Decoding: Two

@@ -40,7 +40,7 @@ EXPORTS = ("spec_verify_create", "spec_verify_run", "spec_verify_run_host",
            "spec_verify_set_wait_limit", "spec_verify_timing",
            "spec_verify_timing_read", "spec_verify_launches_per_run",
            "spec_verify_strerror", "spec_verify_destroy",
-           "spec_verify_run_noalloc", "spec_ngram_draft")
+           "spec_verify_run_noalloc", "spec_ngram_draft", "spec_verify_run_truncated")
 
 
 class SpecVerifyError(RuntimeError):
@@ -89,6 +89,8 @@ def load_library():
         lib.spec_verify_run_noalloc.argtypes = [ctypes.POINTER(sv_config_t), vp, vp, vp, vp,
                                                 vp, f32, vp, vp]
         i32 = ctypes.c_int32
+        lib.spec_verify_run_truncated.argtypes = [vp, vp, vp, vp, vp, vp, f32, i32, f32, i32,
+                                                  f32, vp, vp]
         lib.spec_ngram_draft.argtypes = [vp, ctypes.c_int64, vp, i32, i32, i32, i32, vp, vp,
                                          vp]
         for name in EXPORTS:
@@ -211,6 +213,18 @@ def spec_verify_run_noalloc(V, d, B, K, dtype, hidden, W_lm, draft_tokens, q_log
         "spec_verify_run_noalloc")
 
 
+def spec_verify_run_truncated(h, hidden, W_lm, draft_tokens, q_logits, uniforms,
+                              temperature: float, target_top_k: int, target_top_p: float,
+                              draft_top_k: int, draft_top_p: float, out_tokens,
+                              out_n_accepted) -> None:
+    """The step with truncated sampling (top-k, then top-p; per side)."""
+    _check(load_library().spec_verify_run_truncated(
+        h, _ptr(hidden), _ptr(W_lm), _ptr(draft_tokens), _ptr(q_logits), _ptr(uniforms),
+        float(temperature), int(target_top_k), float(target_top_p), int(draft_top_k),
+        float(draft_top_p), _ptr(out_tokens), _ptr(out_n_accepted)),
+        "spec_verify_run_truncated")
+
+
 def spec_ngram_draft(tokens, lengths, K: int, n_min: int = 2, n_max: int = 5,
                      out_draft=None, out_len=None, stream=None):
     """Prompt-lookup drafts for B contexts (tokens [B, L] int32 on the GPU,
@@ -252,6 +266,19 @@ class SpecVerify:
             out_n_accepted = torch.empty((self.B,), dtype=torch.int32, device=self.device)
         spec_verify_run(self.h, hidden, W_lm, draft_tokens, q_logits, uniforms,
                         temperature, out_tokens, out_n_accepted)
+        return out_tokens, out_n_accepted
+
+    def run_truncated(self, hidden, W_lm, draft_tokens, q_logits, uniforms, temperature,
+                      target_top_k=0, target_top_p=1.0, draft_top_k=0, draft_top_p=1.0,
+                      out_tokens=None, out_n_accepted=None):
+        if out_tokens is None:
+            out_tokens = torch.empty((self.B, self.K + 1), dtype=torch.int32,
+                                     device=self.device)
+        if out_n_accepted is None:
+            out_n_accepted = torch.empty((self.B,), dtype=torch.int32, device=self.device)
+        spec_verify_run_truncated(self.h, hidden, W_lm, draft_tokens, q_logits, uniforms,
+                                  temperature, target_top_k, target_top_p, draft_top_k,
+                                  draft_top_p, out_tokens, out_n_accepted)
         return out_tokens, out_n_accepted
 
     def status(self) -> int:

@@ -17,6 +17,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspec_verify.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["sv_api.cu", "sv_lmhead_tc.cu", "sv_lmhead_simt.cu", "sv_tail.cu", "sv_noalloc.cu",
+           "sv_trunc.cu",
            "sv_ngram.cu"]
 HEADERS = ["sv_internal.cuh", "sv_kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -71,7 +71,7 @@ void free_all(spec_verify *h) {
                   h->w.split_cnt, h->w.status,      h->w.abort_epoch, h->w.ticket,
                   h->w.finished,  h->w.row_count,   h->w.chunk_count, h->w.seq_flag,
                   h->w.seq_final,
-                  h->w.cand,      h->w.draft_logit,
+                  h->w.cand,      h->w.draft_logit, h->w.row_tau,
                   h->st_hidden,   h->st_draft,      h->st_q,        h->st_u,
                   h->st_tokens,   h->st_n};
   for (void *p : ptrs)
@@ -202,6 +202,7 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
             dalloc(&h->w.seq_flag, D.B) &&
             dalloc(&h->w.seq_final, D.B) &&
             dalloc(&h->w.cand, static_cast<size_t>(R) * (1 + sv::kMaxCand)) &&
+            dalloc(&h->w.row_tau, static_cast<size_t>(R + D.RQ)) &&
             dalloc(&h->w.draft_logit, static_cast<size_t>(D.RQ)) &&
             dalloc(&h->w.chunk_mass, static_cast<size_t>(D.B) * D.nchunk) &&
             dalloc(&h->w.split_buf, split_floats) &&
@@ -258,9 +259,58 @@ int spec_verify_launches_per_run(spec_verify_t *h, float temperature) {
   return 2;
 }
 
+namespace {
+
+// Truncated sampling settings of one run (which rows are cut, and how).
+struct TruncSpec {
+  int p_cut = 0, q_cut = 0;
+  int p_top_k = 0, q_top_k = 0;
+  float p_top_p = 1.0f, q_top_p = 1.0f;
+};
+
+int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
+             const int32_t *draft_tokens, const float *q_logits, const float *uniforms,
+             float temperature, int32_t *out_tokens, int32_t *out_n_accepted,
+             const TruncSpec &tr);
+
+}  // namespace
+
 int spec_verify_run(spec_verify_t *h, const void *hidden, const void *W_lm,
                     const int32_t *draft_tokens, const float *q_logits, const float *uniforms,
                     float temperature, int32_t *out_tokens, int32_t *out_n_accepted) {
+  return run_impl(h, hidden, W_lm, draft_tokens, q_logits, uniforms, temperature, out_tokens,
+                  out_n_accepted, TruncSpec{});
+}
+
+int spec_verify_run_truncated(spec_verify_t *h, const void *hidden, const void *W_lm,
+                              const int32_t *draft_tokens, const float *q_logits,
+                              const float *uniforms, float temperature, int32_t target_top_k,
+                              float target_top_p, int32_t draft_top_k, float draft_top_p,
+                              int32_t *out_tokens, int32_t *out_n_accepted) {
+  if (!h) return SV_ERR_ARG;
+  if (target_top_k < 0 || draft_top_k < 0 || !(target_top_p > 0.0f) || !(target_top_p <= 1.0f) ||
+      !(draft_top_p > 0.0f) || !(draft_top_p <= 1.0f))
+    return SV_ERR_ARG;
+  const sv::Dims &D = h->dims;
+  TruncSpec tr;
+  const bool sampling = temperature > 0.0f;  // greedy keeps the argmax, which no cut removes
+  tr.p_top_k = target_top_k;
+  tr.p_top_p = target_top_p;
+  tr.q_top_k = draft_top_k;
+  tr.q_top_p = draft_top_p;
+  tr.p_cut = sampling && ((target_top_k > 0 && target_top_k < D.V) || target_top_p < 1.0f);
+  tr.q_cut = sampling && q_logits != nullptr && D.K > 0 &&
+             ((draft_top_k > 0 && draft_top_k < D.V) || draft_top_p < 1.0f);
+  return run_impl(h, hidden, W_lm, draft_tokens, q_logits, uniforms, temperature, out_tokens,
+                  out_n_accepted, tr);
+}
+
+namespace {
+
+int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
+             const int32_t *draft_tokens, const float *q_logits, const float *uniforms,
+             float temperature, int32_t *out_tokens, int32_t *out_n_accepted,
+             const TruncSpec &tr) {
   if (!h || !hidden || !W_lm || !out_tokens || !out_n_accepted) return SV_ERR_ARG;
   if (!(temperature >= 0.0f) || !std::isfinite(temperature)) return SV_ERR_ARG;
   const sv::Dims &D = h->dims;
@@ -354,9 +404,27 @@ int spec_verify_run(spec_verify_t *h, const void *hidden, const void *W_lm,
   T.wait_limit_ns = h->wait_limit_ns;
   T.split_cnt_n = h->num_sms * 4;
   T.draft_logits_ready = h->cfg.dtype == SV_BF16 ? 1 : 0;
+  T.p_cut = tr.p_cut;
+  T.q_cut = tr.q_cut;
+  if (tr.p_cut || tr.q_cut) {
+    sv::TruncParams TP{};
+    TP.dims = D;
+    TP.w = h->w;
+    TP.q_logits = q_logits;
+    TP.inv_t = inv_t;
+    TP.p_cut = tr.p_cut;
+    TP.q_cut = tr.q_cut;
+    TP.p_top_k = tr.p_top_k;
+    TP.q_top_k = tr.q_top_k;
+    TP.p_top_p = tr.p_top_p;
+    TP.q_top_p = tr.q_top_p;
+    if (sv::launch_trunc(TP, st) != cudaSuccess) return SV_ERR_CUDA;
+  }
   if (sv::launch_tail(T, st) != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
 }
+
+}  // namespace
 
 int spec_verify_status(spec_verify_t *h) {
   if (!h) return SV_ERR_ARG;

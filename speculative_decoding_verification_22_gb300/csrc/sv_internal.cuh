@@ -20,6 +20,7 @@ constexpr int kTileM = 128;     // vocab rows per tensor-core tile (MMA M)
 constexpr int kChunk = 4096;    // vocab entries per residual-mass chunk
 constexpr int kTailThreads = 512;
 constexpr int kChunkPerThread = kChunk / kTailThreads;  // 8
+constexpr int kTailWarps = kTailThreads / 32;
 constexpr int kMaxCand = 64;    // greedy: near-maximal subtiles listed per row
 
 // Per-sequence state handed from the decision pass to the residual and
@@ -39,7 +40,9 @@ struct SeqState {
   float q_max;   // q(v) = expf(ql[v] * inv_t - q_max) * q_corr
   float q_corr;
   float u_final; // the final uniform
-  int pad[3];
+  float p_tau;   // truncated sampling: p(v) = 0 where L[v] < p_tau (-inf: no cut)
+  float q_tau;   // likewise q(v) = 0 where ql[v] < q_tau
+  int pad;
 };
 
 struct Dims {
@@ -73,6 +76,7 @@ struct Work {
   unsigned *seq_flag;  // [B]   epoch of the sequence's published decision
   int *seq_final;      // [B]   decision + chunk-phase arrivals, poison bit
   int *cand;           // [R, 1 + kMaxCand] greedy: count, then subtile ids
+  float *row_tau;      // [R + RQ] truncated sampling: the row's cut logit
   float2 *draft_logit; // [RQ]  exact logit of each draft token (float-float)
 };
 
@@ -440,6 +444,41 @@ __device__ __forceinline__ ff dot_bf16_warp(const uint4 *h, const uint4 *w, int6
   }
   const float hi2 = __fadd_rn(s, c);
   return warp_sum_ff(ff{hi2, __fsub_rn(c, __fsub_rn(hi2, s))});
+}
+
+// ---------------------------------------------------------------------------
+// Block-level helpers (kTailThreads threads)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void st_ff_raw(float2 *p, ff v) { *p = make_float2(v.hi, v.lo); }
+
+__device__ __forceinline__ ff block_sum_ff(ff x, ff *s_warp) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  x = warp_sum_ff(x);
+  __syncthreads();
+  if (lane == 0) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    ff t = lane < kTailWarps ? s_warp[lane] : ff_make(0.0f);
+    t = warp_sum_ff(t);
+    if (lane == 0) s_warp[0] = t;
+  }
+  __syncthreads();
+  return s_warp[0];
+}
+
+__device__ __forceinline__ float block_max_f(float x, float *s_warp) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  x = warp_max(x);
+  __syncthreads();
+  if (lane == 0) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    float t = lane < kTailWarps ? s_warp[lane] : -INFINITY;
+    t = warp_max(t);
+    if (lane == 0) s_warp[0] = t;
+  }
+  __syncthreads();
+  return s_warp[0];
 }
 
 }  // namespace sv

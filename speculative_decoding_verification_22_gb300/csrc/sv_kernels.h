@@ -71,8 +71,21 @@ struct TailParams {
   uint64_t wait_limit_ns;  // bound of the wait for a sequence's decision
   int split_cnt_n;         // entries of w.split_cnt
   int draft_logits_ready;  // w.draft_logit was written by the contraction
+  int p_cut, q_cut;        // truncated target / draft rows: (M, S, cut) are given
 };
 cudaError_t launch_tail(const TailParams &P, cudaStream_t stream);
+
+// ---- truncated sampling: (M, S, cut) of every truncated row --------------
+struct TruncParams {
+  Dims dims;
+  Work w;
+  const float *q_logits;   // [RQ, V]
+  float inv_t;
+  int p_cut, q_cut;        // which side is truncated
+  int p_top_k, q_top_k;    // 0: no top-k
+  float p_top_p, q_top_p;  // 1: no top-p
+};
+cudaError_t launch_trunc(const TruncParams &P, cudaStream_t stream);
 
 // cudaLaunchKernelEx with programmatic stream serialisation (PDL).
 cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, size_t smem,

@@ -38,40 +38,9 @@
 namespace sv {
 
 // ---------------------------------------------------------------------------
-// Block-level helpers (kTailThreads threads)
+// Block-level helpers (kTailThreads threads; block_sum_ff and block_max_f
+// live in sv_internal.cuh)
 // ---------------------------------------------------------------------------
-constexpr int kTailWarps = kTailThreads / 32;
-
-__device__ __forceinline__ ff block_sum_ff(ff x, ff *s_warp) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  x = warp_sum_ff(x);
-  __syncthreads();
-  if (lane == 0) s_warp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    ff t = lane < kTailWarps ? s_warp[lane] : ff_make(0.0f);
-    t = warp_sum_ff(t);
-    if (lane == 0) s_warp[0] = t;
-  }
-  __syncthreads();
-  return s_warp[0];
-}
-
-__device__ __forceinline__ float block_max_f(float x, float *s_warp) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  x = warp_max(x);
-  __syncthreads();
-  if (lane == 0) s_warp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    float t = lane < kTailWarps ? s_warp[lane] : -INFINITY;
-    t = warp_max(t);
-    if (lane == 0) s_warp[0] = t;
-  }
-  __syncthreads();
-  return s_warp[0];
-}
-
 // Exclusive prefix sum over the block, in thread order (float-float).
 __device__ __forceinline__ ff block_excl_scan_ff(ff x, ff *s_warp) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -226,9 +195,12 @@ __device__ int exact_argmax(const TailParams &P, int64_t r, float M, int lane) {
 // recomputed.
 __device__ __forceinline__ float draw_weight(const SeqState &st, int64_t v, float l, float ql,
                                              float inv_t) {
-  const float p = __fmul_rn(expf(fmaf(l, inv_t, -st.p_max)), st.p_corr);
+  // truncated sampling: entries below a row's cut have no mass (the cut is
+  // -inf for an untruncated row)
+  const float p = l >= st.p_tau ? __fmul_rn(expf(fmaf(l, inv_t, -st.p_max)), st.p_corr) : 0.0f;
   if (st.mode == kModeResidual) {
-    const float q = __fmul_rn(expf(fmaf(ql, inv_t, -st.q_max)), st.q_corr);
+    const float q =
+        ql >= st.q_tau ? __fmul_rn(expf(fmaf(ql, inv_t, -st.q_max)), st.q_corr) : 0.0f;
     return fmaxf(__fsub_rn(p, q), 0.0f);
   }
   if (st.mode == kModeResidualPoint && v == st.q_row) return 0.0f;
@@ -326,6 +298,7 @@ __device__ int decide(const TailParams &P, int b) {
   __shared__ ff s_lp_s[SV_MAX_K + 1], s_lq_s[SV_MAX_K];       // row sums
   __shared__ float s_ql[SV_MAX_K], s_u[SV_MAX_K + 1];
   __shared__ int s_x[SV_MAX_K], s_arg[SV_MAX_K + 1];
+  __shared__ float s_tp[SV_MAX_K + 1], s_tq[SV_MAX_K], s_lbuf[SV_MAX_K];  // cuts, L[x]
   __shared__ int s_err, s_fin, s_kb;
   // no draft distribution: the draft was proposed with certainty (q is a
   // point mass at each proposed token) and a -1 ends it early
@@ -336,6 +309,7 @@ __device__ int decide(const TailParams &P, int b) {
   // everything the walk needs, loaded in parallel
   if (threadIdx.x < rows) {
     const int i = threadIdx.x;
+    s_tp[i] = P.p_cut ? __ldcg(&P.w.row_tau[out0 + i]) : -INFINITY;
     s_lp_m[i] = __ldcg(&P.w.row_m[out0 + i]);
     s_lp_s[i] = ld_ff(&P.w.row_s[out0 + i]);
     if (!P.greedy) s_u[i] = P.u[out0 + i];
@@ -358,6 +332,10 @@ __device__ int decide(const TailParams &P, int b) {
       s_lq_m[i] = __ldcg(&P.w.row_m[rq]);
       s_lq_s[i] = ld_ff(&P.w.row_s[rq]);
       s_ql[i] = point ? 0.0f : P.q_logits[(static_cast<int64_t>(b) * K + i) * V + x];
+      // truncated sampling: membership of x is decided on the same fp32
+      // values the cut was found on
+      s_tq[i] = P.q_cut ? __ldcg(&P.w.row_tau[rq]) : -INFINITY;
+      s_lbuf[i] = P.p_cut ? __ldcg(&P.w.logits[(out0 + i) * V + x]) : 0.0f;
       s_l[i] = ld_ff(&P.w.draft_logit[static_cast<int64_t>(b) * K + i]);
       const bool fin = isfinite(s_lq_m[i]) && s_lq_s[i].hi > 0.0f && s_lq_s[i].hi < INFINITY;
       if (!fin) atomicCAS(&s_err, 0, SV_ERR_NONFINITE);
@@ -396,7 +374,13 @@ __device__ int decide(const TailParams &P, int b) {
         const ff lp = ff_add(ff_div_f(l, T), ff_make(-s_lp_m[i]));
         const ff lq = ff_add(ff_div_f(ff_make(s_ql[i]), T), ff_make(-s_lq_m[i]));
         const float ratio = ff_to_f(ff_div(s_lq_s[i], s_lp_s[i]));
-        s_acc[i] = isfinite(l.hi) ? (s_u[i] < accept_threshold(lp, lq, ratio) ? 1 : 0) : -1;
+        // outside the truncated target: p(x) = 0, rejected; outside the
+        // truncated draft only: q(x) = 0 < p(x), accepted (R2)
+        const bool keep_p = !P.p_cut || s_lbuf[i] >= s_tp[i];
+        const bool keep_q = !P.q_cut || s_ql[i] >= s_tq[i];
+        const float thr =
+            keep_p ? (keep_q ? accept_threshold(lp, lq, ratio) : INFINITY) : 0.0f;
+        s_acc[i] = isfinite(l.hi) ? (s_u[i] < thr ? 1 : 0) : -1;
       }
     } else {
       for (int i = warp; i <= kb; i += kTailWarps) {
@@ -433,10 +417,13 @@ __device__ int decide(const TailParams &P, int b) {
         st.p_row = static_cast<int>(out0 + n);
         st.p_max = s_lp_m[n];
         st.p_corr = __fdiv_rn(1.0f, ff_to_f(s_lp_s[n]));
+        st.p_tau = s_tp[n];
+        st.q_tau = -INFINITY;
         if (mode == kModeResidual) {
           st.q_row = b * K + n;
           st.q_max = s_lq_m[n];
           st.q_corr = __fdiv_rn(1.0f, ff_to_f(s_lq_s[n]));
+          st.q_tau = s_tq[n];
         } else if (mode == kModeResidualPoint) {
           st.q_row = s_x[n];  // the token whose entry the residual drops
         }
@@ -628,9 +615,12 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailParams P) 
     // rescaling whenever the running maximum grows.  A point-mass draft
     // row has no partials: it is published as M = 0, S = 1.
     const bool neutral = qrow && P.q_logits == nullptr;
+    // a truncated row's (M, S) were published by the truncation kernel
+    const bool given = !P.greedy && (qrow ? P.q_cut : P.p_cut);
     float m = -INFINITY, acc = 0.0f;
     int bad = 0;
-    for (int s0 = threadIdx.x; s0 < P.dims.nsub && !neutral; s0 += kTailThreads * 8) {
+    for (int s0 = threadIdx.x; s0 < P.dims.nsub && !neutral && !given;
+         s0 += kTailThreads * 8) {
       float2 pm[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -661,6 +651,10 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailParams P) 
     if (neutral) {
       M = 0.0f;
       S = ff_make(1.0f);
+    }
+    if (given) {
+      M = __ldcg(&P.w.row_m[t]);
+      S = ld_ff(&P.w.row_s[t]);
     }
     if (bad) M = NAN;
     if (P.greedy && !bad) {
