@@ -10,7 +10,9 @@ K=4, T=1) on synthetic inputs, through the C ABI.
 
 ``--drafts ngram`` times the prompt-lookup variant instead: each step runs
 the GPU n-gram drafter over a synthetic 4096-token context and verifies its
-drafts as point masses (no draft logits are streamed).
+drafts as point masses (no draft logits are streamed).  ``--top-k`` and
+``--top-p`` time truncated sampling (the same settings for target and
+draft), which adds the per-row cut kernel to each step.
 
 Prints one JSON line (rank 0).  Metric: verify rounds/s; ``roofline`` is
 the LM-head contraction kernel's algorithmic bytes over its CUDA-event
@@ -306,10 +308,12 @@ def reference_arm(args, wl, dev):
                     "d2h_bytes_per_step": 0}}
 
 
-def workload_config(wl, extra=None, drafts="model"):
+def workload_config(wl, extra=None, drafts="model", top_k=0, top_p=1.0):
     what = (f"draft acceptance ~{wl.alpha}" if drafts == "model" else
             f"prompt-lookup drafts (n-gram 5..2) over a {CTX_TOKENS}-token synthetic context, "
             "verified as point masses")
+    if top_k or top_p < 1.0:
+        what += f", truncated sampling top-k {top_k} top-p {top_p} on both sides"
     cfg = {"workload": f"Llama-3.1-8B-shaped LM-head verify round, V={wl.V}, d={wl.d}, "
                        f"B={wl.B}, K={wl.K}, T={wl.T}, {what}",
            "V": wl.V, "d": wl.d, "B": wl.B, "K": wl.K, "T": wl.T,
@@ -331,6 +335,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--drafts", default="model", choices=["model", "ngram"])
+    ap.add_argument("--top-k", type=int, default=0)
+    ap.add_argument("--top-p", type=float, default=1.0)
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--clock-log", default=None)
@@ -388,10 +394,17 @@ def main():
         if ngram:
             sv.spec_ngram_draft(s["ctx"], s["lens"], wl.K, 2, 5, s["draft"], s["dlen"],
                                 stream=torch.cuda.current_stream())
-        sv.spec_verify_run(eng.h, s["hidden"], W, s["draft"], s["q_logits"],
-                           s["uniforms"], T, out_tok[i], out_n[i])
+        if truncated:
+            sv.spec_verify_run_truncated(eng.h, s["hidden"], W, s["draft"], s["q_logits"],
+                                         s["uniforms"], T, args.top_k, args.top_p, args.top_k,
+                                         args.top_p, out_tok[i], out_n[i])
+        else:
+            sv.spec_verify_run(eng.h, s["hidden"], W, s["draft"], s["q_logits"],
+                               s["uniforms"], T, out_tok[i], out_n[i])
 
-    launches_per_run = sv.spec_verify_launches_per_run(eng.h, T) + (1 if ngram else 0)
+    truncated = T > 0 and (0 < args.top_k < wl.V or args.top_p < 1.0)
+    launches_per_run = (sv.spec_verify_launches_per_run(eng.h, T) + (1 if ngram else 0)
+                        + (1 if truncated else 0))
     # warm-up (also the first use of every input set)
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, nsets)):
@@ -488,16 +501,30 @@ def main():
     pin = [{k: sets[i][k].cpu().pin_memory() for k in keys} for i in range(min(nsets, 8))]
     ht = torch.empty((wl.B, wl.K + 1), dtype=torch.int32).pin_memory()
     hn = torch.empty((wl.B,), dtype=torch.int32).pin_memory()
-    if ngram:
+    if ngram or truncated:
         dbuf = {k: torch.empty_like(sets[0][k]) for k in keys}
-        dbuf.update(draft=torch.empty_like(sets[0]["draft"]),
-                    dlen=torch.empty_like(sets[0]["dlen"]))
+        if ngram:
+            dbuf.update(draft=torch.empty_like(sets[0]["draft"]),
+                        dlen=torch.empty_like(sets[0]["dlen"]))
         dtok, dn = out_tok[0], out_n[0]
 
     def e2e_step(p):
-        if not ngram:
+        if not ngram and not truncated:
             sv.spec_verify_run_host(eng.h, p["hidden"], W, p["draft"], p["q_logits"],
                                     p["uniforms"], T, ht, hn)
+            return
+        if not ngram:
+            # truncated sampling: the host buffers copied in, the step, the
+            # outputs copied back (through the public entry points)
+            with torch.cuda.stream(stream):
+                for k in keys:
+                    dbuf[k].copy_(p[k], non_blocking=True)
+                sv.spec_verify_run_truncated(eng.h, dbuf["hidden"], W, dbuf["draft"],
+                                             dbuf["q_logits"], dbuf["uniforms"], T, args.top_k,
+                                             args.top_p, args.top_k, args.top_p, dtok, dn)
+                ht.copy_(dtok, non_blocking=True)
+                hn.copy_(dn, non_blocking=True)
+            stream.synchronize()
             return
         with torch.cuda.stream(stream):
             for k in keys:
@@ -540,7 +567,7 @@ def main():
                       f"{nsets} rotating input sets ({nsets * set_bytes} B)",
                 "graph": graph is not None,
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
-                drafts=args.drafts),
+                drafts=args.drafts, top_k=args.top_k, top_p=args.top_p),
             "emitted_tokens_per_round": tokens_per_round,
             "emitted_tokens_per_s": value * tokens_per_round,
             "roofline": roofline,
