@@ -83,6 +83,9 @@ def _load():
                                                        vp, vp, dbl, i32, dbl, i32, dbl, dbl,
                                                        dbl, vp, vp, vp, vp, vp]
             lib.sv_oracle_verify_truncated.restype = ctypes.c_int
+            lib.sv_oracle_tree_greedy.argtypes = [i64, i64, i32, i32, i32, vp, vp, vp, vp, vp,
+                                                  vp, vp, vp]
+            lib.sv_oracle_tree_greedy.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -292,3 +295,29 @@ def verify_truncated(hidden, W, draft, q_logits, uniforms, temperature: float,
         raise ValueError(f"sv_oracle_verify_truncated failed ({rc})")
     return {"tokens": tokens, "n_accepted": n_acc, "dist": dist, "trunc_sens": sens,
             "trunc_xgap": xgap, "status": rc}
+
+
+def tree_greedy(hidden, W, tokens, parents) -> dict:
+    """Greedy tree verification (reading R12 in sv_oracle.c): hidden
+    [B, N+1, d], W [V, d] (uint16 bf16 bits or float32), tokens / parents
+    [B, N] int32 (parents in [-1, j)).  Returns tokens [B, N+1], nodes
+    [B, N] (the accepted path's node indices), n [B] and gap [B]."""
+    hidden, dt = _matrix(hidden)
+    W, dt2 = _matrix(W)
+    if dt != dt2:
+        raise TypeError("hidden and W must share a dtype")
+    B, rows, d = hidden.shape
+    N = rows - 1
+    V = W.shape[0]
+    tokens = _c(tokens, np.int32).reshape(B, N)
+    parents = _c(parents, np.int32).reshape(B, N)
+    out_t = np.empty((B, rows), dtype=np.int32)
+    out_nodes = np.empty((B, max(N, 1)), dtype=np.int32)
+    out_n = np.empty((B,), dtype=np.int32)
+    gap = np.empty((B,), dtype=np.float64)
+    rc = _load().sv_oracle_tree_greedy(V, d, B, N, dt, _ptr(hidden), _ptr(W), _ptr(tokens),
+                                       _ptr(parents), _ptr(out_t), _ptr(out_nodes),
+                                       _ptr(out_n), _ptr(gap))
+    if rc not in (OK, ETOKEN):
+        raise ValueError(f"sv_oracle_tree_greedy failed ({rc})")
+    return {"tokens": out_t, "nodes": out_nodes[:, :N], "n": out_n, "gap": gap, "status": rc}

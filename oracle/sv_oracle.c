@@ -73,6 +73,17 @@
  *       or above the k-th largest x (ties at the boundary kept), top-p
  *       every x at or above the value of the first token, in descending
  *       order, at which the cumulative mass reaches top_p.
+ *   R12 Greedy tree verification ([P3] "Tree attention": several branches
+ *       verified in one pass; the summary's "accepting the longest matching
+ *       path"; greedy only, as the pages give no sampled multi-branch rule).
+ *       Node j (0..N-1) holds a token and a parent in [-1, j) (-1: the
+ *       root, the last committed position); hidden row 0 scores the root's
+ *       continuation and row 1 + j that of node j.  A node matches when its
+ *       parent matches (the root always does) and its token is the argmax
+ *       of its parent's row (ties to the smallest id, R6).  The round emits
+ *       the tokens on the path to the deepest matched node (the smallest
+ *       index among equally deep ones), then the argmax of that node's row;
+ *       with no match it emits the argmax of row 0.
  */
 #include <math.h>
 #include <stdint.h>
@@ -723,5 +734,98 @@ int sv_oracle_verify_truncated(int64_t V, int64_t d, int32_t B, int32_t K, int32
     if (trunc_xgap) trunc_xgap[b] = xgap;
   }
   free(L); free(p); free(q); free(x); free(scratch); free(ud); free(keep); free(order);
+  return status;
+}
+
+/* ------------------------------------------------------------------------
+ * Greedy tree verification (R12) for B sequences of N draft nodes:
+ *   hidden  [B, N+1, d] (bf16 bits or fp32), W [V, d]
+ *   tokens  [B, N] node tokens, parents [B, N] node parents (-1: root)
+ * Outputs: out_tokens [B, N+1] (path tokens, then the final argmax, then
+ * -1), out_nodes [B, N] (the path's node indices, then -1; may be NULL),
+ * out_n [B] (path length; -1 for an invalid tree), gap [B] (may be NULL):
+ * the smallest top-1 minus top-2 logit gap over the rows whose argmax
+ * decided something (every row whose children were compared, and the row
+ * of the final token).
+ * ---------------------------------------------------------------------- */
+int sv_oracle_tree_greedy(int64_t V, int64_t d, int32_t B, int32_t N, int32_t dtype,
+                          const void *hidden, const void *W, const int32_t *tokens,
+                          const int32_t *parents, int32_t *out_tokens, int32_t *out_nodes,
+                          int32_t *out_n, double *gap) {
+  if (V < 1 || d < 1 || B < 1 || N < 0 || (dtype != 0 && dtype != 1) || !hidden || !W ||
+      (N > 0 && (!tokens || !parents)) || !out_tokens || !out_n)
+    return SV_ORACLE_EARG;
+  const int64_t rows = (int64_t)N + 1;
+  const size_t esz = dtype == 0 ? 2 : 4;
+  double *L = (double *)malloc(sizeof(double) * (size_t)(rows * V));
+  int64_t *arg = (int64_t *)malloc(sizeof(int64_t) * (size_t)rows);
+  double *g = (double *)malloc(sizeof(double) * (size_t)rows);
+  unsigned char *matched = (unsigned char *)malloc((size_t)rows);
+  int32_t *depth = (int32_t *)malloc(sizeof(int32_t) * (size_t)rows);
+  if (!L || !arg || !g || !matched || !depth) {
+    free(L); free(arg); free(g); free(matched); free(depth);
+    return SV_ORACLE_ENOMEM;
+  }
+  int status = SV_ORACLE_OK;
+  for (int32_t b = 0; b < B; ++b) {
+    int32_t *tb = out_tokens + (int64_t)b * rows;
+    int32_t *nb = out_nodes ? out_nodes + (int64_t)b * N : NULL;
+    for (int64_t i = 0; i < rows; ++i) tb[i] = -1;
+    for (int64_t i = 0; i < N && nb; ++i) nb[i] = -1;
+    const int32_t *tk = N > 0 ? tokens + (int64_t)b * N : NULL;
+    const int32_t *pa = N > 0 ? parents + (int64_t)b * N : NULL;
+    int valid = 1;
+    for (int32_t j = 0; j < N; ++j)
+      if (tk[j] < 0 || (int64_t)tk[j] >= V || pa[j] < -1 || pa[j] >= j) valid = 0;
+    if (!valid) {
+      status = SV_ORACLE_ETOKEN;
+      out_n[b] = -1;
+      if (gap) gap[b] = INFINITY;
+      continue;
+    }
+    const char *hb = (const char *)hidden + (size_t)b * (size_t)(rows * d) * esz;
+    int rc = sv_oracle_logits(V, d, rows, dtype, hb, W, 0, V, L);
+    if (rc != SV_ORACLE_OK) { status = rc; break; }
+    for (int64_t i = 0; i < rows; ++i) {
+      const double *row = L + i * V;
+      int64_t a = 0;
+      for (int64_t v = 1; v < V; ++v)
+        if (row[v] > row[a]) a = v; /* ties keep the smaller id */
+      double second = -INFINITY;
+      for (int64_t v = 0; v < V; ++v)
+        if (v != a && row[v] > second) second = row[v];
+      arg[i] = a;
+      g[i] = row[a] - second;
+    }
+    /* matched[0] is the root; matched[1 + j] node j */
+    matched[0] = 1;
+    depth[0] = 0;
+    int64_t best = 0; /* row of the deepest matched node (0: the root) */
+    double gmin = INFINITY;
+    for (int32_t j = 0; j < N; ++j) {
+      const int64_t pr = (int64_t)pa[j] + 1; /* parent's row */
+      depth[1 + j] = depth[pr] + 1;
+      matched[1 + j] = 0;
+      if (matched[pr]) {
+        if (g[pr] < gmin) gmin = g[pr];
+        matched[1 + j] = (int64_t)tk[j] == arg[pr];
+      }
+      if (matched[1 + j] && depth[1 + j] > depth[best]) best = 1 + j;
+    }
+    if (g[best] < gmin) gmin = g[best];
+    /* the path to `best`, root first */
+    const int32_t n = depth[best];
+    int64_t r = best;
+    for (int32_t i = n - 1; i >= 0; --i) {
+      const int32_t node = (int32_t)(r - 1);
+      tb[i] = tk[node];
+      if (nb) nb[i] = node;
+      r = (int64_t)pa[node] + 1;
+    }
+    tb[n] = (int32_t)arg[best];
+    out_n[b] = n;
+    if (gap) gap[b] = gmin;
+  }
+  free(L); free(arg); free(g); free(matched); free(depth);
   return status;
 }
