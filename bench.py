@@ -12,7 +12,9 @@ K=4, T=1) on synthetic inputs, through the C ABI.
 the GPU n-gram drafter over a synthetic 4096-token context and verifies its
 drafts as point masses (no draft logits are streamed).  ``--top-k`` and
 ``--top-p`` time truncated sampling (the same settings for target and
-draft), which adds the per-row cut kernel to each step.
+draft), which adds the per-row cut kernel to each step.  ``--tree`` times
+greedy tree verification of a Medusa-like tree (3 levels of 3 branches, 39
+nodes) at the same shape.
 
 Prints one JSON line (rank 0).  Metric: verify rounds/s; ``roofline`` is
 the LM-head contraction kernel's algorithmic bytes over its CUDA-event
@@ -308,10 +310,26 @@ def reference_arm(args, wl, dev):
                     "d2h_bytes_per_step": 0}}
 
 
-def workload_config(wl, extra=None, drafts="model", top_k=0, top_p=1.0):
+def medusa_tree(levels=3, branches=3):
+    """Parents of a full tree, level by level (each node's parent precedes it)."""
+    par, level = [], [-1]
+    for _ in range(levels):
+        nxt = []
+        for p in level:
+            for _ in range(branches):
+                par.append(p)
+                nxt.append(len(par) - 1)
+        level = nxt
+    return par
+
+
+def workload_config(wl, extra=None, drafts="model", top_k=0, top_p=1.0, tree=False):
     what = (f"draft acceptance ~{wl.alpha}" if drafts == "model" else
             f"prompt-lookup drafts (n-gram 5..2) over a {CTX_TOKENS}-token synthetic context, "
             "verified as point masses")
+    if tree:
+        what = (f"greedy tree verification of a 3x3x3 tree ({wl.K} nodes; first child of "
+                "each node follows the target's choice)")
     if top_k or top_p < 1.0:
         what += f", truncated sampling top-k {top_k} top-p {top_p} on both sides"
     cfg = {"workload": f"Llama-3.1-8B-shaped LM-head verify round, V={wl.V}, d={wl.d}, "
@@ -337,6 +355,7 @@ def main():
     ap.add_argument("--drafts", default="model", choices=["model", "ngram"])
     ap.add_argument("--top-k", type=int, default=0)
     ap.add_argument("--top-p", type=float, default=1.0)
+    ap.add_argument("--tree", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--clock-log", default=None)
@@ -356,6 +375,9 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     wl = si.workload(args.workload)
+    if args.tree:
+        tree_par = medusa_tree()
+        wl = si.workload(args.workload, K=len(tree_par), T=0.0)
 
     if args.impl == "reference":
         if rank == 0:
@@ -374,6 +396,19 @@ def main():
                  + 4 * wl.B * (wl.K + 1))
     nsets = n_input_sets(set_bytes)
     sets = [si.make_round(wl, W, seed=10_000 + 1000 * rank + i) for i in range(nsets)]
+    if args.tree:
+        par_t = torch.tensor(tree_par, dtype=torch.int32, device=dev).repeat(wl.B, 1)
+        for s in sets:
+            # node tokens: the first child of each node follows the target's
+            # choice (plain torch matmul, input shaping only), others random
+            L = (s["hidden"].float() @ W.float().T)
+            arg = L.argmax(dim=-1)
+            tok = s["draft"].clone()
+            for j, pj in enumerate(tree_par):
+                if j % 3 == 0:
+                    tok[:, j] = arg[:, pj + 1].to(torch.int32)
+            s["draft"], s["parents"] = tok.contiguous(), par_t.contiguous()
+            s["nodes"] = torch.empty((wl.B, wl.K), dtype=torch.int32, device=dev)
     if ngram:
         for i, s in enumerate(sets):
             s["q_logits"] = None
@@ -394,7 +429,10 @@ def main():
         if ngram:
             sv.spec_ngram_draft(s["ctx"], s["lens"], wl.K, 2, 5, s["draft"], s["dlen"],
                                 stream=torch.cuda.current_stream())
-        if truncated:
+        if args.tree:
+            sv.spec_verify_tree_greedy(eng.h, s["hidden"], W, s["draft"], s["parents"],
+                                       out_tok[i], s["nodes"], out_n[i])
+        elif truncated:
             sv.spec_verify_run_truncated(eng.h, s["hidden"], W, s["draft"], s["q_logits"],
                                          s["uniforms"], T, args.top_k, args.top_p, args.top_k,
                                          args.top_p, out_tok[i], out_n[i])
@@ -478,7 +516,7 @@ def main():
     sv.spec_verify_timing(eng.h, False)
     k1_s = ms_k1 / 1e3 / n_k1
     peaks, peak_src = measured_peaks()
-    k1_bytes = contraction_bytes(wl.V, wl.d, wl.B, wl.K, point_mass=ngram)
+    k1_bytes = contraction_bytes(wl.V, wl.d, wl.B, wl.K, greedy=T == 0, point_mass=ngram)
     achieved = k1_bytes / k1_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
@@ -488,7 +526,7 @@ def main():
                 "kernel_us": k1_s * 1e6, "algorithmic_bytes_per_launch": k1_bytes,
                 "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
                 "step_frac_of_measured": algorithmic_bytes(
-                    wl.V, wl.d, wl.B, wl.K, point_mass=ngram,
+                    wl.V, wl.d, wl.B, wl.K, greedy=T == 0, point_mass=ngram,
                     ctx_tokens=CTX_TOKENS if ngram else 0)
                 * value / world / 1e9 / peaks["hbm_gbs"]}
 
@@ -501,7 +539,10 @@ def main():
     pin = [{k: sets[i][k].cpu().pin_memory() for k in keys} for i in range(min(nsets, 8))]
     ht = torch.empty((wl.B, wl.K + 1), dtype=torch.int32).pin_memory()
     hn = torch.empty((wl.B,), dtype=torch.int32).pin_memory()
-    if ngram or truncated:
+    if args.tree:
+        keys = ("hidden", "draft", "parents")
+        pin = [{k: sets[i][k].cpu().pin_memory() for k in keys} for i in range(min(nsets, 8))]
+    if ngram or truncated or args.tree:
         dbuf = {k: torch.empty_like(sets[0][k]) for k in keys}
         if ngram:
             dbuf.update(draft=torch.empty_like(sets[0]["draft"]),
@@ -509,6 +550,16 @@ def main():
         dtok, dn = out_tok[0], out_n[0]
 
     def e2e_step(p):
+        if args.tree:
+            with torch.cuda.stream(stream):
+                for k in keys:
+                    dbuf[k].copy_(p[k], non_blocking=True)
+                sv.spec_verify_tree_greedy(eng.h, dbuf["hidden"], W, dbuf["draft"],
+                                           dbuf["parents"], dtok, sets[0]["nodes"], dn)
+                ht.copy_(dtok, non_blocking=True)
+                hn.copy_(dn, non_blocking=True)
+            stream.synchronize()
+            return
         if not ngram and not truncated:
             sv.spec_verify_run_host(eng.h, p["hidden"], W, p["draft"], p["q_logits"],
                                     p["uniforms"], T, ht, hn)
@@ -567,7 +618,7 @@ def main():
                       f"{nsets} rotating input sets ({nsets * set_bytes} B)",
                 "graph": graph is not None,
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
-                drafts=args.drafts, top_k=args.top_k, top_p=args.top_p),
+                drafts=args.drafts, top_k=args.top_k, top_p=args.top_p, tree=args.tree),
             "emitted_tokens_per_round": tokens_per_round,
             "emitted_tokens_per_s": value * tokens_per_round,
             "roofline": roofline,

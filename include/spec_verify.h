@@ -69,7 +69,7 @@ extern "C" {
 #define SV_FP32 1 /* reference-precision path for small vocabularies         */
 
 /* Limits checked at create time. */
-#define SV_MAX_K 16      /* draft tokens per sequence                        */
+#define SV_MAX_K 64      /* draft tokens (tree nodes) per sequence           */
 #define SV_MAX_B 4096    /* sequences per call                               */
 #define SV_MAX_ROWS_BF16 384 /* B * (K+1) for the bf16 path                  */
 
@@ -237,6 +237,33 @@ int spec_verify_run_truncated(spec_verify_t *h, const void *hidden, const void *
                               const float *uniforms, float temperature, int32_t target_top_k,
                               float target_top_p, int32_t draft_top_k, float draft_top_p,
                               int32_t *out_tokens, int32_t *out_n_accepted);
+
+/* Greedy tree verification ("Speculative Decoding: Guess Several Tokens,
+ * Check Them in One Pass", "Tree attention": several draft branches verified
+ * in one pass, the longest matching path accepted).  The handle's K is the
+ * number of tree nodes N; hidden is [B, N+1, d] with row 0 scoring the
+ * continuation of the last committed token (the root) and row 1 + j that of
+ * node j (the tree-attention forward pass produces exactly these rows).
+ *   tree_tokens    device, int32 [B, N]: node j's token, in [0, V)
+ *   tree_parents   device, int32 [B, N]: node j's parent in [-1, j) (-1: the
+ *                  root), so parents come before their children
+ * A node matches when its parent matches (the root always does) and its
+ * token is the argmax of its parent's row (ties to the smallest id).  The
+ * round emits the tokens on the path to the deepest matched node (the
+ * smallest index among equally deep ones), then the argmax of that node's
+ * row; with no match, the argmax of row 0.  (The tie rule is this library's
+ * reading.)
+ *   out_tokens     device, int32 [B, N+1]: the path's tokens, the final
+ *                  argmax, then -1
+ *   out_nodes      device, int32 [B, N] or NULL: the path's node indices
+ *                  (root first; for KV rollback), then -1
+ *   out_n          device, int32 [B]: the path length; -1 for a sequence
+ *                  with an invalid token or parent (status SV_ERR_TOKEN) or
+ *                  non-finite logits
+ * Errors: as spec_verify_run. */
+int spec_verify_tree_greedy(spec_verify_t *h, const void *hidden, const void *W_lm,
+                            const int32_t *tree_tokens, const int32_t *tree_parents,
+                            int32_t *out_tokens, int32_t *out_nodes, int32_t *out_n);
 
 /* ---------------------------------------------------------------------------
  * Prompt-lookup drafting ("Speculative Decoding: Guess Several Tokens, Check

@@ -28,7 +28,7 @@ SV_ERR_TOKEN = -7
 SV_ERR_NONFINITE = -8
 SV_BF16 = 0
 SV_FP32 = 1
-SV_MAX_K = 16
+SV_MAX_K = 64
 SV_MAX_B = 4096
 SV_MAX_ROWS_BF16 = 384
 SV_NGRAM_MAX = 16
@@ -40,7 +40,8 @@ EXPORTS = ("spec_verify_create", "spec_verify_run", "spec_verify_run_host",
            "spec_verify_set_wait_limit", "spec_verify_timing",
            "spec_verify_timing_read", "spec_verify_launches_per_run",
            "spec_verify_strerror", "spec_verify_destroy",
-           "spec_verify_run_noalloc", "spec_ngram_draft", "spec_verify_run_truncated")
+           "spec_verify_run_noalloc", "spec_ngram_draft", "spec_verify_run_truncated",
+           "spec_verify_tree_greedy")
 
 
 class SpecVerifyError(RuntimeError):
@@ -91,6 +92,7 @@ def load_library():
         i32 = ctypes.c_int32
         lib.spec_verify_run_truncated.argtypes = [vp, vp, vp, vp, vp, vp, f32, i32, f32, i32,
                                                   f32, vp, vp]
+        lib.spec_verify_tree_greedy.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         lib.spec_ngram_draft.argtypes = [vp, ctypes.c_int64, vp, i32, i32, i32, i32, vp, vp,
                                          vp]
         for name in EXPORTS:
@@ -225,6 +227,15 @@ def spec_verify_run_truncated(h, hidden, W_lm, draft_tokens, q_logits, uniforms,
         "spec_verify_run_truncated")
 
 
+def spec_verify_tree_greedy(h, hidden, W_lm, tree_tokens, tree_parents, out_tokens,
+                            out_nodes, out_n) -> None:
+    """Greedy tree verification: the longest path whose tokens are the
+    target's argmax choices (N = the handle's K nodes)."""
+    _check(load_library().spec_verify_tree_greedy(
+        h, _ptr(hidden), _ptr(W_lm), _ptr(tree_tokens), _ptr(tree_parents), _ptr(out_tokens),
+        _ptr(out_nodes), _ptr(out_n)), "spec_verify_tree_greedy")
+
+
 def spec_ngram_draft(tokens, lengths, K: int, n_min: int = 2, n_max: int = 5,
                      out_draft=None, out_len=None, stream=None):
     """Prompt-lookup drafts for B contexts (tokens [B, L] int32 on the GPU,
@@ -280,6 +291,15 @@ class SpecVerify:
                                   temperature, target_top_k, target_top_p, draft_top_k,
                                   draft_top_p, out_tokens, out_n_accepted)
         return out_tokens, out_n_accepted
+
+    def run_tree_greedy(self, hidden, W_lm, tree_tokens, tree_parents):
+        """Returns (tokens [B, N+1], nodes [B, N], n [B])."""
+        out_t = torch.empty((self.B, self.K + 1), dtype=torch.int32, device=self.device)
+        out_nodes = torch.empty((self.B, max(self.K, 1)), dtype=torch.int32, device=self.device)
+        out_n = torch.empty((self.B,), dtype=torch.int32, device=self.device)
+        spec_verify_tree_greedy(self.h, hidden, W_lm, tree_tokens, tree_parents, out_t,
+                                out_nodes, out_n)
+        return out_t, out_nodes[:, :self.K], out_n
 
     def status(self) -> int:
         return spec_verify_status(self.h)

@@ -261,11 +261,14 @@ int spec_verify_launches_per_run(spec_verify_t *h, float temperature) {
 
 namespace {
 
-// Truncated sampling settings of one run (which rows are cut, and how).
+// Variants of one run: truncated sampling (which rows are cut, and how) and
+// greedy tree verification.
 struct TruncSpec {
   int p_cut = 0, q_cut = 0;
   int p_top_k = 0, q_top_k = 0;
   float p_top_p = 1.0f, q_top_p = 1.0f;
+  const int32_t *parents = nullptr;
+  int32_t *out_nodes = nullptr;
 };
 
 int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
@@ -303,6 +306,19 @@ int spec_verify_run_truncated(spec_verify_t *h, const void *hidden, const void *
              ((draft_top_k > 0 && draft_top_k < D.V) || draft_top_p < 1.0f);
   return run_impl(h, hidden, W_lm, draft_tokens, q_logits, uniforms, temperature, out_tokens,
                   out_n_accepted, tr);
+}
+
+int spec_verify_tree_greedy(spec_verify_t *h, const void *hidden, const void *W_lm,
+                            const int32_t *tree_tokens, const int32_t *tree_parents,
+                            int32_t *out_tokens, int32_t *out_nodes, int32_t *out_n) {
+  if (!h) return SV_ERR_ARG;
+  if (h->dims.K > 0 && (!tree_tokens || !tree_parents)) return SV_ERR_ARG;
+  if ((tree_parents && !aligned16(tree_parents)) || (out_nodes && !aligned16(out_nodes)))
+    return SV_ERR_ALIGN;
+  TruncSpec tr;
+  tr.parents = h->dims.K > 0 ? tree_parents : nullptr;
+  tr.out_nodes = out_nodes;
+  return run_impl(h, hidden, W_lm, tree_tokens, nullptr, nullptr, 0.0f, out_tokens, out_n, tr);
 }
 
 namespace {
@@ -406,6 +422,8 @@ int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
   T.draft_logits_ready = h->cfg.dtype == SV_BF16 ? 1 : 0;
   T.p_cut = tr.p_cut;
   T.q_cut = tr.q_cut;
+  T.parents = tr.parents;
+  T.out_nodes = tr.out_nodes;
   if (tr.p_cut || tr.q_cut) {
     sv::TruncParams TP{};
     TP.dims = D;

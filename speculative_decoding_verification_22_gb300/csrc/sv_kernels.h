@@ -72,6 +72,8 @@ struct TailParams {
   int split_cnt_n;         // entries of w.split_cnt
   int draft_logits_ready;  // w.draft_logit was written by the contraction
   int p_cut, q_cut;        // truncated target / draft rows: (M, S, cut) are given
+  const int32_t *parents;  // greedy tree verification: [B, K] node parents (else null)
+  int32_t *out_nodes;      // tree: [B, K] accepted path's nodes (may be null)
 };
 cudaError_t launch_tail(const TailParams &P, cudaStream_t stream);
 

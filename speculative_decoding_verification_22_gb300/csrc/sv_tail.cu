@@ -301,8 +301,12 @@ __device__ int decide(const TailParams &P, int b) {
   __shared__ float s_tp[SV_MAX_K + 1], s_tq[SV_MAX_K], s_lbuf[SV_MAX_K];  // cuts, L[x]
   __shared__ int s_err, s_fin, s_kb;
   // no draft distribution: the draft was proposed with certainty (q is a
-  // point mass at each proposed token) and a -1 ends it early
-  const bool point = P.q_logits == nullptr;
+  // point mass at each proposed token) and a -1 ends it early (not for a
+  // tree, whose nodes all carry tokens)
+  const bool point = P.q_logits == nullptr && P.parents == nullptr;
+  __shared__ int s_par[SV_MAX_K];               // tree: node parents
+  __shared__ int s_depth[SV_MAX_K + 1];         // tree: depth of root / nodes
+  __shared__ unsigned char s_match[SV_MAX_K + 1];
 
   if (threadIdx.x == 0) s_err = 0;
   __syncthreads();
@@ -321,6 +325,12 @@ __device__ int decide(const TailParams &P, int b) {
     const int i = threadIdx.x - 32;
     const int x = P.draft[static_cast<int64_t>(b) * K + i];
     s_x[i] = x;
+    if (P.parents) {
+      // a parent must come before its child
+      const int pa = P.parents[static_cast<int64_t>(b) * K + i];
+      s_par[i] = pa;
+      if (pa < -1 || pa >= i) atomicExch(&s_err, SV_ERR_TOKEN);
+    }
     if (point && x == -1) {
       // end of a short draft (checked below)
     } else if (x < 0 || static_cast<int64_t>(x) >= V) {
@@ -434,6 +444,31 @@ __device__ int decide(const TailParams &P, int b) {
       for (int i = 0; i <= kb; ++i) ok = ok && s_arg[i] >= 0;
       if (!ok) {
         err = SV_ERR_NONFINITE;
+      } else if (P.parents) {
+        // greedy tree verification: one pass over the nodes (parents come
+        // first); row 0 is the root, row 1 + j node j
+        s_depth[0] = 0;
+        s_match[0] = 1;
+        int best = 0;
+        for (int j = 0; j < K; ++j) {
+          const int pr = s_par[j] + 1;
+          s_depth[1 + j] = s_depth[pr] + 1;
+          s_match[1 + j] = (s_match[pr] && s_x[j] == s_arg[pr]) ? 1 : 0;
+          if (s_match[1 + j] && s_depth[1 + j] > s_depth[best]) best = 1 + j;
+        }
+        const int n = s_depth[best];
+        int r = best;
+        for (int i = n - 1; i >= 0; --i) {
+          const int node = r - 1;
+          P.out_tokens[out0 + i] = s_x[node];
+          if (P.out_nodes) P.out_nodes[static_cast<int64_t>(b) * K + i] = node;
+          r = s_par[node] + 1;
+        }
+        P.out_tokens[out0 + n] = s_arg[best];
+        for (int i = n + 1; i < rows; ++i) P.out_tokens[out0 + i] = -1;
+        if (P.out_nodes)
+          for (int i = n; i < K; ++i) P.out_nodes[static_cast<int64_t>(b) * K + i] = -1;
+        P.out_n[b] = n;
       } else {
         int n = kb;
         for (int i = 0; i < kb; ++i) {
@@ -454,6 +489,8 @@ __device__ int decide(const TailParams &P, int b) {
       if (err != SV_ERR_TIMEOUT) set_status(P.w.status, err);
       st.mode = kModeSkip;
       for (int i = 0; i < rows; ++i) P.out_tokens[out0 + i] = -1;
+      if (P.out_nodes)
+        for (int i = 0; i < K; ++i) P.out_nodes[static_cast<int64_t>(b) * K + i] = -1;
       P.out_n[b] = -1;
     }
     P.w.seq[b] = st;

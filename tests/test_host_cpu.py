@@ -49,7 +49,7 @@ def test_strerror_covers_every_code(lib):
     (dict(V=0, d=4096, B=1, K=4, dtype=0), sv.SV_ERR_SHAPE),
     (dict(V=128256, d=4095, B=1, K=4, dtype=0), sv.SV_ERR_SHAPE),   # d % 8
     (dict(V=128256, d=4096, B=0, K=4, dtype=0), sv.SV_ERR_SHAPE),
-    (dict(V=128256, d=4096, B=1, K=17, dtype=0), sv.SV_ERR_SHAPE),  # K > 16
+    (dict(V=128256, d=4096, B=1, K=65, dtype=0), sv.SV_ERR_SHAPE),  # K > 64
     (dict(V=128256, d=4096, B=65, K=5, dtype=0), sv.SV_ERR_SHAPE),  # 390 rows
     (dict(V=1000, d=256, B=1, K=4, dtype=7), sv.SV_ERR_ARG),
     (dict(V=1000, d=6, B=1, K=4, dtype=1), sv.SV_ERR_SHAPE),        # d % 4
@@ -139,7 +139,7 @@ def test_ngram_draft_rejects_bad_arguments_before_cuda(lib):
     assert f(good, 8, good, 0, 4, 2, 5, good, good, None) == sv.SV_ERR_ARG    # B
     assert f(good, 0, good, 1, 4, 2, 5, good, good, None) == sv.SV_ERR_ARG    # ld
     assert f(good, 8, good, 1, 0, 2, 5, good, good, None) == sv.SV_ERR_ARG    # K
-    assert f(good, 8, good, 1, 17, 2, 5, good, good, None) == sv.SV_ERR_ARG   # K > 16
+    assert f(good, 8, good, 1, 65, 2, 5, good, good, None) == sv.SV_ERR_ARG   # K > 64
     assert f(good, 8, good, 1, 4, 0, 5, good, good, None) == sv.SV_ERR_ARG    # n_min
     assert f(good, 8, good, 1, 4, 3, 2, good, good, None) == sv.SV_ERR_ARG    # n_max < n_min
     assert f(good, 8, good, 1, 4, 2, 17, good, good, None) == sv.SV_ERR_ARG   # n_max > 16
