@@ -60,6 +60,17 @@ template <int NCOL>
 constexpr int drain_slots() {
   return NCOL == 0 ? 1 : (512 / NCOL < SV_TC_DRAIN_SLOTS ? 512 / NCOL : SV_TC_DRAIN_SLOTS);
 }
+// 64-wide k blocks accumulated into one drain slot.  At 64 columns TMEM
+// holds only 8 slots; two blocks per slot halve the drain's TMEM reads per
+// block and let the MMA run 16 blocks ahead of a draining tile end (the
+// tensor cores then sum 8 MMAs of K=16 before each round-to-nearest add).
+#ifndef SV_TC_KPS64
+#define SV_TC_KPS64 4
+#endif
+template <int NCOL>
+constexpr int kblocks_per_slot() {
+  return NCOL == 64 ? SV_TC_KPS64 : 1;
+}
 constexpr uint64_t kCleanupLimitNs = 2000000000ull;
 
 struct Ctl {
@@ -280,8 +291,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t adesc = 0, bdesc = 0;
       int j = 0;  // chunk within the current stage (kb0 is a multiple of C)
       for (int kb = kb0; kb < kb1; ++kb) {
+        // drain mode: groups of kblocks_per_slot k blocks share a slot
+        const int gpos = (kb - kb0) % kblocks_per_slot<NCOL>();
+        const bool group_first = gpos == 0;
+        const bool group_last = gpos == kblocks_per_slot<NCOL>() - 1 || kb == kb1 - 1;
         if constexpr (NCOL != 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->tempty[slot]), tphase ^ 1u,
+          if (group_first &&
+              !__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->tempty[slot]), tphase ^ 1u,
                                                  P.wait_limit_ns, abort))) {
             if (lane == 0) raise_abort(ctl, P);
             ok = false;
@@ -305,14 +321,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (elect_one()) {
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-              umma_bf16(d, adesc + 2u * k, bdesc + 2u * k, idesc, k > 0 ? 1u : 0u);
+              umma_bf16(d, adesc + 2u * k, bdesc + 2u * k, idesc,
+                        (k > 0 || !group_first) ? 1u : 0u);
             // release the stage first: the producer's refill is on the
             // critical path, the drain of this slot is not
             if (j == C - 1) umma_commit(smem_u32(&ctl->empty[stage]));
-            umma_commit(smem_u32(&ctl->tfull[slot]));
+            if (group_last) umma_commit(smem_u32(&ctl->tfull[slot]));
           }
           __syncwarp();
-          if (++slot == drain_slots<NCOL>()) {
+          if (group_last && ++slot == drain_slots<NCOL>()) {
             slot = 0;
             tphase ^= 1u;
           }
@@ -415,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int n = 0; n < NCOL; ++n) acc[n] = 0.0f;
         bool ok = true;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; kb += kblocks_per_slot<NCOL>()) {
           if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->tfull[slot]), tphase,
                                                  P.wait_limit_ns, abort))) {
             if (lane == 0) raise_abort(ctl, P);
