@@ -86,6 +86,11 @@ def _load():
             lib.sv_oracle_tree_greedy.argtypes = [i64, i64, i32, i32, i32, vp, vp, vp, vp, vp,
                                                   vp, vp, vp]
             lib.sv_oracle_tree_greedy.restype = ctypes.c_int
+            lib.sv_oracle_verify_fp8.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, vp,
+                                                 vp, dbl, vp, vp, vp, vp, vp, vp]
+            lib.sv_oracle_verify_fp8.restype = ctypes.c_int
+            lib.sv_oracle_e4m3_decode.argtypes = [i64, vp, vp]
+            lib.sv_oracle_e4m3_decode.restype = None
             _lib = lib
     return _lib
 
@@ -321,3 +326,43 @@ def tree_greedy(hidden, W, tokens, parents) -> dict:
     if rc not in (OK, ETOKEN):
         raise ValueError(f"sv_oracle_tree_greedy failed ({rc})")
     return {"tokens": out_t, "nodes": out_nodes[:, :N], "n": out_n, "gap": gap, "status": rc}
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """FP8 E4M3 bytes to float64 (reading R13 in sv_oracle.c)."""
+    codes = _c(codes, np.uint8)
+    out = np.empty(codes.shape, dtype=np.float64)
+    _load().sv_oracle_e4m3_decode(codes.size, _ptr(codes), _ptr(out))
+    return out
+
+
+def verify_fp8(hidden8, hscale, W8, wscale, draft, q_logits, uniforms, temperature: float,
+               want_logits: bool = False) -> dict:
+    """The verify step with an FP8 LM head (R13): hidden8 [B, K+1, d] and
+    W8 [V, d] E4M3 bytes (uint8), hscale [B, K+1] and wscale [V] float32.
+    Other arguments and the result as verify()."""
+    hidden8 = _c(hidden8, np.uint8)
+    W8 = _c(W8, np.uint8)
+    B, rows, d = hidden8.shape
+    K = rows - 1
+    V = W8.shape[0]
+    hscale = _c(hscale, np.float32).reshape(B * rows)
+    wscale = _c(wscale, np.float32).reshape(V)
+    draft = _c(draft, np.int32).reshape(B, K)
+    T = float(temperature)
+    q = None if (K == 0 or q_logits is None) else _c(q_logits, np.float32).reshape(B, K, V)
+    u = None if T == 0.0 else _c(uniforms, np.float32).reshape(B, rows)
+    tokens = np.empty((B, rows), dtype=np.int32)
+    n_acc = np.empty((B,), dtype=np.int32)
+    dist = np.empty((B,), dtype=np.float64)
+    lg = np.empty((B * rows, V), dtype=np.float64) if want_logits else None
+    lse_p = np.full((B * rows,), np.nan)
+    lse_q = np.full((max(B * K, 1),), np.nan)
+    rc = _load().sv_oracle_verify_fp8(V, d, B, K, _ptr(hidden8), _ptr(hscale), _ptr(W8),
+                                      _ptr(wscale), _ptr(draft), _ptr(q), _ptr(u), T,
+                                      _ptr(tokens), _ptr(n_acc), _ptr(dist), _ptr(lg),
+                                      _ptr(lse_p), _ptr(lse_q))
+    if rc not in (OK, ETOKEN):
+        raise ValueError(f"sv_oracle_verify_fp8 failed ({rc})")
+    return {"tokens": tokens, "n_accepted": n_acc, "dist": dist, "logits": lg,
+            "lse_p": lse_p, "lse_q": lse_q[:B * K], "status": rc}

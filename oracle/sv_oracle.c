@@ -84,6 +84,13 @@
  *       the tokens on the path to the deepest matched node (the smallest
  *       index among equally deep ones), then the argmax of that node's row;
  *       with no match it emits the argmax of row 0.
+ *   R13 FP8 LM head ([P4] "Where it breaks": native FP8 doubles both the
+ *       arithmetic intensity and the peak).  Weights and hidden states
+ *       arrive as FP8 E4M3 values (sign, 4-bit exponent of bias 7, 3-bit
+ *       mantissa, subnormals, one NaN code, no infinities; largest finite
+ *       448) with one fp32 scale per vocabulary row and per hidden row; the
+ *       logit is hs[r] * ws[v] * sum_k H8[r][k] * W8[v][k].  The method then
+ *       runs unchanged on these logits.
  */
 #include <math.h>
 #include <stdint.h>
@@ -103,11 +110,27 @@ static double bf16_bits_to_double(uint16_t bits) {
   return (double)f;
 }
 
-/* Widen row `row` of a [rows, d] matrix stored as bf16 (dtype 0) or fp32
- * (dtype 1) into `out` (d doubles).  Both widenings are exact. */
+/* An FP8 E4M3 value (R13): sign bit, 4 exponent bits (bias 7), 3 mantissa
+ * bits; exponent 0 holds the subnormals m * 2^-9; exponent 15 with mantissa
+ * 7 is NaN (there are no infinities). */
+static double e4m3_to_double(uint8_t b) {
+  const int s = b >> 7, e = (b >> 3) & 0xF, m = b & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m, -9);
+  else v = ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* Widen row `row` of a [rows, d] matrix stored as bf16 (dtype 0), fp32
+ * (dtype 1) or FP8 E4M3 (dtype 2) into `out` (d doubles).  All widenings
+ * are exact. */
 static void widen_row(const void *base, int dtype, int64_t d, int64_t row,
                       double *out) {
-  if (dtype == 0) {
+  if (dtype == 2) {
+    const uint8_t *p = (const uint8_t *)base + row * d;
+    for (int64_t k = 0; k < d; ++k) out[k] = e4m3_to_double(p[k]);
+  } else if (dtype == 0) {
     const uint16_t *p = (const uint16_t *)base + row * d;
     for (int64_t k = 0; k < d; ++k) out[k] = bf16_bits_to_double(p[k]);
   } else {
@@ -128,7 +151,7 @@ static void widen_row(const void *base, int dtype, int64_t d, int64_t row,
 int sv_oracle_logits(int64_t V, int64_t d, int64_t R, int32_t dtype,
                      const void *H, const void *W, int64_t v0, int64_t v1,
                      double *L) {
-  if (V < 1 || d < 1 || R < 1 || (dtype != 0 && dtype != 1) || !H || !W ||
+  if (V < 1 || d < 1 || R < 1 || dtype < 0 || dtype > 2 || !H || !W ||
       !L || v0 < 0 || v1 > V || v0 > v1)
     return SV_ORACLE_EARG;
   double *h = (double *)malloc(sizeof(double) * (size_t)(R * d));
@@ -357,19 +380,48 @@ static int32_t greedy_one_sequence(int64_t V, int32_t K, const double *L,
  * sequence held an out-of-range draft token (that sequence's outputs are
  * -1 and the others are still computed).
  * ---------------------------------------------------------------------- */
+static int verify_impl(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
+                       const void *hidden, const float *hscale, const void *W,
+                       const float *wscale, const int32_t *draft, const float *q_logits,
+                       const float *u, double T, int32_t *out_tokens, int32_t *out_n,
+                       double *dist, double *logits, double *lse_p, double *lse_q);
+
 int sv_oracle_verify(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
                      const void *hidden, const void *W, const int32_t *draft,
                      const float *q_logits, const float *u, double T,
                      int32_t *out_tokens, int32_t *out_n, double *dist,
                      double *logits, double *lse_p, double *lse_q) {
-  if (V < 1 || d < 1 || B < 1 || K < 0 || (dtype != 0 && dtype != 1) ||
+  if (dtype != 0 && dtype != 1) return SV_ORACLE_EARG;
+  return verify_impl(V, d, B, K, dtype, hidden, NULL, W, NULL, draft, q_logits, u, T,
+                     out_tokens, out_n, dist, logits, lse_p, lse_q);
+}
+
+/* The step with an FP8 LM head (R13): hidden8 [B, K+1, d] and W8 [V, d]
+ * are E4M3 bytes, hscale [B*(K+1)] and wscale [V] their fp32 scales; other
+ * arguments as sv_oracle_verify. */
+int sv_oracle_verify_fp8(int64_t V, int64_t d, int32_t B, int32_t K, const void *hidden8,
+                         const float *hscale, const void *W8, const float *wscale,
+                         const int32_t *draft, const float *q_logits, const float *u,
+                         double T, int32_t *out_tokens, int32_t *out_n, double *dist,
+                         double *logits, double *lse_p, double *lse_q) {
+  if (!hscale || !wscale) return SV_ORACLE_EARG;
+  return verify_impl(V, d, B, K, 2, hidden8, hscale, W8, wscale, draft, q_logits, u, T,
+                     out_tokens, out_n, dist, logits, lse_p, lse_q);
+}
+
+static int verify_impl(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
+                       const void *hidden, const float *hscale, const void *W,
+                       const float *wscale, const int32_t *draft, const float *q_logits,
+                       const float *u, double T, int32_t *out_tokens, int32_t *out_n,
+                       double *dist, double *logits, double *lse_p, double *lse_q) {
+  if (V < 1 || d < 1 || B < 1 || K < 0 || dtype < 0 || dtype > 2 ||
       !hidden || !W || !out_tokens || !out_n || !(T >= 0.0) || T == INFINITY)
     return SV_ORACLE_EARG;
   if (K > 0 && !draft) return SV_ORACLE_EARG;
   if (T > 0.0 && !u) return SV_ORACLE_EARG;
   const int point_mass = q_logits == NULL; /* R8, R9 */
   const int64_t rows = (int64_t)K + 1;
-  const size_t esz = dtype == 0 ? 2 : 4;
+  const size_t esz = dtype == 0 ? 2 : dtype == 1 ? 4 : 1;
   double *L = (double *)malloc(sizeof(double) * (size_t)(rows * V));
   double *p = (double *)malloc(sizeof(double) * (size_t)(rows * V));
   double *q = (double *)malloc(sizeof(double) * (size_t)((K > 0 ? K : 1) * V));
@@ -385,6 +437,11 @@ int sv_oracle_verify(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
     const char *hb = (const char *)hidden + (size_t)b * (size_t)(rows * d) * esz;
     int rc = sv_oracle_logits(V, d, rows, dtype, hb, W, 0, V, L);
     if (rc != SV_ORACLE_OK) { status = rc; break; }
+    if (hscale) /* R13: the row and vocabulary scales */
+      for (int64_t i = 0; i < rows; ++i) {
+        const double hs = (double)hscale[(int64_t)b * rows + i];
+        for (int64_t v = 0; v < V; ++v) L[i * V + v] *= hs * (double)wscale[v];
+      }
     if (logits)
       memcpy(logits + (size_t)b * (size_t)(rows * V), L,
              sizeof(double) * (size_t)(rows * V));
@@ -828,4 +885,9 @@ int sv_oracle_tree_greedy(int64_t V, int64_t d, int32_t B, int32_t N, int32_t dt
   }
   free(L); free(arg); free(g); free(matched); free(depth);
   return status;
+}
+
+/* Decodes n FP8 E4M3 bytes (R13) into doubles; for the pins. */
+void sv_oracle_e4m3_decode(int64_t n, const uint8_t *in, double *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_to_double(in[i]);
 }

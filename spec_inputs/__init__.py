@@ -171,3 +171,41 @@ def to_oracle(t: torch.Tensor):
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view("uint16")
     return t.numpy()
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 inputs (input shaping for the FP8 LM head)
+# ---------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def quantize_rows_e4m3(x: torch.Tensor):
+    """Per-row FP8 E4M3 quantisation: scale = max|x| / 448 per row (fp32),
+    codes = x / scale converted by torch's float8_e4m3fn (round to nearest
+    even).  Returns (codes as uint8 [..., d], scales fp32 [...])."""
+    xf = x.float()
+    scale = (xf.abs().amax(dim=-1).clamp_min(1e-30) / E4M3_MAX).float()
+    q = (xf / scale.unsqueeze(-1)).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).contiguous(), scale.contiguous()
+
+
+def dequantize_e4m3(codes: torch.Tensor, scale: torch.Tensor) -> torch.Tensor:
+    return codes.view(torch.float8_e4m3fn).float() * scale.unsqueeze(-1)
+
+
+def make_fp8_weights(wl: Workload, seed: int, device="cpu"):
+    """The bf16-shaped weights of the workload, quantised per vocabulary row:
+    (W8 uint8 [V, d], w_scale fp32 [V])."""
+    W = make_weights(wl, seed=seed, device=device)
+    return quantize_rows_e4m3(W)
+
+
+def make_fp8_round(wl: Workload, W8: torch.Tensor, w_scale: torch.Tensor, seed: int,
+                   T: float | None = None) -> dict:
+    """make_round on the dequantised weights, with the hidden states
+    quantised per row: adds hidden8 [B, K+1, d] uint8 and h_scale [B, K+1]."""
+    Wd = dequantize_e4m3(W8, w_scale)
+    r = make_round(wl, Wd, seed, T=T)
+    h8, hs = quantize_rows_e4m3(r["hidden"])
+    r["hidden8"], r["h_scale"] = h8, hs
+    return r
