@@ -14,7 +14,8 @@ drafts as point masses (no draft logits are streamed).  ``--top-k`` and
 ``--top-p`` time truncated sampling (the same settings for target and
 draft), which adds the per-row cut kernel to each step.  ``--tree`` times
 greedy tree verification of a Medusa-like tree (3 levels of 3 branches, 39
-nodes) at the same shape.
+nodes) at the same shape.  ``--fp8`` times the step with an FP8 E4M3 LM head
+(weights and hidden states quantised per row, fp32 scales).
 
 Prints one JSON line (rank 0).  Metric: verify rounds/s; ``roofline`` is
 the LM-head contraction kernel's algorithmic bytes over its CUDA-event
@@ -70,9 +71,10 @@ def algorithmic_bytes(V, d, B, K, greedy=False, elt=2, point_mass=False, ctx_tok
 def contraction_bytes(V, d, B, K, greedy=False, elt=2, point_mass=False):
     """Algorithmic bytes of the contraction kernel alone: W_lm, hidden and
     (sampling with draft logits) the draft logits it streams for the softmax
-    partials."""
+    partials; with 1-byte (FP8) elements also the fp32 row scales."""
     q = 0 if (greedy or point_mass) else 4 * B * K * V
-    return elt * V * d + elt * B * (K + 1) * d + q
+    scales = 4 * V + 4 * B * (K + 1) if elt == 1 else 0
+    return elt * V * d + elt * B * (K + 1) * d + q + scales
 
 
 CTX_TOKENS = 4096
@@ -230,7 +232,7 @@ class ClockSampler:
 # oracle timing (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_rate(wl, W_np, inputs, budget_s):
+def oracle_rate(wl, W_np, inputs, budget_s, w_scale=None):
     """Times the CPU oracle (one thread) on this workload.  Full rounds while
     they fit the budget; otherwise a vocabulary slice of the contraction,
     which is >99.9% of an oracle round at this shape, scaled to a round."""
@@ -244,11 +246,19 @@ def oracle_rate(wl, W_np, inputs, budget_s):
     round_est = per_row * wl.V
     if round_est <= budget_s / 2:
         q = inputs.get("q_logits")
-        args = (si.to_oracle(inputs["hidden"]), W_np, si.to_oracle(inputs["draft"]),
-                None if q is None else si.to_oracle(q), si.to_oracle(inputs["uniforms"]), wl.T)
+        qa = None if q is None else si.to_oracle(q)
+        if w_scale is not None:   # FP8 LM head
+            fn = oracle.verify_fp8
+            args = (si.to_oracle(inputs["hidden8"]), si.to_oracle(inputs["h_scale"]), W_np,
+                    si.to_oracle(w_scale), si.to_oracle(inputs["draft"]), qa,
+                    si.to_oracle(inputs["uniforms"]), wl.T)
+        else:
+            fn = oracle.verify
+            args = (si.to_oracle(inputs["hidden"]), W_np, si.to_oracle(inputs["draft"]), qa,
+                    si.to_oracle(inputs["uniforms"]), wl.T)
         n, t0 = 0, time.perf_counter()
         while True:
-            oracle.verify(*args)
+            fn(*args)
             n += 1
             el = time.perf_counter() - t0
             if el >= budget_s / 2 or n >= 1000:
@@ -323,7 +333,8 @@ def medusa_tree(levels=3, branches=3):
     return par
 
 
-def workload_config(wl, extra=None, drafts="model", top_k=0, top_p=1.0, tree=False):
+def workload_config(wl, extra=None, drafts="model", top_k=0, top_p=1.0, tree=False,
+                    fp8=False):
     what = (f"draft acceptance ~{wl.alpha}" if drafts == "model" else
             f"prompt-lookup drafts (n-gram 5..2) over a {CTX_TOKENS}-token synthetic context, "
             "verified as point masses")
@@ -332,6 +343,8 @@ def workload_config(wl, extra=None, drafts="model", top_k=0, top_p=1.0, tree=Fal
                 "each node follows the target's choice)")
     if top_k or top_p < 1.0:
         what += f", truncated sampling top-k {top_k} top-p {top_p} on both sides"
+    if fp8:
+        what += ", FP8 E4M3 LM head and hidden states (fp32 row scales)"
     cfg = {"workload": f"Llama-3.1-8B-shaped LM-head verify round, V={wl.V}, d={wl.d}, "
                        f"B={wl.B}, K={wl.K}, T={wl.T}, {what}",
            "V": wl.V, "d": wl.d, "B": wl.B, "K": wl.K, "T": wl.T,
@@ -356,6 +369,7 @@ def main():
     ap.add_argument("--top-k", type=int, default=0)
     ap.add_argument("--top-p", type=float, default=1.0)
     ap.add_argument("--tree", action="store_true")
+    ap.add_argument("--fp8", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--clock-log", default=None)
@@ -390,12 +404,23 @@ def main():
 
     T = wl.T
     ngram = args.drafts == "ngram"
-    W = si.make_weights(wl, seed=1 + 1000 * rank, device=dev)
+    fp8 = args.fp8
+    if fp8:
+        W8, w_scale = si.make_fp8_weights(wl, seed=1 + 1000 * rank, device=dev)
+        W = W8
+    else:
+        W = si.make_weights(wl, seed=1 + 1000 * rank, device=dev)
     set_bytes = (2 * wl.B * (wl.K + 1) * wl.d + 4 * wl.B * wl.K
                  + (4 * wl.B * CTX_TOKENS if ngram else 4 * wl.B * wl.K * wl.V)
                  + 4 * wl.B * (wl.K + 1))
     nsets = n_input_sets(set_bytes)
-    sets = [si.make_round(wl, W, seed=10_000 + 1000 * rank + i) for i in range(nsets)]
+    if fp8:
+        sets = [si.make_fp8_round(wl, W8, w_scale, seed=10_000 + 1000 * rank + i)
+                for i in range(nsets)]
+        for s in sets:
+            s["hidden"] = s["hidden8"]
+    else:
+        sets = [si.make_round(wl, W, seed=10_000 + 1000 * rank + i) for i in range(nsets)]
     if args.tree:
         par_t = torch.tensor(tree_par, dtype=torch.int32, device=dev).repeat(wl.B, 1)
         for s in sets:
@@ -415,7 +440,7 @@ def main():
             s["ctx"], s["lens"] = make_contexts(wl.B, wl.V, 20_000 + 1000 * rank + i, dev)
             s["draft"] = torch.empty((wl.B, wl.K), dtype=torch.int32, device=dev)
             s["dlen"] = torch.empty((wl.B,), dtype=torch.int32, device=dev)
-    eng = sv.SpecVerify(wl.V, wl.d, wl.B, wl.K, "bf16", device=dev)
+    eng = sv.SpecVerify(wl.V, wl.d, wl.B, wl.K, "fp8" if fp8 else "bf16", device=dev)
     stream = torch.cuda.Stream(device=dev)
     sv.spec_verify_set_stream(eng.h, stream)
     # one (16-byte aligned) output pair per input set
@@ -429,7 +454,10 @@ def main():
         if ngram:
             sv.spec_ngram_draft(s["ctx"], s["lens"], wl.K, 2, 5, s["draft"], s["dlen"],
                                 stream=torch.cuda.current_stream())
-        if args.tree:
+        if fp8:
+            sv.spec_verify_run_fp8(eng.h, s["hidden8"], s["h_scale"], W8, w_scale, s["draft"],
+                                   s["q_logits"], s["uniforms"], T, out_tok[i], out_n[i])
+        elif args.tree:
             sv.spec_verify_tree_greedy(eng.h, s["hidden"], W, s["draft"], s["parents"],
                                        out_tok[i], s["nodes"], out_n[i])
         elif truncated:
@@ -516,8 +544,15 @@ def main():
     sv.spec_verify_timing(eng.h, False)
     k1_s = ms_k1 / 1e3 / n_k1
     peaks, peak_src = measured_peaks()
-    k1_bytes = contraction_bytes(wl.V, wl.d, wl.B, wl.K, greedy=T == 0, point_mass=ngram)
+    k1_bytes = contraction_bytes(wl.V, wl.d, wl.B, wl.K, greedy=T == 0, point_mass=ngram,
+                                 elt=1 if fp8 else 2)
     achieved = k1_bytes / k1_s / 1e9
+    # the whole round's algorithmic bytes (FP8: 1-byte elements plus the
+    # fp32 row scales)
+    step_bytes = algorithmic_bytes(wl.V, wl.d, wl.B, wl.K, greedy=T == 0, point_mass=ngram,
+                                   elt=1 if fp8 else 2, ctx_tokens=CTX_TOKENS if ngram else 0)
+    if fp8:
+        step_bytes += 4 * wl.V + 4 * wl.B * (wl.K + 1)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "traffic": recorded_traffic(),
@@ -525,10 +560,7 @@ def main():
                 "kernel": "lmhead_tc_kernel (LM-head contraction + softmax partials)",
                 "kernel_us": k1_s * 1e6, "algorithmic_bytes_per_launch": k1_bytes,
                 "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
-                "step_frac_of_measured": algorithmic_bytes(
-                    wl.V, wl.d, wl.B, wl.K, greedy=T == 0, point_mass=ngram,
-                    ctx_tokens=CTX_TOKENS if ngram else 0)
-                * value / world / 1e9 / peaks["hbm_gbs"]}
+                "step_frac_of_measured": step_bytes * value / world / 1e9 / peaks["hbm_gbs"]}
 
     # end to end through the host-buffer entry point (prompt lookup: the
     # context, hidden states and uniforms copied in from pinned memory, the
@@ -542,7 +574,10 @@ def main():
     if args.tree:
         keys = ("hidden", "draft", "parents")
         pin = [{k: sets[i][k].cpu().pin_memory() for k in keys} for i in range(min(nsets, 8))]
-    if ngram or truncated or args.tree:
+    if fp8:
+        keys = ("hidden8", "h_scale", "draft", "q_logits", "uniforms")
+        pin = [{k: sets[i][k].cpu().pin_memory() for k in keys} for i in range(min(nsets, 8))]
+    if ngram or truncated or args.tree or fp8:
         dbuf = {k: torch.empty_like(sets[0][k]) for k in keys}
         if ngram:
             dbuf.update(draft=torch.empty_like(sets[0]["draft"]),
@@ -550,6 +585,17 @@ def main():
         dtok, dn = out_tok[0], out_n[0]
 
     def e2e_step(p):
+        if fp8:
+            with torch.cuda.stream(stream):
+                for k in keys:
+                    dbuf[k].copy_(p[k], non_blocking=True)
+                sv.spec_verify_run_fp8(eng.h, dbuf["hidden8"], dbuf["h_scale"], W8, w_scale,
+                                       dbuf["draft"], dbuf["q_logits"], dbuf["uniforms"], T,
+                                       dtok, dn)
+                ht.copy_(dtok, non_blocking=True)
+                hn.copy_(dn, non_blocking=True)
+            stream.synchronize()
+            return
         if args.tree:
             with torch.cuda.stream(stream):
                 for k in keys:
@@ -603,7 +649,8 @@ def main():
     cpu = None
     if rank == 0:
         W_np = si.to_oracle(W)
-        rate, sample, _ = oracle_rate(wl, W_np, sets[0], args.cpu_budget)
+        rate, sample, _ = oracle_rate(wl, W_np, sets[0], args.cpu_budget,
+                                      w_scale=w_scale if fp8 else None)
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
 
     if rank == 0:
@@ -618,7 +665,8 @@ def main():
                       f"{nsets} rotating input sets ({nsets * set_bytes} B)",
                 "graph": graph is not None,
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
-                drafts=args.drafts, top_k=args.top_k, top_p=args.top_p, tree=args.tree),
+                drafts=args.drafts, top_k=args.top_k, top_p=args.top_p, tree=args.tree,
+                fp8=fp8),
             "emitted_tokens_per_round": tokens_per_round,
             "emitted_tokens_per_s": value * tokens_per_round,
             "roofline": roofline,

@@ -66,7 +66,9 @@ extern "C" {
 
 /* Element type of hidden and W_lm. */
 #define SV_BF16 0 /* production path: TMA + tcgen05 tensor-core contraction   */
-#define SV_FP32 1 /* reference-precision path for small vocabularies         */
+#define SV_FP32 1
+#define SV_FP8 2         /* FP8 E4M3 hidden and W_lm with fp32 row scales:
+                          * run through spec_verify_run_fp8                  */ /* reference-precision path for small vocabularies         */
 
 /* Limits checked at create time. */
 #define SV_MAX_K 64      /* draft tokens (tree nodes) per sequence           */
@@ -237,6 +239,28 @@ int spec_verify_run_truncated(spec_verify_t *h, const void *hidden, const void *
                               const float *uniforms, float temperature, int32_t target_top_k,
                               float target_top_p, int32_t draft_top_k, float draft_top_p,
                               int32_t *out_tokens, int32_t *out_n_accepted);
+
+/* The step with an FP8 LM head, on a handle created with dtype SV_FP8
+ * ("Speculative Decoding: The Algebra and the Proof", "Where it breaks":
+ * native FP8 doubles both the arithmetic intensity and the peak, and halves
+ * the bytes of the weight stream).  Values are FP8 E4M3 (sign, 4-bit
+ * exponent of bias 7, 3-bit mantissa; largest finite 448) with one fp32
+ * scale per hidden row and per vocabulary row:
+ *   hidden8        device, E4M3 bytes [B, K+1, d] (d a multiple of 16)
+ *   hidden_scale   device, fp32 [B, K+1]
+ *   W8             device, E4M3 bytes [V, d]
+ *   w_scale        device, fp32 [V]
+ * The logit of row r and token v is hidden_scale[r] * w_scale[v] *
+ * sum_k hidden8[r][k] * W8[v][k]; the contraction runs on the FP8 tensor
+ * cores (tcgen05 kind::f8f6f4) with fp32 accumulation, and everything after
+ * it is the same step on those logits.  Other arguments, outputs and errors
+ * as spec_verify_run; SV_ERR_ARG if the handle is not SV_FP8 or a scale
+ * pointer is NULL.  (spec_verify_run, spec_verify_run_host and the variants
+ * return SV_ERR_ARG on an SV_FP8 handle: they carry no scales.) */
+int spec_verify_run_fp8(spec_verify_t *h, const void *hidden8, const float *hidden_scale,
+                        const void *W8, const float *w_scale, const int32_t *draft_tokens,
+                        const float *q_logits, const float *uniforms, float temperature,
+                        int32_t *out_tokens, int32_t *out_n_accepted);
 
 /* Greedy tree verification ("Speculative Decoding: Guess Several Tokens,
  * Check Them in One Pass", "Tree attention": several draft branches verified

@@ -104,14 +104,17 @@ def _c(a, dtype):
 
 
 def _matrix(a):
-    """bf16 matrices travel as their uint16 bit patterns (dtype code 0);
-    fp32 as float32 (code 1)."""
+    """bf16 matrices travel as their uint16 bit patterns (dtype code 0),
+    fp32 as float32 (code 1), FP8 E4M3 as uint8 codes (code 2; logits()
+    then returns the unscaled sums, see verify_fp8 for the scaled step)."""
     a = np.ascontiguousarray(a)
     if a.dtype == np.uint16:
         return a, 0
     if a.dtype == np.float32:
         return a, 1
-    raise TypeError("matrices must be uint16 (bf16 bits) or float32")
+    if a.dtype == np.uint8:
+        return a, 2
+    raise TypeError("matrices must be uint16 (bf16 bits), float32 or uint8 (E4M3)")
 
 
 def logits(H, W, v0: int = 0, v1: int | None = None) -> np.ndarray:

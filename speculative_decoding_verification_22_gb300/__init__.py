@@ -28,6 +28,7 @@ SV_ERR_TOKEN = -7
 SV_ERR_NONFINITE = -8
 SV_BF16 = 0
 SV_FP32 = 1
+SV_FP8 = 2
 SV_MAX_K = 64
 SV_MAX_B = 4096
 SV_MAX_ROWS_BF16 = 384
@@ -41,7 +42,7 @@ EXPORTS = ("spec_verify_create", "spec_verify_run", "spec_verify_run_host",
            "spec_verify_timing_read", "spec_verify_launches_per_run",
            "spec_verify_strerror", "spec_verify_destroy",
            "spec_verify_run_noalloc", "spec_ngram_draft", "spec_verify_run_truncated",
-           "spec_verify_tree_greedy")
+           "spec_verify_tree_greedy", "spec_verify_run_fp8")
 
 
 class SpecVerifyError(RuntimeError):
@@ -93,6 +94,7 @@ def load_library():
         lib.spec_verify_run_truncated.argtypes = [vp, vp, vp, vp, vp, vp, f32, i32, f32, i32,
                                                   f32, vp, vp]
         lib.spec_verify_tree_greedy.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.spec_verify_run_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp]
         lib.spec_ngram_draft.argtypes = [vp, ctypes.c_int64, vp, i32, i32, i32, i32, vp, vp,
                                          vp]
         for name in EXPORTS:
@@ -129,7 +131,7 @@ def spec_verify_strerror(code: int) -> str:
 
 def spec_verify_create(V: int, d: int, B: int, K: int, dtype="bf16", stream=None):
     """Creates a handle; ``dtype`` is "bf16"/"fp32" (or SV_BF16/SV_FP32)."""
-    code = {"bf16": SV_BF16, "fp32": SV_FP32}.get(dtype, dtype)
+    code = {"bf16": SV_BF16, "fp32": SV_FP32, "fp8": SV_FP8}.get(dtype, dtype)
     cfg = sv_config_t(int(V), int(d), int(B), int(K), int(code),
                       _stream_handle(stream))
     h = ctypes.c_void_p()
@@ -207,7 +209,7 @@ def spec_verify_run_noalloc(V, d, B, K, dtype, hidden, W_lm, draft_tokens, q_log
     """The step without a handle or any allocation (scratch in a fixed
     device array inside the library); for callers that cannot allocate
     device memory at call time.  Calls that overlap on the GPU race."""
-    code = {"bf16": SV_BF16, "fp32": SV_FP32}.get(dtype, dtype)
+    code = {"bf16": SV_BF16, "fp32": SV_FP32, "fp8": SV_FP8}.get(dtype, dtype)
     cfg = sv_config_t(int(V), int(d), int(B), int(K), int(code), _stream_handle(stream))
     _check(load_library().spec_verify_run_noalloc(
         ctypes.byref(cfg), _ptr(hidden), _ptr(W_lm), _ptr(draft_tokens), _ptr(q_logits),
@@ -225,6 +227,15 @@ def spec_verify_run_truncated(h, hidden, W_lm, draft_tokens, q_logits, uniforms,
         float(temperature), int(target_top_k), float(target_top_p), int(draft_top_k),
         float(draft_top_p), _ptr(out_tokens), _ptr(out_n_accepted)),
         "spec_verify_run_truncated")
+
+
+def spec_verify_run_fp8(h, hidden8, hidden_scale, W8, w_scale, draft_tokens, q_logits,
+                        uniforms, temperature: float, out_tokens, out_n_accepted) -> None:
+    """The step with an FP8 E4M3 LM head (handle dtype "fp8")."""
+    _check(load_library().spec_verify_run_fp8(
+        h, _ptr(hidden8), _ptr(hidden_scale), _ptr(W8), _ptr(w_scale), _ptr(draft_tokens),
+        _ptr(q_logits), _ptr(uniforms), float(temperature), _ptr(out_tokens),
+        _ptr(out_n_accepted)), "spec_verify_run_fp8")
 
 
 def spec_verify_tree_greedy(h, hidden, W_lm, tree_tokens, tree_parents, out_tokens,
@@ -290,6 +301,17 @@ class SpecVerify:
         spec_verify_run_truncated(self.h, hidden, W_lm, draft_tokens, q_logits, uniforms,
                                   temperature, target_top_k, target_top_p, draft_top_k,
                                   draft_top_p, out_tokens, out_n_accepted)
+        return out_tokens, out_n_accepted
+
+    def run_fp8(self, hidden8, hidden_scale, W8, w_scale, draft_tokens, q_logits, uniforms,
+                temperature, out_tokens=None, out_n_accepted=None):
+        if out_tokens is None:
+            out_tokens = torch.empty((self.B, self.K + 1), dtype=torch.int32,
+                                     device=self.device)
+        if out_n_accepted is None:
+            out_n_accepted = torch.empty((self.B,), dtype=torch.int32, device=self.device)
+        spec_verify_run_fp8(self.h, hidden8, hidden_scale, W8, w_scale, draft_tokens, q_logits,
+                            uniforms, temperature, out_tokens, out_n_accepted)
         return out_tokens, out_n_accepted
 
     def run_tree_greedy(self, hidden, W_lm, tree_tokens, tree_parents):

@@ -63,7 +63,7 @@ struct spec_verify {
 
 namespace {
 
-size_t esize(int dtype) { return dtype == SV_BF16 ? 2 : 4; }
+size_t esize(int dtype) { return dtype == SV_BF16 ? 2 : dtype == SV_FP8 ? 1 : 4; }
 
 void free_all(spec_verify *h) {
   void *ptrs[] = {h->w.logits,    h->w.part_p,      h->w.part_q,    h->w.row_m,
@@ -86,30 +86,36 @@ bool dalloc(T **p, size_t count) {
   return cudaMalloc(reinterpret_cast<void **>(p), count * sizeof(T)) == cudaSuccess;
 }
 
-// TMA map of a bf16 [outer, inner] row-major matrix.  chunks == 1: 2-D,
-// box {64, box_rows}.  chunks > 1: 3-D view {64, outer, inner / 64} (the
-// k-chunk dimension has a 128-byte stride), box {64, box_rows, chunks}, so
-// one copy brings `chunks` consecutive 64-wide k blocks of box_rows rows.
+// TMA map of a row-major [outer, inner] matrix of bf16 (elt 2) or FP8 E4M3
+// bytes (elt 1).  A block is one 128-byte row piece: kbk = 128 / elt
+// elements.  chunks == 1: 2-D, box {kbk, box_rows}.  chunks > 1: 3-D view
+// {kbk, outer, inner / kbk} (the k-chunk dimension has a 128-byte stride),
+// box {kbk, box_rows, chunks}, so one copy brings `chunks` consecutive k
+// blocks of box_rows rows.
 int encode_w(CUtensorMap *map, const void *base, int64_t inner, int64_t outer,
-             uint32_t box_rows, int chunks) {
+             uint32_t box_rows, int chunks, int elt = 2) {
   auto fn = encode_fn();
   if (!fn) return SV_ERR_CUDA;
+  const CUtensorMapDataType type =
+      elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const cuuint32_t kbk = static_cast<cuuint32_t>(128 / elt);
   CUresult r;
   if (chunks > 1) {
-    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(outer), static_cast<cuuint64_t>(inner / 64)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2, 128};
-    cuuint32_t box[3] = {64, box_rows, static_cast<cuuint32_t>(chunks)};
+    cuuint64_t dims[3] = {kbk, static_cast<cuuint64_t>(outer),
+                          static_cast<cuuint64_t>(inner / kbk)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * elt, 128};
+    cuuint32_t box[3] = {kbk, box_rows, static_cast<cuuint32_t>(chunks)};
     cuuint32_t estr[3] = {1, 1, 1};
-    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    r = fn(map, type, 3, const_cast<void *>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
-    cuuint32_t box[2] = {64, box_rows};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * elt};
+    cuuint32_t box[2] = {kbk, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    r = fn(map, type, 2, const_cast<void *>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   }
   return r == CUDA_SUCCESS ? SV_OK : SV_ERR_CUDA;
@@ -148,13 +154,15 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
   if (!out) return SV_ERR_ARG;
   *out = nullptr;
   if (!cfg) return SV_ERR_ARG;
-  if (cfg->dtype != SV_BF16 && cfg->dtype != SV_FP32) return SV_ERR_ARG;
+  if (cfg->dtype != SV_BF16 && cfg->dtype != SV_FP32 && cfg->dtype != SV_FP8) return SV_ERR_ARG;
   if (cfg->V < 1 || cfg->V > INT32_MAX || cfg->d < 1 || cfg->d > (1 << 20) || cfg->B < 1 ||
       cfg->B > SV_MAX_B || cfg->K < 0 || cfg->K > SV_MAX_K)
     return SV_ERR_SHAPE;
-  if (cfg->d % (cfg->dtype == SV_BF16 ? 8 : 4) != 0) return SV_ERR_SHAPE;
+  // rows of 16-byte multiples (TMA and 16-byte loads)
+  if (cfg->d % (cfg->dtype == SV_BF16 ? 8 : cfg->dtype == SV_FP8 ? 16 : 4) != 0)
+    return SV_ERR_SHAPE;
   const int64_t R = static_cast<int64_t>(cfg->B) * (cfg->K + 1);
-  if (cfg->dtype == SV_BF16 && R > SV_MAX_ROWS_BF16) return SV_ERR_SHAPE;
+  if (cfg->dtype != SV_FP32 && R > SV_MAX_ROWS_BF16) return SV_ERR_SHAPE;
   if (R * cfg->V > (int64_t(1) << 40)) return SV_ERR_SHAPE;
 
   int dev = 0;
@@ -183,8 +191,8 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
   D.nchunk = static_cast<int>((cfg->V + sv::kChunk - 1) / sv::kChunk);
 
   size_t split_floats = 1;
-  if (cfg->dtype == SV_BF16) {
-    h->plan = sv::plan_tc(D, h->num_sms, h->smem_optin);
+  if (cfg->dtype != SV_FP32) {
+    h->plan = sv::plan_tc(D, h->num_sms, h->smem_optin, static_cast<int>(esize(cfg->dtype)));
     if (!h->plan.valid) {
       delete h;
       return SV_ERR_SHAPE;
@@ -269,6 +277,8 @@ struct TruncSpec {
   float p_top_p = 1.0f, q_top_p = 1.0f;
   const int32_t *parents = nullptr;
   int32_t *out_nodes = nullptr;
+  const float *h_scale = nullptr;  // FP8 handles: hidden-row and vocabulary-row scales
+  const float *w_scale = nullptr;
 };
 
 int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
@@ -281,8 +291,22 @@ int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
 int spec_verify_run(spec_verify_t *h, const void *hidden, const void *W_lm,
                     const int32_t *draft_tokens, const float *q_logits, const float *uniforms,
                     float temperature, int32_t *out_tokens, int32_t *out_n_accepted) {
+  if (h && h->cfg.dtype == SV_FP8) return SV_ERR_ARG;  // needs the scales: run_fp8
   return run_impl(h, hidden, W_lm, draft_tokens, q_logits, uniforms, temperature, out_tokens,
                   out_n_accepted, TruncSpec{});
+}
+
+int spec_verify_run_fp8(spec_verify_t *h, const void *hidden8, const float *hidden_scale,
+                        const void *W8, const float *w_scale, const int32_t *draft_tokens,
+                        const float *q_logits, const float *uniforms, float temperature,
+                        int32_t *out_tokens, int32_t *out_n_accepted) {
+  if (!h || h->cfg.dtype != SV_FP8 || !hidden_scale || !w_scale) return SV_ERR_ARG;
+  if (!aligned16(hidden_scale) || !aligned16(w_scale)) return SV_ERR_ALIGN;
+  TruncSpec tr;
+  tr.h_scale = hidden_scale;
+  tr.w_scale = w_scale;
+  return run_impl(h, hidden8, W8, draft_tokens, q_logits, uniforms, temperature, out_tokens,
+                  out_n_accepted, tr);
 }
 
 int spec_verify_run_truncated(spec_verify_t *h, const void *hidden, const void *W_lm,
@@ -328,6 +352,7 @@ int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
              float temperature, int32_t *out_tokens, int32_t *out_n_accepted,
              const TruncSpec &tr) {
   if (!h || !hidden || !W_lm || !out_tokens || !out_n_accepted) return SV_ERR_ARG;
+  if (h->cfg.dtype == SV_FP8 && (!tr.h_scale || !tr.w_scale)) return SV_ERR_ARG;
   if (!(temperature >= 0.0f) || !std::isfinite(temperature)) return SV_ERR_ARG;
   const sv::Dims &D = h->dims;
   const bool greedy = temperature == 0.0f;
@@ -352,15 +377,17 @@ int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
     if (cudaEventRecord(h->ev0[ti], st) != cudaSuccess) return SV_ERR_CUDA;
   }
 
-  if (h->cfg.dtype == SV_BF16) {
+  if (h->cfg.dtype != SV_FP32) {
     const sv::TcPlan &pl = h->plan;
+    const int elt = static_cast<int>(esize(h->cfg.dtype));
     if (h->tmW_ptr != W_lm) {
-      if (encode_w(&h->tmW, W_lm, D.d, D.V, sv::kTileM, pl.chunks) != SV_OK) return SV_ERR_CUDA;
+      if (encode_w(&h->tmW, W_lm, D.d, D.V, sv::kTileM, pl.chunks, elt) != SV_OK)
+        return SV_ERR_CUDA;
       h->tmW_ptr = W_lm;
     }
     if (h->tmH_ptr != hidden) {
-      if (encode_w(&h->tmH, hidden, D.d, D.R, static_cast<uint32_t>(pl.h_box_rows), pl.chunks) !=
-          SV_OK)
+      if (encode_w(&h->tmH, hidden, D.d, D.R, static_cast<uint32_t>(pl.h_box_rows), pl.chunks,
+                   elt) != SV_OK)
         return SV_ERR_CUDA;
       h->tmH_ptr = hidden;
     }
@@ -372,6 +399,10 @@ int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
     P.greedy = greedy ? 1 : 0;
     P.npad = pl.npad;
     P.nkb = pl.nkb;
+    P.kbk = pl.kbk;
+    P.fp8 = h->cfg.dtype == SV_FP8 ? 1 : 0;
+    P.h_scale = tr.h_scale;
+    P.w_scale = tr.w_scale;
     P.chunks = pl.chunks;
     P.stages = pl.stages;
     P.stage_bytes = pl.stage_bytes;
@@ -419,7 +450,9 @@ int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
   T.epoch = epoch;
   T.wait_limit_ns = h->wait_limit_ns;
   T.split_cnt_n = h->num_sms * 4;
-  T.draft_logits_ready = h->cfg.dtype == SV_BF16 ? 1 : 0;
+  T.draft_logits_ready = h->cfg.dtype != SV_FP32 ? 1 : 0;
+  T.h_scale = tr.h_scale;
+  T.w_scale = tr.w_scale;
   T.p_cut = tr.p_cut;
   T.q_cut = tr.q_cut;
   T.parents = tr.parents;
@@ -466,6 +499,7 @@ int spec_verify_run_host(spec_verify_t *h, const void *hidden_host, const void *
                          int32_t *out_tokens_host, int32_t *out_n_accepted_host) {
   if (!h || !hidden_host || !W_lm || !out_tokens_host || !out_n_accepted_host)
     return SV_ERR_ARG;
+  if (h->cfg.dtype == SV_FP8) return SV_ERR_ARG;  // no host path for the FP8 scales
   const sv::Dims &D = h->dims;
   const bool greedy = temperature == 0.0f;
   if (D.K > 0 && !draft_tokens_host) return SV_ERR_ARG;

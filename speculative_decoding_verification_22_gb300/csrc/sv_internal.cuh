@@ -5,6 +5,8 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -226,6 +228,17 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc,
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same with FP8 E4M3 operands (kind::f8f6f4, K = 32 per instruction:
+// the 32 bytes of a row that one bf16 instruction reads).
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives once on `bar` when all tcgen05.mma issued so far by this thread
 // have completed.
 // One lane of the (converged) warp; the same lane every time.
@@ -289,6 +302,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) |
          (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+// kind::f8f6f4 with A and B in E4M3 (type code 0) and an fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
@@ -439,6 +457,42 @@ __device__ __forceinline__ ff dot_bf16_warp(const uint4 *h, const uint4 *w, int6
         acc_product(__uint_as_float(hw[e] << 16), __uint_as_float(ww[e] << 16), s, c);
         acc_product(__uint_as_float(hw[e] & 0xffff0000u), __uint_as_float(ww[e] & 0xffff0000u),
                     s, c);
+      }
+    }
+  }
+  const float hi2 = __fadd_rn(s, c);
+  return warp_sum_ff(ff{hi2, __fsub_rn(c, __fsub_rn(hi2, s))});
+}
+
+// The same for two FP8 E4M3 rows of length d (a multiple of 16): E4M3
+// values are exact in fp32, and so are products of two of them.
+__device__ __forceinline__ ff dot_e4m3_warp(const uint4 *h, const uint4 *w, int64_t lo,
+                                            int64_t hi, int lane) {
+  float s = 0.0f, c = 0.0f;
+  constexpr int kBatch = 4;
+  for (int64_t k0 = lo; k0 < hi; k0 += 32 * kBatch) {
+    uint4 hv[kBatch], wv[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int64_t k = k0 + j * 32 + lane;
+      hv[j] = k < hi ? __ldg(&h[k]) : make_uint4(0, 0, 0, 0);
+      wv[j] = k < hi ? __ldg(&w[k]) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const uint32_t hw[4] = {hv[j].x, hv[j].y, hv[j].z, hv[j].w};
+      const uint32_t ww[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const __nv_fp8x2_storage_t h2 = static_cast<__nv_fp8x2_storage_t>(hw[e] >> (16 * hh));
+          const __nv_fp8x2_storage_t w2 = static_cast<__nv_fp8x2_storage_t>(ww[e] >> (16 * hh));
+          const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
+          const float2 wf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(w2, __NV_E4M3)));
+          acc_product(hf.x, wf.x, s, c);
+          acc_product(hf.y, wf.y, s, c);
+        }
       }
     }
   }

@@ -14,7 +14,11 @@ struct TcParams {
   float inv_t;             // 1/T (T > 0); unused for greedy
   int greedy;              // T == 0
   int npad;                // MMA N = R rounded up to 16
-  int nkb;                 // 64-wide k blocks per tile
+  int nkb;                 // k blocks (128 bytes of a row) per tile
+  int kbk;                 // elements per k block: 64 (bf16) or 128 (FP8 E4M3)
+  int fp8;                 // FP8 E4M3 operands (kind::f8f6f4) and scales
+  const float *h_scale;    // FP8: [R] hidden-row scales
+  const float *w_scale;    // FP8: [V] vocabulary-row scales
   int chunks;              // k blocks per stage (one 3-D TMA box when > 1)
   int stages;              // shared-memory ring depth
   int stage_bytes;         // W slab + H slab, multiple of 1024
@@ -24,19 +28,20 @@ struct TcParams {
   uint32_t tmem_cols;      // TMEM columns allocated per CTA
   uint64_t wait_limit_ns;  // bound of every device-side wait
   unsigned epoch;          // run counter (stamps an abort)
-  const void *H;           // [R, d] bf16 hidden states (draft-token logits)
-  const void *W;           // [V, d] bf16 LM head
+  const void *H;           // [R, d] bf16 / FP8 hidden states (draft-token logits)
+  const void *W;           // [V, d] bf16 / FP8 LM head
   const int32_t *draft;    // [B, K]
 };
 
 struct TcPlan {
-  int npad, ncol, nkb, chunks, stage_bytes, stages, smem, h_boxes, h_box_rows, nslot;
+  int npad, ncol, nkb, kbk, chunks, stage_bytes, stages, smem, h_boxes, h_box_rows, nslot;
   uint32_t tmem_cols;
   int grid, threads;
   bool valid;
 };
 
-TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin);
+// elt: bytes per element of hidden and W (2: bf16, 1: FP8 E4M3)
+TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin, int elt);
 cudaError_t launch_tc(const TcPlan &pl, const TcParams &P, const CUtensorMap &tmW,
                       const CUtensorMap &tmH, cudaStream_t stream);
 
@@ -73,6 +78,8 @@ struct TailParams {
   int draft_logits_ready;  // w.draft_logit was written by the contraction
   int p_cut, q_cut;        // truncated target / draft rows: (M, S, cut) are given
   const int32_t *parents;  // greedy tree verification: [B, K] node parents (else null)
+  const float *h_scale;    // FP8 (dtype SV_FP8): [R] hidden-row scales
+  const float *w_scale;    // FP8: [V] vocabulary-row scales
   int32_t *out_nodes;      // tree: [B, K] accepted path's nodes (may be null)
 };
 cudaError_t launch_tail(const TailParams &P, cudaStream_t stream);

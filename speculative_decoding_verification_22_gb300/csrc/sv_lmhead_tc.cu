@@ -48,8 +48,7 @@ namespace tc {
 #define SV_TC_MAX_CHUNKS 2
 #endif
 
-constexpr int kBK = 64;                            // k per stage (128 bytes)
-constexpr int kWSlabBytes = kTileM * kBK * 2;      // 16 KB
+constexpr int kWSlabBytes = kTileM * 128;          // 16 KB: 128 rows x 128 bytes
 constexpr int kMaxStages = SV_TC_MAX_STAGES;
 constexpr int kNumEpiWarps = 4;
 constexpr int kNumQWarps = 4;
@@ -128,12 +127,15 @@ __device__ __forceinline__ void q_partials(const TcParams &P, int64_t v, bool va
 __device__ __forceinline__ void finish_group(const TcParams &P, const float (&x)[16], int n0,
                                              int64_t v, bool valid, int sub, int lane) {
   const int64_t V = P.dims.V;
+  // FP8: logit = acc * h_scale[row] * w_scale[v]
+  const float ws = P.fp8 ? (valid ? __ldg(&P.w_scale[v]) : 0.0f) : 1.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int n = n0 + i;
     if (n < P.dims.R) {
-      if (valid) P.w.logits[static_cast<int64_t>(n) * V + v] = x[i];
-      const float2 pm = subtile_partial(x[i], valid, P.inv_t, P.greedy != 0);
+      const float l = P.fp8 ? __fmul_rn(__fmul_rn(x[i], __ldg(&P.h_scale[n])), ws) : x[i];
+      if (valid) P.w.logits[static_cast<int64_t>(n) * V + v] = l;
+      const float2 pm = subtile_partial(l, valid, P.inv_t, P.greedy != 0);
       if (lane == 0 && sub < P.dims.nsub)  // the last tile may end inside a subtile row
         P.w.part_p[static_cast<int64_t>(n) * P.dims.nsub + sub] = pm;
     }
@@ -241,10 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sbase + static_cast<uint32_t>(C * kWSlabBytes), &tmH, 0, 0, kb, full,
                         pol_h);
           } else {
-            tma_load_2d(sbase, &tmW, kb * kBK, t * kTileM, full, pol_w);
+            tma_load_2d(sbase, &tmW, kb * P.kbk, t * kTileM, full, pol_w);
             for (int hb = 0; hb < P.h_boxes; ++hb)
               tma_load_2d(sbase + kWSlabBytes + static_cast<uint32_t>(hb * P.h_box_rows * 128),
-                          &tmH, kb * kBK, hb * P.h_box_rows, full, pol_h);
+                          &tmH, kb * P.kbk, hb * P.h_box_rows, full, pol_h);
           }
           ++issued;
           if (++stage == P.stages) {
@@ -275,8 +277,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t bdesc0 = sw128_desc(base + static_cast<uint32_t>(C * kWSlabBytes));
     const uint32_t stage16 = static_cast<uint32_t>(P.stage_bytes >> 4);
     const uint32_t bchunk16 = static_cast<uint32_t>((P.npad * 128) >> 4);
-    const uint32_t idesc = idesc_bf16(kTileM, NCOL != 0 ? P.npad : (P.npad <= 256 ? P.npad : 256));
-    const uint32_t idesc2 = idesc_bf16(kTileM, P.npad > 256 ? P.npad - 256 : 16);
+    const int n1 = NCOL != 0 ? P.npad : (P.npad <= 256 ? P.npad : 256);
+    const int n2 = P.npad > 256 ? P.npad - 256 : 16;
+    const uint32_t idesc = P.fp8 ? idesc_e4m3(kTileM, n1) : idesc_bf16(kTileM, n1);
+    const uint32_t idesc2 = P.fp8 ? idesc_e4m3(kTileM, n2) : idesc_bf16(kTileM, n2);
+    // one 128-byte row of a stage is 4 instructions of 32 bytes: K = 16
+    // bf16 or K = 32 E4M3 each
+    auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+      if (P.fp8) umma_f8(d, a, b, id, acc);
+      else umma_bf16(d, a, b, id, acc);
+    };
     for (int t = t_first; t <= t_last && ok; ++t) {
       int kb0, kb1;
       tile_range(t, u0, u1, ngr, C, kb0, kb1);
@@ -320,9 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d = tmem + static_cast<uint32_t>(slot * NCOL);
           if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              umma_bf16(d, adesc + 2u * k, bdesc + 2u * k, idesc,
-                        (k > 0 || !group_first) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)
+              mma(d, adesc + 2u * k, bdesc + 2u * k, idesc, (k > 0 || !group_first) ? 1u : 0u);
             // release the stage first: the producer's refill is on the
             // critical path, the drain of this slot is not
             if (j == C - 1) umma_commit(smem_u32(&ctl->empty[stage]));
@@ -342,10 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bdesc2 = bdesc + ((256u * 128u) >> 4);
           if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
+            for (int k = 0; k < 4; ++k) {
               const uint32_t acc = (k > 0 || !first) ? 1u : 0u;
-              umma_bf16(d, adesc + 2u * k, bdesc + 2u * k, idesc, acc);
-              if (P.npad > 256) umma_bf16(d + 256u, adesc + 2u * k, bdesc2 + 2u * k, idesc2, acc);
+              mma(d, adesc + 2u * k, bdesc + 2u * k, idesc, acc);
+              if (P.npad > 256) mma(d + 256u, adesc + 2u * k, bdesc2 + 2u * k, idesc2, acc);
             }
             if (j == C - 1) umma_commit(smem_u32(&ctl->empty[stage]));
           }
@@ -393,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the exact logit of every draft token (one warp each, spread over
       // the grid); the decision pass reads them instead of recomputing
       const int K = P.dims.K;
-      const int64_t n16 = P.dims.d / 8;
+      const int64_t n16 = P.dims.d / (P.fp8 ? 16 : 8);
       for (int idx = c * kNumQWarps + quad; idx < P.dims.RQ; idx += G * kNumQWarps) {
         const int b = idx / K, i = idx - b * K;
         const int x = P.draft[idx];
@@ -402,7 +411,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4 *h = static_cast<const uint4 *>(P.H) +
                            (static_cast<int64_t>(b) * (K + 1) + i) * n16;
           const uint4 *w = static_cast<const uint4 *>(P.W) + static_cast<int64_t>(x) * n16;
-          l = dot_bf16_warp(h, w, 0, n16, lane);
+          if (P.fp8) {
+            const int64_t r = static_cast<int64_t>(b) * (K + 1) + i;
+            l = ff_mul_f(ff_mul_f(dot_e4m3_warp(h, w, 0, n16, lane), __ldg(&P.h_scale[r])),
+                         __ldg(&P.w_scale[x]));
+          } else {
+            l = dot_bf16_warp(h, w, 0, n16, lane);
+          }
         }
         if (lane == 0) P.w.draft_logit[idx] = make_float2(l.hi, l.lo);
       }
@@ -554,18 +569,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin) {
+TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin, int elt) {
   TcPlan pl{};
   pl.npad = ((dims.R + 15) / 16) * 16;
   pl.ncol = pl.npad <= 16 ? 16 : pl.npad <= 32 ? 32 : pl.npad <= 64 ? 64 : 0;
-  pl.nkb = static_cast<int>((dims.d + tc::kBK - 1) / tc::kBK);
+  pl.kbk = 128 / elt;  // elements in one 128-byte row of a block
+  pl.nkb = static_cast<int>((dims.d + pl.kbk - 1) / pl.kbk);
   const int ctl_bytes = static_cast<int>(sizeof(tc::Ctl));
   const int budget = smem_optin - 1024 - ctl_bytes;
   // Stages of C consecutive k blocks, loaded as one 3-D box (longer
   // contiguous DRAM runs per W row); needs d a multiple of 64 * C and the
   // hidden slab in one box (npad <= 256).
   pl.chunks = 1;
-  if (dims.d % tc::kBK == 0 && pl.npad <= 256) {
+  if (dims.d % pl.kbk == 0 && pl.npad <= 256) {
     for (int cand = SV_TC_MAX_CHUNKS; cand >= 2; cand /= 2) {
       const int sb = ((cand * (tc::kWSlabBytes + pl.npad * 128) + 1023) / 1024) * 1024;
       if (pl.nkb % cand == 0 && 2 * sb <= budget) {

@@ -142,7 +142,7 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
   D.nchunk = static_cast<int>((cfg->V + sv::kChunk - 1) / sv::kChunk);
   sv::TcPlan plan{};
   if (cfg->dtype == SV_BF16) {
-    plan = sv::plan_tc(D, sms, smem);
+    plan = sv::plan_tc(D, sms, smem, 2);
     if (!plan.valid) return SV_ERR_SHAPE;
   }
 

@@ -102,7 +102,14 @@ __device__ ff dot_warp(const TailParams &P, int64_t hrow, int64_t wrow, int lane
   const int64_t d = P.dims.d;
   float s = 0.0f, c = 0.0f;
   constexpr int kBatch = 4;
-  if (P.dtype == SV_BF16) {
+  if (P.dtype == SV_FP8) {
+    // FP8 LM head: the exact dot of the E4M3 values times both scales
+    const uint4 *h = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(P.H) + hrow * d);
+    const uint4 *w = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(P.W) + wrow * d);
+    const int64_t n = d / 16;
+    const ff raw = dot_e4m3_warp(h, w, n * part / nparts, n * (part + 1) / nparts, lane);
+    return ff_mul_f(ff_mul_f(raw, __ldg(&P.h_scale[hrow])), __ldg(&P.w_scale[wrow]));
+  } else if (P.dtype == SV_BF16) {
     const uint4 *h =
         reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(P.H) + hrow * d);
     const uint4 *w =
@@ -628,7 +635,10 @@ __device__ void finalize_sequence(const TailParams &P, int b, int fin) {
   }
 }
 
-__global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailParams P) {
+// two CTAs per SM (64 registers): one fits beside a contraction CTA, so
+// programmatic dependent launch stages it early, and twice as many run at
+// once when a round has many rows
+__global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const TailParams P) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ unsigned s_ticket;
