@@ -348,6 +348,62 @@ __device__ __forceinline__ float2 subtile_partial(float logit, bool valid, float
   return make_float2(m, warp_sum(e));
 }
 
+// Reduce-scatter over a warp of a 32 x 16 block held as 16 values per lane:
+// every exchange halves the columns a lane keeps (8 + 4 + 2 + 1 shuffles,
+// one more pairs the lanes), so on return lanes 2c and 2c+1 hold column c's
+// reduction.  16 shuffles for 16 columns, against 80 for one butterfly per
+// column, and the shuffles of each stage are independent of one another.
+template <class Op>
+__device__ __forceinline__ float reduce_scatter16(const float (&a)[16], int lane, Op op) {
+  float v8[8], v4[4], v2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float give = b4 ? a[j] : a[j + 8];
+    const float keep = b4 ? a[j + 8] : a[j];
+    v8[j] = op(keep, __shfl_xor_sync(0xffffffffu, give, 16));
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float give = b3 ? v8[j] : v8[j + 4];
+    const float keep = b3 ? v8[j + 4] : v8[j];
+    v4[j] = op(keep, __shfl_xor_sync(0xffffffffu, give, 8));
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float give = b2 ? v4[j] : v4[j + 2];
+    const float keep = b2 ? v4[j + 2] : v4[j];
+    v2[j] = op(keep, __shfl_xor_sync(0xffffffffu, give, 4));
+  }
+  const float give = b1 ? v2[0] : v2[1];
+  const float keep = b1 ? v2[1] : v2[0];
+  const float v1 = op(keep, __shfl_xor_sync(0xffffffffu, give, 2));
+  return op(v1, __shfl_xor_sync(0xffffffffu, v1, 1));
+}
+
+// Subtile partials of 16 columns at once (the same values subtile_partial
+// gives column by column): a[i] is this lane's entry of column i, already
+// divided by T (or the raw logit for greedy), -inf where the entry is past
+// V; bit i of `bad` marks a NaN or +inf entry.  Lanes 2c and 2c+1 return
+// column c's (max, sum-exp), or (NaN, NaN).
+__device__ __forceinline__ float2 column_partials16(const float (&a)[16], unsigned bad,
+                                                   bool greedy, int lane) {
+  const unsigned any_bad = __reduce_or_sync(0xffffffffu, bad);
+  const float m = reduce_scatter16(a, lane, [](float x, float y) { return fmaxf(x, y); });
+  float s = 0.0f;
+  if (!greedy) {
+    float e[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float mi = __shfl_sync(0xffffffffu, m, 2 * i);
+      e[i] = mi > -INFINITY ? expf(a[i] - mi) : 0.0f;
+    }
+    s = reduce_scatter16(e, lane, [](float x, float y) { return x + y; });
+  }
+  if ((any_bad >> (lane >> 1)) & 1u) return make_float2(NAN, NAN);
+  return make_float2(m, s);
+}
+
 // Error-free sum of two floats (Knuth's TwoSum): s + e == a + b exactly.
 __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
   s = __fadd_rn(a, b);

@@ -99,24 +99,64 @@ __device__ __forceinline__ void raise_abort(Ctl *ctl, const TcParams &P) {
   atomicExch(P.w.abort_epoch, P.epoch);
 }
 
-// Streams the draft logits of one 32-entry subtile for every draft row and
-// writes their (max, sum-exp) partials of q / T (8 rows in flight per lane).
-__device__ __forceinline__ void q_partials(const TcParams &P, int64_t v, bool valid,
-                                           int sub, int lane) {
+// Draft-logit rows streamed per warp and batch (loads in flight per lane).
+constexpr int kQBatch = 8;
+
+// (max, sum-exp) partials of q / T for every draft row over the 128 entries
+// of tile t.  Warp wq of the four takes rows wq, wq + 4, ...; a lane holds
+// four consecutive entries (one 16-byte load when rows are 16-byte
+// aligned), eight lanes one 32-entry subtile, so a row of the tile costs
+// three shuffle levels per reduction and a batch keeps 8 x 512 bytes of
+// each warp's loads in flight.
+__device__ __forceinline__ void q_partials(const TcParams &P, int t, int wq, int lane) {
   const int RQ = P.dims.RQ;
   const int64_t V = P.dims.V;
-  for (int r0 = 0; r0 < RQ; r0 += 8) {
-    float x[8];
+  const int64_t v0 = static_cast<int64_t>(t) * kTileM + lane * 4;
+  const bool vec = (V & 3) == 0 && v0 < V;  // then v0 + 3 < V too
+  const int sub = t * (kTileM / kSub) + (lane >> 3);
+  for (int r0 = wq; r0 < RQ; r0 += 4 * kQBatch) {
+    float4 x[kQBatch];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      x[j] = (r0 + j < RQ && valid) ? __ldg(&P.q_logits[static_cast<int64_t>(r0 + j) * V + v])
-                                    : 0.0f;
+    for (int j = 0; j < kQBatch; ++j) {
+      const int r = r0 + 4 * j;
+      const float *row = P.q_logits + static_cast<int64_t>(r < RQ ? r : 0) * V;
+      if (vec) {
+        x[j] = __ldg(reinterpret_cast<const float4 *>(row + v0));
+      } else {
+        x[j].x = v0 < V ? __ldg(row + v0) : 0.0f;
+        x[j].y = v0 + 1 < V ? __ldg(row + v0 + 1) : 0.0f;
+        x[j].z = v0 + 2 < V ? __ldg(row + v0 + 2) : 0.0f;
+        x[j].w = v0 + 3 < V ? __ldg(row + v0 + 3) : 0.0f;
+      }
+    }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (r0 + j < RQ) {
-        const float2 pm = subtile_partial(x[j], valid, P.inv_t, false);
-        if (lane == 0 && sub < P.dims.nsub)
-          P.w.part_q[static_cast<int64_t>(r0 + j) * P.dims.nsub + sub] = pm;
+    for (int j = 0; j < kQBatch; ++j) {
+      const int r = r0 + 4 * j;
+      if (r >= RQ) break;  // warp-uniform
+      const float xv[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+      float a[4];
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool ok = v0 + i < V;
+        a[i] = ok ? xv[i] * P.inv_t : -INFINITY;
+        bad |= ok && (isnan(xv[i]) || xv[i] == INFINITY);
+      }
+      float m = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float s = 0.0f;
+      if (m > -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s += expf(a[i] - m);
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      const unsigned bmask = __ballot_sync(0xffffffffu, bad);
+      if ((lane & 7) == 0 && sub < P.dims.nsub) {
+        const bool sub_bad = ((bmask >> (lane & ~7)) & 0xffu) != 0;
+        P.w.part_q[static_cast<int64_t>(r) * P.dims.nsub + sub] =
+            sub_bad ? make_float2(NAN, NAN) : make_float2(m, s);
       }
     }
   }
@@ -127,19 +167,26 @@ __device__ __forceinline__ void q_partials(const TcParams &P, int64_t v, bool va
 __device__ __forceinline__ void finish_group(const TcParams &P, const float (&x)[16], int n0,
                                              int64_t v, bool valid, int sub, int lane) {
   const int64_t V = P.dims.V;
+  const int R = P.dims.R;
+  const bool greedy = P.greedy != 0;
   // FP8: logit = acc * h_scale[row] * w_scale[v]
   const float ws = P.fp8 ? (valid ? __ldg(&P.w_scale[v]) : 0.0f) : 1.0f;
+  float a[16];
+  unsigned bad = 0;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int n = n0 + i;
-    if (n < P.dims.R) {
-      const float l = P.fp8 ? __fmul_rn(__fmul_rn(x[i], __ldg(&P.h_scale[n])), ws) : x[i];
-      if (valid) P.w.logits[static_cast<int64_t>(n) * V + v] = l;
-      const float2 pm = subtile_partial(l, valid, P.inv_t, P.greedy != 0);
-      if (lane == 0 && sub < P.dims.nsub)  // the last tile may end inside a subtile row
-        P.w.part_p[static_cast<int64_t>(n) * P.dims.nsub + sub] = pm;
-    }
+    const float l =
+        P.fp8 ? __fmul_rn(__fmul_rn(x[i], __ldg(&P.h_scale[n < R ? n : 0])), ws) : x[i];
+    if (valid && n < R) P.w.logits[static_cast<int64_t>(n) * V + v] = l;
+    a[i] = valid ? (greedy ? l : l * P.inv_t) : -INFINITY;
+    bad |= (valid && (isnan(l) || l == INFINITY)) ? (1u << i) : 0u;
   }
+  const float2 pm = column_partials16(a, bad, greedy, lane);
+  const int n = n0 + (lane >> 1);
+  // the last tile may end inside a subtile row
+  if ((lane & 1) == 0 && n < R && sub < P.dims.nsub)
+    P.w.part_p[static_cast<int64_t>(n) * P.dims.nsub + sub] = pm;
 }
 
 // Split-tile hand-off, per warp (each warp owns 32 vocab rows of the tile and
@@ -396,8 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kb0, kb1;
         tile_range(t, u0, u1, ngr, C, kb0, kb1);
         if (kb0 != 0) continue;  // the CTA holding a tile's first k block does it
-        const int64_t v = static_cast<int64_t>(t) * kTileM + quad * 32 + lane;
-        q_partials(P, v, v < P.dims.V, t * (kTileM / kSub) + quad, lane);
+        q_partials(P, t, quad, lane);
       }
       // the exact logit of every draft token (one warp each, spread over
       // the grid); the decision pass reads them instead of recomputing
@@ -509,13 +555,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           float x[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) x[i] = 0.0f;
-          for (int s = s_lo; s <= s_hi; ++s) {
-            uint32_t y[16];
-            tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(s * P.npad + g * 16), y);
-            tmem_ld_wait();
-            tmem_reg_fence(y);
+          // the tile's accumulators (at most four) in one round of loads
+          uint32_t y[4][16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] += __uint_as_float(y[i]);
+          for (int j = 0; j < 4; ++j)
+            if (s_lo + j <= s_hi)
+              tmem_ld16(tmem + lane_addr + static_cast<uint32_t>((s_lo + j) * P.npad + g * 16),
+                        y[j]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (s_lo + j <= s_hi) {
+              tmem_reg_fence(y[j]);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) x[i] += __uint_as_float(y[j][i]);
+            }
           }
           if (split) {
 #pragma unroll
