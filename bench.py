@@ -17,6 +17,13 @@ greedy tree verification of a Medusa-like tree (3 levels of 3 branches, 39
 nodes) at the same shape.  ``--fp8`` times the step with an FP8 E4M3 LM head
 (weights and hidden states quantised per row, fp32 scales).
 
+``--sweep`` runs the batch sweep of the 8B shape instead (B in
+{1,2,4,8,16,32,64} x K in {3,4,5}, T=1, alpha ~0.7; ``--sweep-points
+16x4,64x5`` picks points) and prints one JSON line per point with the
+round rate, the contraction's time and its fractions of the HBM and the
+tensor-core rooflines, to show where the step leaves the memory-bound
+regime.
+
 Prints one JSON line (rank 0).  Metric: verify rounds/s; ``roofline`` is
 the LM-head contraction kernel's algorithmic bytes over its CUDA-event
 duration against the measured HBM copy bandwidth; ``e2e`` is the same
@@ -49,6 +56,7 @@ NOMINAL_HBM_GBS = 8000.0
 KERNEL_SRCS = [os.path.join(ROOT, "speculative_decoding_verification_22_gb300", "csrc", f)
                for f in ("sv_lmhead_tc.cu", "sv_internal.cuh", "sv_kernels.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lmhead_tc_llama8b.md")
+TRAFFIC_FILE_FP8 = os.path.join(ROOT, "profiles", "lmhead_tc_llama8b_fp8.md")
 
 
 # ---------------------------------------------------------------------------
@@ -171,11 +179,14 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
+def recorded_traffic(path=TRAFFIC_FILE):
     """DRAM bytes per launch of the contraction kernel from the committed
-    ncu summary, or None if the kernel source changed since the capture."""
+    ncu summary of this workload, or None if the kernel source changed since
+    the capture (or there is none)."""
+    if path is None:
+        return None
     try:
-        text = open(TRAFFIC_FILE).read()
+        text = open(path).read()
         src = kernel_source_hash()
     except OSError:
         return None
@@ -358,6 +369,95 @@ def workload_config(wl, extra=None, drafts="model", top_k=0, top_p=1.0, tree=Fal
 # GPU arm
 # ---------------------------------------------------------------------------
 
+SWEEP_B = (1, 2, 4, 8, 16, 32, 64)
+SWEEP_K = (3, 4, 5)
+
+
+def sweep_points(spec=None):
+    """(B, K) points of the batch sweep: all of SWEEP_B x SWEEP_K, or the
+    'BxK,BxK' list given."""
+    if not spec:
+        return [(b, k) for b in SWEEP_B for k in SWEEP_K]
+    out = []
+    for item in spec.split(","):
+        b, k = item.lower().split("x")
+        out.append((int(b), int(k)))
+    return out
+
+
+def regime(hbm_frac, tensor_frac):
+    """Which roofline a point is closer to: the bound whose fraction is
+    larger is the one the kernel is pressing against."""
+    return "tensor" if tensor_frac > hbm_frac else "hbm"
+
+
+def batch_sweep(args, dev):
+    """One JSON line per (B, K) point of the 8B-shape batch sweep."""
+    import torch
+    import spec_inputs as si
+    import speculative_decoding_verification_22_gb300 as sv
+    peaks, peak_src = measured_peaks()
+    base = si.workload("sweep")
+    W = si.make_weights(base, seed=1, device=dev)
+    steps = max(20, min(args.steps, 400))
+    for B, K in sweep_points(args.sweep_points):
+        wl = si.workload("sweep", B=B, K=K)
+        set_bytes = 2 * B * (K + 1) * wl.d + 4 * B * K * wl.V + 8 * B * (K + 1)
+        nsets = min(8, n_input_sets(set_bytes))
+        sets = [si.make_round(wl, W, seed=30_000 + 100 * B + 10 * K + i) for i in range(nsets)]
+        eng = sv.SpecVerify(wl.V, wl.d, B, K, "bf16", device=dev)
+        stream = torch.cuda.Stream(device=dev)
+        sv.spec_verify_set_stream(eng.h, stream)
+        ot = [torch.empty((B, K + 1), dtype=torch.int32, device=dev) for _ in range(nsets)]
+        on = [torch.empty((B,), dtype=torch.int32, device=dev) for _ in range(nsets)]
+
+        def run(i):
+            s = sets[i % nsets]
+            sv.spec_verify_run(eng.h, s["hidden"], W, s["draft"], s["q_logits"], s["uniforms"],
+                               wl.T, ot[i % nsets], on[i % nsets])
+
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for i in range(max(args.warmup, nsets)):
+                run(i)
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(steps):
+                run(i)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        el = e0.elapsed_time(e1) / 1e3
+        sv.spec_verify_timing(eng.h, True)
+        with torch.cuda.stream(stream):
+            for i in range(steps):
+                run(i)
+        ms_k1, n_k1 = sv.spec_verify_timing_read(eng.h)
+        sv.spec_verify_timing(eng.h, False)
+        code = eng.status()
+        tokens = float((torch.stack(on).cpu().numpy() + 1).sum(axis=1).mean())
+        eng.close()
+        if code != sv.SV_OK:
+            raise RuntimeError(f"B={B} K={K}: {sv.spec_verify_strerror(code)}")
+        k1_s = ms_k1 / 1e3 / n_k1
+        k1_bytes = contraction_bytes(wl.V, wl.d, B, K)
+        flops = 2.0 * B * (K + 1) * wl.d * wl.V
+        hbm = k1_bytes / k1_s / 1e9 / peaks["hbm_gbs"]
+        tc = flops / k1_s / 1e12 / peaks["bf16_tflops"]
+        rate = steps / el
+        print(json.dumps({
+            "mode": "sweep", "unit": UNIT, "B": B, "K": K, "rows": B * (K + 1),
+            "value": rate, "ms_per_step": 1e3 * el / steps,
+            "emitted_tokens_per_s": rate * tokens, "emitted_tokens_per_round": tokens,
+            "contraction_us": k1_s * 1e6, "contraction_bytes": k1_bytes,
+            "contraction_gflop": flops / 1e9, "flop_per_byte": flops / k1_bytes,
+            "hbm_frac": hbm, "tensor_frac": tc, "pressing_on": regime(hbm, tc),
+            "peaks": f"{peak_src}: hbm {peaks['hbm_gbs']} GB/s, bf16 {peaks['bf16_tflops']} TF/s",
+            "steps": steps, "data": "synthetic"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -373,6 +473,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--clock-log", default=None)
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--sweep-points", default=None)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -392,6 +494,13 @@ def main():
     if args.tree:
         tree_par = medusa_tree()
         wl = si.workload(args.workload, K=len(tree_par), T=0.0)
+
+    if args.sweep and args.impl != "reference":
+        if rank == 0:
+            batch_sweep(args, dev)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     if args.impl == "reference":
         if rank == 0:
@@ -531,8 +640,8 @@ def main():
     value = total_rounds / max_el
 
     # emitted tokens per round over the input sets
-    n_host = torch.stack(out_n).cpu().numpy()
-    tokens_per_round = float((n_host + 1).mean())
+    n_host = torch.stack(out_n).cpu().numpy()   # [sets, B]
+    tokens_per_round = float((n_host + 1).sum(axis=1).mean())
 
     # contraction kernel timing (CUDA events on the launching stream)
     kt_steps = min(steps, 2000)
@@ -553,9 +662,12 @@ def main():
                                    elt=1 if fp8 else 2, ctx_tokens=CTX_TOKENS if ngram else 0)
     if fp8:
         step_bytes += 4 * wl.V + 4 * wl.B * (wl.K + 1)
+    # ncu captures exist for the default workload and its FP8 variant only
+    plain = args.workload == "llama8b" and not (ngram or truncated or args.tree)
+    traffic_file = (TRAFFIC_FILE_FP8 if fp8 else TRAFFIC_FILE) if plain else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "traffic": recorded_traffic(),
+                "traffic": recorded_traffic(traffic_file),
                 "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                 "kernel": "lmhead_tc_kernel (LM-head contraction + softmax partials)",
                 "kernel_us": k1_s * 1e6, "algorithmic_bytes_per_launch": k1_bytes,

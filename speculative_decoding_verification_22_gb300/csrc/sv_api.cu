@@ -409,6 +409,7 @@ int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
     P.h_boxes = pl.h_boxes;
     P.h_box_rows = pl.h_box_rows;
     P.nslot = pl.nslot;
+    P.nbuf = pl.nbuf;
     P.tmem_cols = pl.tmem_cols;
     P.wait_limit_ns = h->wait_limit_ns;
     P.epoch = epoch;

@@ -25,6 +25,7 @@ struct TcParams {
   int h_boxes;             // TMA boxes per H slab (1 or 2)
   int h_box_rows;          // rows per H box
   int nslot;               // direct mode: TMEM accumulators per tile
+  int nbuf;                // direct mode: tiles in TMEM at once (1 or 2)
   uint32_t tmem_cols;      // TMEM columns allocated per CTA
   uint64_t wait_limit_ns;  // bound of every device-side wait
   unsigned epoch;          // run counter (stamps an abort)
@@ -34,7 +35,7 @@ struct TcParams {
 };
 
 struct TcPlan {
-  int npad, ncol, nkb, kbk, chunks, stage_bytes, stages, smem, h_boxes, h_box_rows, nslot;
+  int npad, ncol, nkb, kbk, chunks, stage_bytes, stages, smem, h_boxes, h_box_rows, nslot, nbuf;
   uint32_t tmem_cols;
   int grid, threads;
   bool valid;

@@ -55,9 +55,10 @@ constexpr int kNumQWarps = 4;
 constexpr int kThreads = 64 + 32 * (kNumEpiWarps + kNumQWarps);  // 320
 constexpr int kMaxDrainSlots = 32;
 // TMEM slots of the drain ring for a column capacity NCOL (<= 512 columns)
+// (direct mode: the two tile buffers)
 template <int NCOL>
 constexpr int drain_slots() {
-  return NCOL == 0 ? 1 : (512 / NCOL < SV_TC_DRAIN_SLOTS ? 512 / NCOL : SV_TC_DRAIN_SLOTS);
+  return NCOL == 0 ? 2 : (512 / NCOL < SV_TC_DRAIN_SLOTS ? 512 / NCOL : SV_TC_DRAIN_SLOTS);
 }
 // 64-wide k blocks accumulated into one drain slot.  At 64 columns TMEM
 // holds only 8 slots; two blocks per slot halve the drain's TMEM reads per
@@ -338,8 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int kb0, kb1;
       tile_range(t, u0, u1, ngr, C, kb0, kb1);
       if constexpr (NCOL == 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->tempty[0]), tphase ^ 1u,
-                                               P.wait_limit_ns, abort))) {
+        // direct mode: tiles alternate between nbuf TMEM buffers of 256
+        // columns; tphase bit b is buffer b's phase
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->tempty[slot]),
+                                               ((tphase >> slot) & 1u) ^ 1u, P.wait_limit_ns,
+                                               abort))) {
           if (lane == 0) raise_abort(ctl, P);
           break;
         }
@@ -347,6 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint64_t adesc = 0, bdesc = 0;
       int j = 0;  // chunk within the current stage (kb0 is a multiple of C)
+      // direct mode: accumulator ds = floor(kb * nslot / nkb) of block kb and
+      // the first block of the next accumulator, advanced incrementally
+      int ds = 0, dnext = 0;
+      if constexpr (NCOL == 0) {
+        ds = (kb0 * P.nslot) / nkb;
+        dnext = ((ds + 1) * nkb + P.nslot - 1) / P.nslot;
+      }
       for (int kb = kb0; kb < kb1; ++kb) {
         // drain mode: groups of kblocks_per_slot k blocks share a slot
         const int gpos = (kb - kb0) % kblocks_per_slot<NCOL>();
@@ -390,10 +401,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tphase ^= 1u;
           }
         } else {
-          const int s = static_cast<int>(static_cast<int64_t>(kb) * P.nslot / nkb);
-          const bool first =
-              kb == kb0 || static_cast<int>(static_cast<int64_t>(kb - 1) * P.nslot / nkb) != s;
-          const uint32_t d = tmem + static_cast<uint32_t>(s * P.npad);
+          bool first = kb == kb0;
+          if (kb == dnext) {
+            ++ds;
+            first = true;
+            dnext = ((ds + 1) * nkb + P.nslot - 1) / P.nslot;
+          }
+          const uint32_t d = tmem + static_cast<uint32_t>(slot * 256 + ds * P.npad);
           // npad > 256 only with single-chunk stages
           const uint64_t bdesc2 = bdesc + ((256u * 128u) >> 4);
           if (elect_one()) {
@@ -419,9 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if constexpr (NCOL == 0) {
         if (ok) {
-          if (elect_one()) umma_commit(smem_u32(&ctl->tfull[0]));
+          if (elect_one()) umma_commit(smem_u32(&ctl->tfull[slot]));
           __syncwarp();
-          tphase ^= 1u;
+          tphase ^= 1u << slot;
+          if (++slot >= P.nbuf) slot = 0;
         }
       }
     }
@@ -543,14 +558,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // direct mode: sum the tile's accumulators column group by group
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->tfull[0]), tphase,
-                                               P.wait_limit_ns, abort))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->tfull[slot]),
+                                               (tphase >> slot) & 1u, P.wait_limit_ns, abort))) {
           if (lane == 0) raise_abort(ctl, P);
           break;
         }
         tc_fence_after();
-        const int s_lo = static_cast<int>(static_cast<int64_t>(kb0) * P.nslot / nkb);
-        const int s_hi = static_cast<int>(static_cast<int64_t>(kb1 - 1) * P.nslot / nkb);
+        const int s_lo = (kb0 * P.nslot) / nkb;
+        const int s_hi = ((kb1 - 1) * P.nslot) / nkb;
         for (int g = 0; g < P.npad / 16; ++g) {
           float x[16];
 #pragma unroll
@@ -560,7 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             if (s_lo + j <= s_hi)
-              tmem_ld16(tmem + lane_addr + static_cast<uint32_t>((s_lo + j) * P.npad + g * 16),
+              tmem_ld16(tmem + lane_addr +
+                            static_cast<uint32_t>(slot * 256 + (s_lo + j) * P.npad + g * 16),
                         y[j]);
           tmem_ld_wait();
 #pragma unroll
@@ -580,8 +596,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[0]));
-        tphase ^= 1u;
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[slot]));
+        tphase ^= 1u << slot;
+        if (++slot >= P.nbuf) slot = 0;
         if (split) {
           if (!split_publish(P, bidx, quad, lane)) continue;
           for (int g = 0; g < P.npad / 16; ++g) {
@@ -658,6 +675,7 @@ TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin, int elt) {
   pl.h_box_rows = pl.npad <= 256 ? pl.npad : pl.npad / 2;
   if (pl.ncol != 0) {
     pl.nslot = 1;
+    pl.nbuf = 1;
     const int slots = pl.ncol == 16 ? tc::drain_slots<16>()
                       : pl.ncol == 32 ? tc::drain_slots<32>() : tc::drain_slots<64>();
     int cols = 32;
@@ -665,8 +683,11 @@ TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin, int elt) {
     pl.tmem_cols = static_cast<uint32_t>(cols);
   } else {
     // contiguous k ranges, one per accumulator; never more accumulators
-    // than k blocks, so every accumulator of a tile range receives a block
-    int ns = 512 / pl.npad;
+    // than k blocks, so every accumulator of a tile range receives a block.
+    // Up to 256 columns two tiles fit (the MMA fills one while the
+    // epilogue drains the other).
+    pl.nbuf = pl.npad <= 256 ? 2 : 1;
+    int ns = (pl.nbuf == 2 ? 256 : 512) / pl.npad;
     ns = ns < 1 ? 1 : (ns > 4 ? 4 : ns);
     pl.nslot = ns < pl.nkb ? ns : pl.nkb;
     pl.tmem_cols = 512;

@@ -144,3 +144,15 @@ def test_ngram_draft_rejects_bad_arguments_before_cuda(lib):
     assert f(good, 8, good, 1, 4, 3, 2, good, good, None) == sv.SV_ERR_ARG    # n_max < n_min
     assert f(good, 8, good, 1, 4, 2, 17, good, good, None) == sv.SV_ERR_ARG   # n_max > 16
     assert f(good + 2, 8, good, 1, 4, 2, 5, good, good, None) == sv.SV_ERR_ALIGN
+
+
+def test_sweep_points_cover_the_batch_grid():
+    pts = bench.sweep_points()
+    assert len(pts) == 21
+    assert (1, 3) in pts and (64, 5) in pts
+    assert bench.sweep_points("16x4,64X5") == [(16, 4), (64, 5)]
+
+
+def test_sweep_regime_follows_the_larger_fraction():
+    assert bench.regime(0.9, 0.1) == "hbm"
+    assert bench.regime(0.4, 0.7) == "tensor"
