@@ -54,6 +54,9 @@ struct spec_verify {
   // TMA descriptors, re-encoded when the tensor moves
   CUtensorMap tmW{}, tmH{};
   const void *tmW_ptr = nullptr, *tmH_ptr = nullptr;
+  // TMA store map of the logits scratch (fixed for the handle's life)
+  CUtensorMap tmL{};
+  bool tma_logits = false;
   // kernel timing
   bool timing = false;
   std::vector<cudaEvent_t> ev0, ev1;
@@ -118,6 +121,22 @@ int encode_w(CUtensorMap *map, const void *base, int64_t inner, int64_t outer,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   }
+  return r == CUDA_SUCCESS ? SV_OK : SV_ERR_CUDA;
+}
+
+// TMA store map of the fp32 logits scratch [R, V]: box of 16 rows x 32
+// entries (128 bytes, the 128-byte swizzle span).  Rows must be a multiple
+// of 16 bytes apart, so V % 4 == 0.
+int encode_logits(CUtensorMap *map, float *base, int64_t V, int64_t R) {
+  auto fn = encode_fn();
+  if (!fn) return SV_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(R)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 4};
+  cuuint32_t box[2] = {32, 16};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -233,6 +252,10 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
          cudaMemset(h->w.seq_flag, 0, sizeof(unsigned) * D.B) == cudaSuccess &&
          cudaMemset(h->w.seq_final, 0, sizeof(int) * D.B) == cudaSuccess &&
          cudaDeviceSynchronize() == cudaSuccess;
+  if (ok && cfg->dtype != SV_FP32 && cfg->V % 4 == 0) {
+    ok = encode_logits(&h->tmL, h->w.logits, D.V, R) == SV_OK;
+    h->tma_logits = ok;
+  }
   if (!ok) {
     free_all(h);
     delete h;
@@ -410,13 +433,14 @@ int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
     P.h_box_rows = pl.h_box_rows;
     P.nslot = pl.nslot;
     P.nbuf = pl.nbuf;
+    P.tma_logits = h->tma_logits ? 1 : 0;
     P.tmem_cols = pl.tmem_cols;
     P.wait_limit_ns = h->wait_limit_ns;
     P.epoch = epoch;
     P.H = hidden;
     P.W = W_lm;
     P.draft = draft_tokens;
-    e = sv::launch_tc(pl, P, h->tmW, h->tmH, st);
+    e = sv::launch_tc(pl, P, h->tmW, h->tmH, h->tmL, st);
   } else {
     sv::SimtParams P{};
     P.dims = D;

@@ -26,6 +26,7 @@ struct TcParams {
   int h_box_rows;          // rows per H box
   int nslot;               // direct mode: TMEM accumulators per tile
   int nbuf;                // direct mode: tiles in TMEM at once (1 or 2)
+  int tma_logits;          // logits written by TMA stores (needs V % 4 == 0)
   uint32_t tmem_cols;      // TMEM columns allocated per CTA
   uint64_t wait_limit_ns;  // bound of every device-side wait
   unsigned epoch;          // run counter (stamps an abort)
@@ -44,7 +45,7 @@ struct TcPlan {
 // elt: bytes per element of hidden and W (2: bf16, 1: FP8 E4M3)
 TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin, int elt);
 cudaError_t launch_tc(const TcPlan &pl, const TcParams &P, const CUtensorMap &tmW,
-                      const CUtensorMap &tmH, cudaStream_t stream);
+                      const CUtensorMap &tmH, const CUtensorMap &tmL, cudaStream_t stream);
 
 // ---- (a) LM-head contraction, fp32 SIMT path -----------------------------
 struct SimtParams {

@@ -72,6 +72,11 @@ constexpr int kblocks_per_slot() {
   return NCOL == 64 ? SV_TC_KPS64 : 1;
 }
 constexpr uint64_t kCleanupLimitNs = 2000000000ull;
+// Epilogue staging: one 2 KB box ([16 columns][32 entries] fp32) per
+// epilogue warp, after the stage ring (1024-byte aligned: the box uses the
+// TMA 128-byte swizzle).
+constexpr int kBoxFloats = 16 * 32;
+constexpr int kEpiBytes = kNumEpiWarps * kBoxFloats * 4;
 
 struct Ctl {
   uint64_t full[kMaxStages];
@@ -163,31 +168,89 @@ __device__ __forceinline__ void q_partials(const TcParams &P, int t, int wq, int
   }
 }
 
+// One epilogue warp's staging box (generic and shared-window addresses).
+struct EpiBox {
+  float *buf;
+  uint32_t saddr;
+};
+
 // Writes logits and target partials for columns n0 .. n0+15 of a finished
-// tile (this thread holds vocab entry v).
-__device__ __forceinline__ void finish_group(const TcParams &P, const float (&x)[16], int n0,
-                                             int64_t v, bool valid, int sub, int lane) {
+// tile; this lane holds vocab entry v = vw + lane of the warp's 32 entries
+// vw .. vw+31 (one subtile).  The 16 x 32 block goes through a shared-memory
+// box: row i holds column n0+i, its 16-byte chunks swizzled by (i mod 8) as
+// the TMA 128-byte pattern expects, so both the lanes' writes (one column
+// each) and the partial pass's 16-byte reads (half a column each) are free
+// of bank conflicts.  One TMA store then writes the box to the logits; the
+// partials need one shuffle per reduction instead of a butterfly.
+__device__ __forceinline__ void finish_group(const TcParams &P, const CUtensorMap *tmL,
+                                             const EpiBox &bx, const float (&x)[16], int n0,
+                                             int64_t vw, int sub, int lane) {
   const int64_t V = P.dims.V;
   const int R = P.dims.R;
   const bool greedy = P.greedy != 0;
+  const int64_t v = vw + lane;
+  const bool valid = v < V;
   // FP8: logit = acc * h_scale[row] * w_scale[v]
   const float ws = P.fp8 ? (valid ? __ldg(&P.w_scale[v]) : 0.0f) : 1.0f;
-  float a[16];
-  unsigned bad = 0;
+  float l[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int n = n0 + i;
-    const float l =
-        P.fp8 ? __fmul_rn(__fmul_rn(x[i], __ldg(&P.h_scale[n < R ? n : 0])), ws) : x[i];
-    if (valid && n < R) P.w.logits[static_cast<int64_t>(n) * V + v] = l;
-    a[i] = valid ? (greedy ? l : l * P.inv_t) : -INFINITY;
-    bad |= (valid && (isnan(l) || l == INFINITY)) ? (1u << i) : 0u;
+    l[i] = P.fp8 ? __fmul_rn(__fmul_rn(x[i], __ldg(&P.h_scale[n < R ? n : 0])), ws) : x[i];
   }
-  const float2 pm = column_partials16(a, bad, greedy, lane);
-  const int n = n0 + (lane >> 1);
+  float *box = bx.buf;
+  const uint32_t sbox = bx.saddr;
+  // the previous group's store must have finished reading the box
+  if (P.tma_logits && lane == 0) bulk_wait_read0();
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) box[i * 32 + (((lane >> 2) ^ (i & 7)) << 2) + (lane & 3)] = l[i];
+  if (P.tma_logits) {
+    fence_proxy_async_smem();
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (valid && n0 + i < R) P.w.logits[static_cast<int64_t>(n0 + i) * V + v] = l[i];
+  }
+  __syncwarp();
+  if (P.tma_logits && lane == 0 && vw < V) {
+    tma_store_2d(tmL, sbox, static_cast<int32_t>(vw), n0);
+    bulk_commit();
+  }
+  // partials: lane -> column c = lane / 2, entries 16h .. 16h+15 (h = lane % 2)
+  const int c = lane >> 1, h = lane & 1;
+  float a[16];
+  bool bad = false;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 q4 =
+        *reinterpret_cast<const float4 *>(box + c * 32 + (((4 * h + k) ^ (c & 7)) << 2));
+    const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool ok = vw + 16 * h + 4 * k + j < V;
+      a[4 * k + j] = ok ? (greedy ? qv[j] : qv[j] * P.inv_t) : -INFINITY;
+      bad |= ok && (isnan(qv[j]) || qv[j] == INFINITY);
+    }
+  }
+  float m = a[0];
+#pragma unroll
+  for (int i = 1; i < 16; ++i) m = fmaxf(m, a[i]);
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  float sum = 0.0f;
+  if (!greedy) {
+    if (m > -INFINITY) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sum += expf(a[i] - m);
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  }
+  const unsigned bmask = __ballot_sync(0xffffffffu, bad);
+  const int n = n0 + c;
   // the last tile may end inside a subtile row
-  if ((lane & 1) == 0 && n < R && sub < P.dims.nsub)
-    P.w.part_p[static_cast<int64_t>(n) * P.dims.nsub + sub] = pm;
+  if (h == 0 && n < R && sub < P.dims.nsub)
+    P.w.part_p[static_cast<int64_t>(n) * P.dims.nsub + sub] =
+        ((bmask >> (2 * c)) & 3u) ? make_float2(NAN, NAN) : make_float2(m, sum);
 }
 
 // Split-tile hand-off, per warp (each warp owns 32 vocab rows of the tile and
@@ -212,12 +275,14 @@ __device__ __forceinline__ void split_reset(const TcParams &P, int bidx, int qua
 template <int NCOL>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmW,
-                     const __grid_constant__ CUtensorMap tmH, const TcParams P) {
+                     const __grid_constant__ CUtensorMap tmH,
+                     const __grid_constant__ CUtensorMap tmL, const TcParams P) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  Ctl *ctl = reinterpret_cast<Ctl *>(smem_raw + (base - raw) +
-                                     static_cast<uint32_t>(P.stages * P.stage_bytes));
+  // [stage ring][epilogue boxes][control block]
+  const uint32_t epi_off = (base - raw) + static_cast<uint32_t>(P.stages * P.stage_bytes);
+  Ctl *ctl = reinterpret_cast<Ctl *>(smem_raw + epi_off + kEpiBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int nkb = P.nkb;
@@ -247,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmH);
+    if (P.tma_logits) tma_prefetch_desc(&tmL);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl->tmem_base), P.tmem_cols);
@@ -488,13 +554,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t box_off = epi_off + static_cast<uint32_t>(quad * kBoxFloats * 4);
+    const EpiBox bx{reinterpret_cast<float *>(smem_raw + box_off), raw + box_off};
     int slot = 0;
     uint32_t tphase = 0;
     for (int t = t_first; t <= t_last; ++t) {
       int kb0, kb1;
       tile_range(t, u0, u1, ngr, C, kb0, kb1);
-      const int64_t v = static_cast<int64_t>(t) * kTileM + row_in_tile;
-      const bool valid = v < P.dims.V;
+      const int64_t vw = static_cast<int64_t>(t) * kTileM + quad * 32;
       const int sub = t * (kTileM / kSub) + quad;
       const bool split = kb0 != 0 || kb1 != nkb;
       const int bidx = kb0 == 0 ? c : c - 1;
@@ -554,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float x[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) x[i] = val[g * 16 + i];
-          finish_group(P, x, g * 16, v, valid, sub, lane);
+          finish_group(P, &tmL, bx, x, g * 16, vw, sub, lane);
         }
       } else {
         // direct mode: sum the tile's accumulators column group by group
@@ -570,28 +637,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           float x[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) x[i] = 0.0f;
-          // the tile's accumulators (at most four) in one round of loads
-          uint32_t y[4][16];
+          // the tile's accumulators (at most four), two per round of loads
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (s_lo + j <= s_hi)
-              tmem_ld16(tmem + lane_addr +
-                            static_cast<uint32_t>(slot * 256 + (s_lo + j) * P.npad + g * 16),
-                        y[j]);
-          tmem_ld_wait();
+          for (int j0 = 0; j0 < 4; j0 += 2) {
+            if (s_lo + j0 > s_hi) break;
+            uint32_t y[2][16];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (s_lo + j <= s_hi) {
-              tmem_reg_fence(y[j]);
+            for (int j = 0; j < 2; ++j)
+              if (s_lo + j0 + j <= s_hi)
+                tmem_ld16(tmem + lane_addr +
+                              static_cast<uint32_t>(slot * 256 + (s_lo + j0 + j) * P.npad + g * 16),
+                          y[j]);
+            tmem_ld_wait();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) x[i] += __uint_as_float(y[j][i]);
+            for (int j = 0; j < 2; ++j) {
+              if (s_lo + j0 + j <= s_hi) {
+                tmem_reg_fence(y[j]);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[i] += __uint_as_float(y[j][i]);
+              }
             }
           }
           if (split) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) mine[(g * 16 + i) * kTileM + row_in_tile] = x[i];
           } else {
-            finish_group(P, x, g * 16, v, valid, sub, lane);
+            finish_group(P, &tmL, bx, x, g * 16, vw, sub, lane);
           }
         }
         tc_fence_before();
@@ -608,12 +679,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int idx = (g * 16 + i) * kTileM + row_in_tile;
               x[i] = __ldcg(&mine[idx]) + __ldcg(&other[idx]);
             }
-            finish_group(P, x, g * 16, v, valid, sub, lane);
+            finish_group(P, &tmL, bx, x, g * 16, vw, sub, lane);
           }
           split_reset(P, bidx, quad, lane);
         }
       }
     }
+    // the logits stores must be complete (and done reading the boxes)
+    // before the kernel ends
+    if (P.tma_logits && lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   // ---------------- teardown ----------------
@@ -646,7 +721,7 @@ TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin, int elt) {
   pl.ncol = pl.npad <= 16 ? 16 : pl.npad <= 32 ? 32 : pl.npad <= 64 ? 64 : 0;
   pl.kbk = 128 / elt;  // elements in one 128-byte row of a block
   pl.nkb = static_cast<int>((dims.d + pl.kbk - 1) / pl.kbk);
-  const int ctl_bytes = static_cast<int>(sizeof(tc::Ctl));
+  const int ctl_bytes = static_cast<int>(sizeof(tc::Ctl)) + tc::kEpiBytes;
   const int budget = smem_optin - 1024 - ctl_bytes;
   // Stages of C consecutive k blocks, loaded as one 3-D box (longer
   // contiguous DRAM runs per W row); needs d a multiple of 64 * C and the
@@ -701,7 +776,7 @@ TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin, int elt) {
 static int g_attr_smem[4] = {0, 0, 0, 0};
 
 cudaError_t launch_tc(const TcPlan &pl, const TcParams &P, const CUtensorMap &tmW,
-                      const CUtensorMap &tmH, cudaStream_t stream) {
+                      const CUtensorMap &tmH, const CUtensorMap &tmL, cudaStream_t stream) {
   const void *fn;
   int which;
   switch (pl.ncol) {
@@ -726,7 +801,7 @@ cudaError_t launch_tc(const TcPlan &pl, const TcParams &P, const CUtensorMap &tm
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void *args[] = {const_cast<CUtensorMap *>(&tmW), const_cast<CUtensorMap *>(&tmH),
-                  const_cast<TcParams *>(&P)};
+                  const_cast<CUtensorMap *>(&tmL), const_cast<TcParams *>(&P)};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

@@ -95,6 +95,25 @@ int encode_w_local(CUtensorMap *map, const void *ptr, int64_t inner, int64_t out
   return r == CUDA_SUCCESS ? SV_OK : SV_ERR_CUDA;
 }
 
+// TMA store map of the fp32 logits scratch (same box as the handle path).
+int encode_logits_local(CUtensorMap *map, float *base, int64_t V, int64_t R) {
+  void *p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return SV_ERR_CUDA;
+  auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(R)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 4};
+  cuuint32_t box[2] = {32, 16};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SV_OK : SV_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidden,
@@ -182,10 +201,12 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
   const float inv_t = greedy ? 1.0f : static_cast<float>(1.0 / static_cast<double>(temperature));
   cudaError_t e;
   if (cfg->dtype == SV_BF16) {
-    CUtensorMap tmW, tmH;
+    CUtensorMap tmW, tmH, tmL{};
+    const bool tma_logits = D.V % 4 == 0;
     if (encode_w_local(&tmW, W_lm, D.d, D.V, sv::kTileM, plan.chunks) != SV_OK ||
         encode_w_local(&tmH, hidden, D.d, D.R, static_cast<uint32_t>(plan.h_box_rows),
-                       plan.chunks) != SV_OK)
+                       plan.chunks) != SV_OK ||
+        (tma_logits && encode_logits_local(&tmL, w.logits, D.V, R) != SV_OK))
       return SV_ERR_CUDA;
     sv::TcParams P{};
     P.dims = D;
@@ -195,6 +216,7 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
     P.greedy = greedy ? 1 : 0;
     P.npad = plan.npad;
     P.nkb = plan.nkb;
+    P.kbk = plan.kbk;
     P.chunks = plan.chunks;
     P.stages = plan.stages;
     P.stage_bytes = plan.stage_bytes;
@@ -202,13 +224,14 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
     P.h_box_rows = plan.h_box_rows;
     P.nslot = plan.nslot;
     P.nbuf = plan.nbuf;
+    P.tma_logits = tma_logits ? 1 : 0;
     P.tmem_cols = plan.tmem_cols;
     P.wait_limit_ns = wait_limit_ns;
     P.epoch = epoch;
     P.H = hidden;
     P.W = W_lm;
     P.draft = draft_tokens;
-    e = sv::launch_tc(plan, P, tmW, tmH, st);
+    e = sv::launch_tc(plan, P, tmW, tmH, tmL, st);
   } else {
     sv::SimtParams P{};
     P.dims = D;

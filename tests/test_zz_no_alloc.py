@@ -36,6 +36,9 @@ def _noalloc_call(wl, inp, W, T, out_t, out_n):
     ("llama8b", {}, 0.0),
     ("tiny", {}, 1.0),
     ("tiny", dict(dtype="bf16", B=8, K=3, V=5000, d=1024, w_std=1 / 32), 0.7),
+    # an odd number of 64-wide k blocks (single-block TMA stages) and a
+    # vocabulary that is not a multiple of 4 (logits stored lane by lane)
+    ("tiny", dict(dtype="bf16", B=2, K=3, V=4999, d=960, w_std=1 / 31), 1.0),
 ])
 def test_noalloc_matches_the_handle_path_twice_in_a_row(name, over, T):
     dev = torch.device("cuda:0")
