@@ -17,14 +17,16 @@
 //  * warp 0 issues TMA loads (128B swizzle, W evict-first in L2) into a
 //    ring of shared-memory stages; warp 1 issues tcgen05.mma (kind::f16,
 //    M=128, K=16) into TMEM; warps 2..5 drain TMEM and run the epilogue;
-//  * drain mode (npad <= 64): every k block accumulates into its own TMEM
-//    slot of a ring and the epilogue adds it into fp32 registers with Kahan
-//    compensation, so no long tensor-core accumulation chain can bias the
-//    logits; direct mode (npad > 64): up to four TMEM accumulators per tile
-//    (contiguous k ranges) summed in registers;
-//  * the epilogue writes the fp32 logits, the per-32-entry (max, sum-exp)
-//    partials of logits / T (or the max for T == 0), and the same partials
-//    of the draft logits q / T for the tile, which it streams alongside.
+//  * drain mode (npad <= 64): each group of k blocks (one, or four at 32
+//    and 64 columns) accumulates into its own TMEM slot of a ring and the
+//    epilogue adds it into fp32 registers with round-to-nearest adds, so no
+//    long tensor-core accumulation chain can bias the logits; direct mode
+//    (npad > 64): up to four TMEM accumulators per tile (contiguous k
+//    ranges) summed in registers, two tiles in TMEM up to 256 columns;
+//  * the epilogue stages each 16-column group in shared memory, writes the
+//    fp32 logits with a TMA store, and computes the per-32-entry (max,
+//    sum-exp) partials of logits / T (or the max for T == 0); four more
+//    warps stream the draft logits q / T of the tile for the same partials.
 #include "sv_internal.cuh"
 #include "sv_kernels.h"
 
@@ -60,16 +62,19 @@ template <int NCOL>
 constexpr int drain_slots() {
   return NCOL == 0 ? 2 : (512 / NCOL < SV_TC_DRAIN_SLOTS ? 512 / NCOL : SV_TC_DRAIN_SLOTS);
 }
-// 64-wide k blocks accumulated into one drain slot.  At 64 columns TMEM
-// holds only 8 slots; two blocks per slot halve the drain's TMEM reads per
-// block and let the MMA run 16 blocks ahead of a draining tile end (the
-// tensor cores then sum 8 MMAs of K=16 before each round-to-nearest add).
-#ifndef SV_TC_KPS64
-#define SV_TC_KPS64 4
+// 64-wide k blocks accumulated into one drain slot.  Every drain costs the
+// epilogue a TMEM read and an add per column, so at 32 and 64 columns four
+// blocks share a slot: the tensor cores sum 16 MMAs of K=16 before each
+// round-to-nearest add (a chain of all 64 blocks in TMEM was measured at
+// about four times the logit error: the tensor-core sum drifts toward zero
+// as the chain grows), and the MMA can run 32 (64 columns) or 64 blocks
+// ahead of a draining tile end.
+#ifndef SV_TC_KPS
+#define SV_TC_KPS 4
 #endif
 template <int NCOL>
 constexpr int kblocks_per_slot() {
-  return NCOL == 64 ? SV_TC_KPS64 : 1;
+  return NCOL >= 32 ? SV_TC_KPS : 1;
 }
 constexpr uint64_t kCleanupLimitNs = 2000000000ull;
 // Epilogue staging: one 2 KB box ([16 columns][32 entries] fp32) per
