@@ -770,7 +770,8 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": steps, "warmup": max(args.warmup, nsets),
             "ms_per_step": 1e3 * max_el / steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 (fp32 accumulate)" if fp8 else "bf16",
             "data": "synthetic",
             "config": workload_config(wl, {
                 "l2": f"inputs larger than L2: W_lm {2 * wl.V * wl.d} B per round plus "

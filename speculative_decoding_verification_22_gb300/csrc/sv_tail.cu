@@ -516,48 +516,26 @@ __device__ int decide(const TailParams &P, int b) {
 // ---------------------------------------------------------------------------
 // Selection (one CTA, the last chunk CTA of sequence b)
 // ---------------------------------------------------------------------------
-__device__ void select_token(const TailParams &P, int b, SeqState st) {
-  __shared__ ff s_warp[kTailWarps];
-  __shared__ ff s_base, s_target;
-  __shared__ int s_chunk, s_found, s_last;
-  const int lane = threadIdx.x & 31;
-  const int nchunk = P.dims.nchunk;
-  float2 *mass = P.w.chunk_mass + static_cast<int64_t>(b) * nchunk;
-
-  ff S = ff_make(0.0f);
-  for (int c = threadIdx.x; c < nchunk; c += kTailThreads) S = ff_add(S, ld_ff(&mass[c]));
-  S = block_sum_ff(S, s_warp);
-  if (!(S.hi > 0.0f) && (st.mode == kModeResidual || st.mode == kModeResidualPoint)) {
-    // p_j == q_j on this row: draw from p_j instead
-    st.mode = kModeP;
-    for (int c = 0; c < nchunk; ++c) {
-      float r[kChunkPerThread];
-      const ff m = block_sum_ff(ff_make(chunk_weights(P, st, c, r)), s_warp);
-      if (threadIdx.x == 0) st_ff(&mass[c], m);
-    }
-    __syncthreads();
-    S = ff_make(0.0f);
-    for (int c = threadIdx.x; c < nchunk; c += kTailThreads) S = ff_add(S, ld_ff(&mass[c]));
-    S = block_sum_ff(S, s_warp);
-  }
-  const int64_t rows = P.dims.K + 1;
-  int32_t *out = P.out_tokens + static_cast<int64_t>(b) * rows + st.n_acc;
-  if (!(S.hi > 0.0f)) {
-    if (threadIdx.x == 0) {
-      set_status(P.w.status, SV_ERR_NONFINITE);
-      *out = -1;
-      P.out_n[b] = -1;
-    }
-    return;
-  }
-  if (threadIdx.x < 32) {
-    // locate the chunk holding u * S: warp-level scan of the chunk masses
-    const ff target = ff_mul_f(S, st.u_final);
-    ff carry = ff_make(0.0f), base = ff_make(0.0f), base_last = ff_make(0.0f);
-    int chunk = -1, last = -1;
+// Warp 0: the total mass S of the chunk masses and the chunk holding
+// u * S (a scan of the masses in chunk order), each mass loaded once when
+// there are at most 32 chunks.  Leaves S, the chunk, the mass before it and
+// the target u * S in shared memory.
+__device__ __forceinline__ void locate_chunk(const float2 *mass, int nchunk, float u, int lane,
+                                             ff &s_S, ff &s_base, ff &s_target, int &s_chunk) {
+  const bool one = nchunk <= 32;
+  const ff m0 = (one && lane < nchunk) ? ld_ff(&mass[lane]) : ff_make(0.0f);
+  ff S = m0;
+  if (!one)
+    for (int c = lane + 32; c < nchunk; c += 32) S = ff_add(S, ld_ff(&mass[c]));
+  if (!one && lane < nchunk) S = ff_add(ld_ff(&mass[lane]), S);
+  S = warp_sum_ff(S);
+  const ff target = ff_mul_f(S, u);
+  ff carry = ff_make(0.0f), base = ff_make(0.0f), base_last = ff_make(0.0f);
+  int chunk = -1, last = -1;
+  if (S.hi > 0.0f) {
     for (int c0 = 0; c0 < nchunk && chunk < 0; c0 += 32) {
       const int c = c0 + lane;
-      const ff m = c < nchunk ? ld_ff(&mass[c]) : ff_make(0.0f);
+      const ff m = one ? m0 : (c < nchunk ? ld_ff(&mass[c]) : ff_make(0.0f));
       ff inc = m;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -580,19 +558,56 @@ __device__ void select_token(const TailParams &P, int b, SeqState st) {
       }
       carry = ff_shfl(incl, 31);
     }
-    if (lane == 0) {
-      if (chunk < 0) {  // rounding pushed the target past the end
-        chunk = last;
-        base = base_last;
-      }
-      s_chunk = chunk;
-      s_base = base;
-      s_target = target;
-      s_found = 0x7fffffff;
-      s_last = -1;
+  }
+  if (lane == 0) {
+    if (chunk < 0) {  // rounding pushed the target past the end
+      chunk = last;
+      base = base_last;
     }
+    s_S = S;
+    s_chunk = chunk;
+    s_base = base;
+    s_target = target;
+  }
+}
+
+__device__ void select_token(const TailParams &P, int b, SeqState st) {
+  __shared__ ff s_warp[kTailWarps];
+  __shared__ ff s_S, s_base, s_target;
+  __shared__ int s_chunk, s_found, s_last;
+  const int lane = threadIdx.x & 31;
+  const int nchunk = P.dims.nchunk;
+  float2 *mass = P.w.chunk_mass + static_cast<int64_t>(b) * nchunk;
+
+  if (threadIdx.x < 32) locate_chunk(mass, nchunk, st.u_final, lane, s_S, s_base, s_target, s_chunk);
+  if (threadIdx.x == 0) {
+    s_found = 0x7fffffff;
+    s_last = -1;
   }
   __syncthreads();
+  if (!(s_S.hi > 0.0f) && (st.mode == kModeResidual || st.mode == kModeResidualPoint)) {
+    // p_j == q_j on this row: draw from p_j instead
+    st.mode = kModeP;
+    for (int c = 0; c < nchunk; ++c) {
+      float r[kChunkPerThread];
+      const ff m = block_sum_ff(ff_make(chunk_weights(P, st, c, r)), s_warp);
+      if (threadIdx.x == 0) st_ff(&mass[c], m);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32)
+      locate_chunk(mass, nchunk, st.u_final, lane, s_S, s_base, s_target, s_chunk);
+    __syncthreads();
+  }
+  const int64_t rows = P.dims.K + 1;
+  int32_t *out = P.out_tokens + static_cast<int64_t>(b) * rows + st.n_acc;
+  if (!(s_S.hi > 0.0f)) {
+    if (threadIdx.x == 0) {
+      set_status(P.w.status, SV_ERR_NONFINITE);
+      *out = -1;
+      P.out_n[b] = -1;
+    }
+    return;
+  }
   const int chunk = s_chunk;
   float r[kChunkPerThread];
   const float tsum = chunk_weights(P, st, chunk, r);
@@ -617,8 +632,10 @@ __device__ void select_token(const TailParams &P, int b, SeqState st) {
 // ---------------------------------------------------------------------------
 // The fused tail kernel
 // ---------------------------------------------------------------------------
-// Carries out what arrive_final decided (block-wide).
-__device__ void finalize_sequence(const TailParams &P, int b, int fin) {
+// Carries out what arrive_final decided (block-wide).  `known` is the
+// sequence's published state when the caller already holds it.
+__device__ void finalize_sequence(const TailParams &P, int b, int fin,
+                                  const SeqState *known = nullptr) {
   if (fin == kFinPoison) {
     if (threadIdx.x == 0) {
       const int rows = P.dims.K + 1;
@@ -627,10 +644,14 @@ __device__ void finalize_sequence(const TailParams &P, int b, int fin) {
     }
   } else if (fin == kFinSelect) {
     SeqState st;
-    const int *src = reinterpret_cast<const int *>(&P.w.seq[b]);
-    int *dst = reinterpret_cast<int *>(&st);
+    if (known) {
+      st = *known;
+    } else {
+      const int *src = reinterpret_cast<const int *>(&P.w.seq[b]);
+      int *dst = reinterpret_cast<int *>(&st);
 #pragma unroll
-    for (int i = 0; i < static_cast<int>(sizeof(SeqState) / 4); ++i) dst[i] = __ldcg(&src[i]);
+      for (int i = 0; i < static_cast<int>(sizeof(SeqState) / 4); ++i) dst[i] = __ldcg(&src[i]);
+    }
     if (st.mode != kModeSkip) select_token(P, b, st);
   }
 }
@@ -802,7 +823,9 @@ __global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const TailParams 
       }
     }
     __syncthreads();
-    finalize_sequence(P, b, s_fin);
+    // a chunk CTA that saw the decision holds its state; one that timed out
+    // set the poison bit, so the selection never runs on its copy
+    finalize_sequence(P, b, s_fin, &st);
   }
 
   // the last CTA to finish rewinds the ticket counter for the next launch
