@@ -433,6 +433,7 @@ int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
     P.h_box_rows = pl.h_box_rows;
     P.nslot = pl.nslot;
     P.nbuf = pl.nbuf;
+    P.half = pl.half;
     P.tma_logits = h->tma_logits ? 1 : 0;
     P.tmem_cols = pl.tmem_cols;
     P.wait_limit_ns = h->wait_limit_ns;

@@ -27,6 +27,7 @@ struct TcParams {
   int nslot;               // direct mode: TMEM accumulators per tile
   int nbuf;                // direct mode: tiles in TMEM at once (1 or 2)
   int tma_logits;          // logits written by TMA stores (needs V % 4 == 0)
+  int half;                // CTAs 2p, 2p+1 share tiles, npad columns each
   uint32_t tmem_cols;      // TMEM columns allocated per CTA
   uint64_t wait_limit_ns;  // bound of every device-side wait
   unsigned epoch;          // run counter (stamps an abort)
@@ -37,6 +38,7 @@ struct TcParams {
 
 struct TcPlan {
   int npad, ncol, nkb, kbk, chunks, stage_bytes, stages, smem, h_boxes, h_box_rows, nslot, nbuf;
+  int half;  // npad is then the columns of one CTA of a pair (half of all)
   uint32_t tmem_cols;
   int grid, threads;
   bool valid;

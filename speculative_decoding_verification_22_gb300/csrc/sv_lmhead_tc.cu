@@ -49,6 +49,13 @@ namespace tc {
 #ifndef SV_TC_MAX_CHUNKS
 #define SV_TC_MAX_CHUNKS 2
 #endif
+// direct-mode widths above which CTA pairs split the columns.  Each CTA of
+// a pair reads the whole W tile, and the two reads were measured to come
+// from HBM twice (a 310 us floor at every width), so this pays only where
+// one tile no longer fits TMEM twice (above 256 columns).
+#ifndef SV_TC_HALF_MIN
+#define SV_TC_HALF_MIN 256
+#endif
 
 constexpr int kWSlabBytes = kTileM * 128;          // 16 KB: 128 rows x 128 bytes
 constexpr int kMaxStages = SV_TC_MAX_STAGES;
@@ -113,23 +120,25 @@ __device__ __forceinline__ void raise_abort(Ctl *ctl, const TcParams &P) {
 // Draft-logit rows streamed per warp and batch (loads in flight per lane).
 constexpr int kQBatch = 8;
 
-// (max, sum-exp) partials of q / T for every draft row over the 128 entries
-// of tile t.  Warp wq of the four takes rows wq, wq + 4, ...; a lane holds
+// (max, sum-exp) partials of q / T over the 128 entries of tile t for the
+// draft rows r0, r0 + rstep, ... (warp wq of the four takes r0 = wq, rstep
+// 4; in half mode the two CTAs of a pair interleave, rstep 8); a lane holds
 // four consecutive entries (one 16-byte load when rows are 16-byte
 // aligned), eight lanes one 32-entry subtile, so a row of the tile costs
 // three shuffle levels per reduction and a batch keeps 8 x 512 bytes of
 // each warp's loads in flight.
-__device__ __forceinline__ void q_partials(const TcParams &P, int t, int wq, int lane) {
+__device__ __forceinline__ void q_partials(const TcParams &P, int t, int rfirst, int rstep,
+                                           int lane) {
   const int RQ = P.dims.RQ;
   const int64_t V = P.dims.V;
   const int64_t v0 = static_cast<int64_t>(t) * kTileM + lane * 4;
   const bool vec = (V & 3) == 0 && v0 < V;  // then v0 + 3 < V too
   const int sub = t * (kTileM / kSub) + (lane >> 3);
-  for (int r0 = wq; r0 < RQ; r0 += 4 * kQBatch) {
+  for (int r0 = rfirst; r0 < RQ; r0 += rstep * kQBatch) {
     float4 x[kQBatch];
 #pragma unroll
     for (int j = 0; j < kQBatch; ++j) {
-      const int r = r0 + 4 * j;
+      const int r = r0 + rstep * j;
       const float *row = P.q_logits + static_cast<int64_t>(r < RQ ? r : 0) * V;
       if (vec) {
         x[j] = __ldg(reinterpret_cast<const float4 *>(row + v0));
@@ -142,7 +151,7 @@ __device__ __forceinline__ void q_partials(const TcParams &P, int t, int wq, int
     }
 #pragma unroll
     for (int j = 0; j < kQBatch; ++j) {
-      const int r = r0 + 4 * j;
+      const int r = r0 + rstep * j;
       if (r >= RQ) break;  // warp-uniform
       const float xv[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
       float a[4];
@@ -218,7 +227,7 @@ __device__ __forceinline__ void finish_group(const TcParams &P, const CUtensorMa
       if (valid && n0 + i < R) P.w.logits[static_cast<int64_t>(n0 + i) * V + v] = l[i];
   }
   __syncwarp();
-  if (P.tma_logits && lane == 0 && vw < V) {
+  if (P.tma_logits && lane == 0 && vw < V && n0 < R) {
     tma_store_2d(tmL, sbox, static_cast<int32_t>(vw), n0);
     bulk_commit();
   }
@@ -303,7 +312,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int C = P.chunks;
   const int ngr = nkb / C;
   const int64_t U = static_cast<int64_t>(P.dims.ntile) * ngr;
-  const int G = gridDim.x, c = blockIdx.x;
+  // half mode: CTAs 2p and 2p+1 take the same units, each for half of the
+  // columns (its first column col0); otherwise every CTA its own units
+  const int G = P.half ? gridDim.x / 2 : gridDim.x;
+  const int c = P.half ? blockIdx.x / 2 : blockIdx.x;
+  const int hsel = P.half ? (blockIdx.x & 1) : 0;
+  const int col0 = hsel * P.npad;
   const int64_t u0 = U * c / G, u1 = U * (c + 1) / G;
   const int t_first = static_cast<int>(u0 / ngr);
   const int t_last = static_cast<int>((u1 - 1) / ngr);
@@ -346,7 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
+      // half mode: the partner CTA reads the same W tile at about the same
+      // time, so it keeps normal priority in L2
+      const uint64_t pol_w = P.half ? policy_evict_normal() : policy_evict_first();
       const uint64_t pol_h = policy_evict_last();
       const uint32_t tx = static_cast<uint32_t>(C * (kWSlabBytes + P.npad * 128));
       int stage = 0, issued = 0;
@@ -368,13 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // C consecutive k blocks in one 3-D box: 128 rows x (C x 128 B)
             // contiguous runs; in shared memory C [128 x 64] swizzled tiles
             tma_load_3d(sbase, &tmW, 0, t * kTileM, kb, full, pol_w);
-            tma_load_3d(sbase + static_cast<uint32_t>(C * kWSlabBytes), &tmH, 0, 0, kb, full,
+            tma_load_3d(sbase + static_cast<uint32_t>(C * kWSlabBytes), &tmH, 0, col0, kb, full,
                         pol_h);
           } else {
             tma_load_2d(sbase, &tmW, kb * P.kbk, t * kTileM, full, pol_w);
             for (int hb = 0; hb < P.h_boxes; ++hb)
               tma_load_2d(sbase + kWSlabBytes + static_cast<uint32_t>(hb * P.h_box_rows * 128),
-                          &tmH, kb * P.kbk, hb * P.h_box_rows, full, pol_h);
+                          &tmH, kb * P.kbk, col0 + hb * P.h_box_rows, full, pol_h);
           }
           ++issued;
           if (++stage == P.stages) {
@@ -538,13 +554,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kb0, kb1;
         tile_range(t, u0, u1, ngr, C, kb0, kb1);
         if (kb0 != 0) continue;  // the CTA holding a tile's first k block does it
-        q_partials(P, t, quad, lane);
+        q_partials(P, t, quad + 4 * hsel, P.half ? 8 : 4, lane);
       }
       // the exact logit of every draft token (one warp each, spread over
       // the grid); the decision pass reads them instead of recomputing
       const int K = P.dims.K;
       const int64_t n16 = P.dims.d / (P.fp8 ? 16 : 8);
-      for (int idx = c * kNumQWarps + quad; idx < P.dims.RQ; idx += G * kNumQWarps) {
+      for (int idx = static_cast<int>(blockIdx.x) * kNumQWarps + quad; idx < P.dims.RQ;
+           idx += static_cast<int>(gridDim.x) * kNumQWarps) {
         const int b = idx / K, i = idx - b * K;
         const int x = P.draft[idx];
         ff l = ff_make(NAN);
@@ -578,7 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t vw = static_cast<int64_t>(t) * kTileM + quad * 32;
       const int sub = t * (kTileM / kSub) + quad;
       const bool split = kb0 != 0 || kb1 != nkb;
-      const int bidx = kb0 == 0 ? c : c - 1;
+      // split-tile partner: the CTA of the same half in the neighbouring
+      // pair (or the neighbouring CTA)
+      const int bidx = P.half ? (kb0 == 0 ? c : c - 1) * 2 + hsel : (kb0 == 0 ? c : c - 1);
       const int part = kb0 == 0 ? 0 : 1;
       float *mine = P.w.split_buf + (static_cast<int64_t>(bidx) * 2 + part) * (kTileM * P.npad);
       float *other =
@@ -635,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float x[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) x[i] = val[g * 16 + i];
-          finish_group(P, &tmL, bx, x, g * 16, vw, sub, lane);
+          finish_group(P, &tmL, bx, x, col0 + g * 16, vw, sub, lane);
         }
       } else {
         // direct mode: sum the tile's accumulators column group by group
@@ -676,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) mine[(g * 16 + i) * kTileM + row_in_tile] = x[i];
           } else {
-            finish_group(P, &tmL, bx, x, g * 16, vw, sub, lane);
+            finish_group(P, &tmL, bx, x, col0 + g * 16, vw, sub, lane);
           }
         }
         tc_fence_before();
@@ -693,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int idx = (g * 16 + i) * kTileM + row_in_tile;
               x[i] = __ldcg(&mine[idx]) + __ldcg(&other[idx]);
             }
-            finish_group(P, &tmL, bx, x, g * 16, vw, sub, lane);
+            finish_group(P, &tmL, bx, x, col0 + g * 16, vw, sub, lane);
           }
           split_reset(P, bidx, quad, lane);
         }
@@ -731,8 +750,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin, int elt) {
   TcPlan pl{};
-  pl.npad = ((dims.R + 15) / 16) * 16;
-  pl.ncol = pl.npad <= 16 ? 16 : pl.npad <= 32 ? 32 : pl.npad <= 64 ? 64 : 0;
+  const int npad_all = ((dims.R + 15) / 16) * 16;
+  pl.ncol = npad_all <= 16 ? 16 : npad_all <= 32 ? 32 : npad_all <= 64 ? 64 : 0;
+  // half mode (direct mode above SV_TC_HALF_MIN columns): the two CTAs of a
+  // pair take the same tiles, each for half of the columns, so each loads
+  // half of the hidden-row block into shared memory and holds two
+  // half-width tiles in TMEM
+  pl.half = (pl.ncol == 0 && npad_all > SV_TC_HALF_MIN && num_sms >= 2) ? 1 : 0;
+  pl.npad = pl.half ? ((npad_all / 2 + 15) / 16) * 16 : npad_all;
   pl.kbk = 128 / elt;  // elements in one 128-byte row of a block
   pl.nkb = static_cast<int>((dims.d + pl.kbk - 1) / pl.kbk);
   const int ctl_bytes = static_cast<int>(sizeof(tc::Ctl)) + tc::kEpiBytes;
@@ -781,9 +806,14 @@ TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin, int elt) {
     pl.nslot = ns < pl.nkb ? ns : pl.nkb;
     pl.tmem_cols = 512;
   }
-  pl.grid = dims.ntile < num_sms ? dims.ntile : num_sms;
+  if (pl.half) {
+    const int pairs = dims.ntile < num_sms / 2 ? dims.ntile : num_sms / 2;
+    pl.grid = 2 * pairs;
+  } else {
+    pl.grid = dims.ntile < num_sms ? dims.ntile : num_sms;
+  }
   pl.threads = tc::kThreads;
-  pl.valid = stages >= 2 && pl.npad <= SV_MAX_ROWS_BF16;
+  pl.valid = stages >= 2 && npad_all <= SV_MAX_ROWS_BF16;
   return pl;
 }
 

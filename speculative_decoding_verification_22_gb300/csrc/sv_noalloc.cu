@@ -224,6 +224,7 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
     P.h_box_rows = plan.h_box_rows;
     P.nslot = plan.nslot;
     P.nbuf = plan.nbuf;
+    P.half = plan.half;
     P.tma_logits = tma_logits ? 1 : 0;
     P.tmem_cols = plan.tmem_cols;
     P.wait_limit_ns = wait_limit_ns;
