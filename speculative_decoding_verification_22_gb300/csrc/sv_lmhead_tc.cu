@@ -49,10 +49,12 @@ namespace tc {
 #ifndef SV_TC_MAX_CHUNKS
 #define SV_TC_MAX_CHUNKS 2
 #endif
-// direct-mode widths above which CTA pairs split the columns.  Each CTA of
-// a pair reads the whole W tile, and the two reads were measured to come
-// from HBM twice (a 310 us floor at every width), so this pays only where
-// one tile no longer fits TMEM twice (above 256 columns).
+// direct-mode widths above which CTA pairs split the columns.  Each SM of a
+// pair still takes in the whole W tile for twice as many k blocks, and at
+// large widths the kernel is bound by the bytes each SM takes in from L2
+// (about 70 GB/s per SM measured, with or without a multicast of W inside a
+// 2-CTA cluster), so splitting pays only where one tile no longer fits
+// TMEM twice (above 256 columns).
 #ifndef SV_TC_HALF_MIN
 #define SV_TC_HALF_MIN 256
 #endif
