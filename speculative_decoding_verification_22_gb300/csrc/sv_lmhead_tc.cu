@@ -23,6 +23,8 @@
 //    long tensor-core accumulation chain can bias the logits; direct mode
 //    (npad > 64): up to four TMEM accumulators per tile (contiguous k
 //    ranges) summed in registers, two tiles in TMEM up to 256 columns;
+//    above 256 columns the two CTAs of a pair take the same tiles, each
+//    for half of the columns (half mode), so two tiles fit again;
 //  * the epilogue stages each 16-column group in shared memory, writes the
 //    fp32 logits with a TMA store, and computes the per-32-entry (max,
 //    sum-exp) partials of logits / T (or the max for T == 0); four more
