@@ -25,7 +25,7 @@
  *   [P5] "Speculative Decoding" (library wiki) -- "One speculation round"
  *        (strict r < min(1, p/q) test, bonus from p at position gamma+1).
  *
- * Readings where the pages leave a step open (each is listed in the design doc):
+ * Readings where the pages leave a step open:
  *   R1  p_i = softmax(L_i / T) and q_i = softmax(q_logits_i / T) with the
  *       same temperature T for both ([P1] "three remarks", [P3] Step 3,
  *       [P4] "Where it breaks").

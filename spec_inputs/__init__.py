@@ -53,7 +53,8 @@ class Workload:
 
 
 def workload(name: str, **over) -> Workload:
-    """The configurations of the verify step (input recipe)."""
+    """The configurations of the verify step: shapes, temperatures and draft
+    acceptance targets of the synthetic workloads."""
     base = {
         "tiny": dict(V=1000, d=256, B=1, K=4, T=1.0, dtype="fp32",
                      w_std=1.0 / 16.0, alpha=None, sigma_fixed=0.5,
