@@ -57,6 +57,9 @@ SMALL = [
     (dict(dtype="bf16", B=40, K=5, V=3000, d=256), 1.0),
     (dict(dtype="bf16", B=64, K=5, V=2000, d=128), 1.0),
     (dict(dtype="bf16", B=64, K=5, V=2000, d=128), 0.0),
+    # column halves whose second half runs past the last row, with an odd
+    # number of 64-wide k blocks (single-block stages)
+    (dict(dtype="bf16", B=53, K=4, V=1300, d=192), 0.9),
     (dict(B=1, K=4), 1.0),
     (dict(B=5, K=2, V=97), 0.5),
     (dict(B=5, K=2, V=97), 0.0),
