@@ -66,9 +66,9 @@ extern "C" {
 
 /* Element type of hidden and W_lm. */
 #define SV_BF16 0 /* production path: TMA + tcgen05 tensor-core contraction   */
-#define SV_FP32 1
-#define SV_FP8 2         /* FP8 E4M3 hidden and W_lm with fp32 row scales:
-                          * run through spec_verify_run_fp8                  */ /* reference-precision path for small vocabularies         */
+#define SV_FP32 1 /* reference-precision path for small vocabularies          */
+#define SV_FP8 2  /* FP8 E4M3 hidden and W_lm with fp32 row scales: run
+                   * through spec_verify_run_fp8                             */
 
 /* Limits checked at create time. */
 #define SV_MAX_K 64      /* draft tokens (tree nodes) per sequence           */
@@ -82,7 +82,7 @@ typedef struct {
   int64_t d;      /* hidden size; bf16: multiple of 8, fp32: multiple of 4   */
   int32_t B;      /* sequences per call, 1..SV_MAX_B                         */
   int32_t K;      /* draft tokens per sequence, 0..SV_MAX_K                  */
-  int32_t dtype;  /* SV_BF16 or SV_FP32                                      */
+  int32_t dtype;  /* SV_BF16, SV_FP32 or SV_FP8                              */
   void *stream;   /* cudaStream_t the calls are enqueued on (NULL = legacy)  */
 } sv_config_t;
 
@@ -181,6 +181,33 @@ int spec_verify_timing_read(spec_verify_t *h, double *total_ms,
  * T: the LM-head contraction and one fused decision / residual / selection
  * launch (2 for every T). */
 int spec_verify_launches_per_run(spec_verify_t *h, float temperature);
+
+/* Launch plan of the tensor-core contraction for a configuration: which
+ * accumulation mode runs and how shared memory and tensor memory are laid
+ * out.  Host arithmetic only (no CUDA call, no GPU needed); num_sms and
+ * smem_optin describe the GPU (152 SMs and 232448 bytes of opt-in shared
+ * memory per block on GB300).  For tests and for callers that want to know
+ * what a shape will run.  Returns SV_OK, SV_ERR_ARG (null pointer, num_sms
+ * < 1, dtype not SV_BF16 or SV_FP8) or SV_ERR_SHAPE (the shape create would
+ * reject, or no plan with at least two stages fits smem_optin). */
+typedef struct {
+  int32_t npad;          /* columns one CTA multiplies (rows padded to 16)       */
+  int32_t drain_cols;    /* drain mode: TMEM slot width (16, 32, 64); 0: direct  */
+  int32_t half;          /* 1: the two CTAs of a pair split the columns          */
+  int32_t kblock_elems;  /* elements of one 128-byte k block (64 bf16, 128 fp8)  */
+  int32_t kblocks;       /* k blocks per row: ceil(d / kblock_elems)             */
+  int32_t chunks;        /* k blocks per pipeline stage                          */
+  int32_t stages;        /* pipeline stages in shared memory                     */
+  int32_t stage_bytes;   /* bytes of one stage (multiple of 1024)                */
+  int32_t smem_bytes;    /* dynamic shared memory per CTA                        */
+  int32_t grid;          /* CTAs (persistent, at most one per SM)                */
+  int32_t tmem_cols;     /* TMEM columns allocated per CTA                       */
+  int32_t tmem_buffers;  /* direct mode: tiles held in TMEM at once (1 or 2)     */
+  int32_t tmem_slots;    /* drain: ring slots; direct: accumulators per tile     */
+} sv_plan_t;
+
+int spec_verify_plan(const sv_config_t *cfg, int32_t num_sms, int32_t smem_optin,
+                     sv_plan_t *out);
 
 /* Static description of an error code. */
 const char *spec_verify_strerror(int code);

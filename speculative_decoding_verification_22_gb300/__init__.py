@@ -42,7 +42,13 @@ EXPORTS = ("spec_verify_create", "spec_verify_run", "spec_verify_run_host",
            "spec_verify_timing_read", "spec_verify_launches_per_run",
            "spec_verify_strerror", "spec_verify_destroy",
            "spec_verify_run_noalloc", "spec_ngram_draft", "spec_verify_run_truncated",
-           "spec_verify_tree_greedy", "spec_verify_run_fp8")
+           "spec_verify_tree_greedy", "spec_verify_run_fp8", "spec_verify_plan")
+
+
+class sv_plan_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "npad", "drain_cols", "half", "kblock_elems", "kblocks", "chunks", "stages",
+        "stage_bytes", "smem_bytes", "grid", "tmem_cols", "tmem_buffers", "tmem_slots")]
 
 
 class SpecVerifyError(RuntimeError):
@@ -97,6 +103,8 @@ def load_library():
         lib.spec_verify_run_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, f32, vp, vp]
         lib.spec_ngram_draft.argtypes = [vp, ctypes.c_int64, vp, i32, i32, i32, i32, vp, vp,
                                          vp]
+        lib.spec_verify_plan.argtypes = [ctypes.POINTER(sv_config_t), i32, i32,
+                                         ctypes.POINTER(sv_plan_t)]
         for name in EXPORTS:
             if name not in ("spec_verify_strerror", "spec_verify_destroy"):
                 getattr(lib, name).restype = ctypes.c_int
@@ -127,6 +135,18 @@ def _stream_handle(stream):
 
 def spec_verify_strerror(code: int) -> str:
     return load_library().spec_verify_strerror(int(code)).decode()
+
+
+def spec_verify_plan(V: int, d: int, B: int, K: int, dtype="bf16", num_sms: int = 152,
+                     smem_optin: int = 232448) -> dict:
+    """The contraction's launch plan for a shape (host arithmetic, no GPU):
+    accumulation mode, pipeline stages, shared and tensor memory layout."""
+    code = {"bf16": SV_BF16, "fp8": SV_FP8}.get(dtype, dtype)
+    cfg = sv_config_t(V, d, B, K, code, None)
+    out = sv_plan_t()
+    _check(load_library().spec_verify_plan(ctypes.byref(cfg), num_sms, smem_optin,
+                                           ctypes.byref(out)), "spec_verify_plan")
+    return {n: getattr(out, n) for n, _ in sv_plan_t._fields_}
 
 
 def spec_verify_create(V: int, d: int, B: int, K: int, dtype="bf16", stream=None):

@@ -154,6 +154,48 @@ void fold_timing(spec_verify *h, int64_t upto) {
 
 extern "C" {
 
+int spec_verify_plan(const sv_config_t *cfg, int32_t num_sms, int32_t smem_optin,
+                     sv_plan_t *out) {
+  if (!cfg || !out || num_sms < 1) return SV_ERR_ARG;
+  if (cfg->dtype != SV_BF16 && cfg->dtype != SV_FP8) return SV_ERR_ARG;
+  // the shape checks of spec_verify_create
+  if (cfg->V < 1 || cfg->V > INT32_MAX || cfg->d < 1 || cfg->d > (1 << 20) || cfg->B < 1 ||
+      cfg->B > SV_MAX_B || cfg->K < 0 || cfg->K > SV_MAX_K)
+    return SV_ERR_SHAPE;
+  if (cfg->d % (cfg->dtype == SV_BF16 ? 8 : 16) != 0) return SV_ERR_SHAPE;
+  const int64_t R = static_cast<int64_t>(cfg->B) * (cfg->K + 1);
+  if (R > SV_MAX_ROWS_BF16 || R * cfg->V > (int64_t(1) << 40)) return SV_ERR_SHAPE;
+  sv::Dims D{};
+  D.V = cfg->V;
+  D.d = cfg->d;
+  D.B = cfg->B;
+  D.K = cfg->K;
+  D.R = static_cast<int>(R);
+  D.RQ = cfg->B * cfg->K;
+  D.nsub = static_cast<int>((cfg->V + sv::kSub - 1) / sv::kSub);
+  D.ntile = static_cast<int>((cfg->V + sv::kTileM - 1) / sv::kTileM);
+  D.nchunk = static_cast<int>((cfg->V + sv::kChunk - 1) / sv::kChunk);
+  const sv::TcPlan pl = sv::plan_tc(D, num_sms, smem_optin, static_cast<int>(esize(cfg->dtype)));
+  if (!pl.valid || pl.smem > smem_optin) return SV_ERR_SHAPE;
+  sv_plan_t o{};
+  o.npad = pl.npad;
+  o.drain_cols = pl.ncol;
+  o.half = pl.half;
+  o.kblock_elems = pl.kbk;
+  o.kblocks = pl.nkb;
+  o.chunks = pl.chunks;
+  o.stages = pl.stages;
+  o.stage_bytes = pl.stage_bytes;
+  o.smem_bytes = pl.smem;
+  o.grid = pl.grid;
+  o.tmem_cols = static_cast<int32_t>(pl.tmem_cols);
+  o.tmem_buffers = pl.ncol != 0 ? 1 : pl.nbuf;
+  // drain mode: a ring of slots filling the allocation (powers of two)
+  o.tmem_slots = pl.ncol != 0 ? static_cast<int32_t>(pl.tmem_cols) / pl.ncol : pl.nslot;
+  *out = o;
+  return SV_OK;
+}
+
 const char *spec_verify_strerror(int code) {
   switch (code) {
     case SV_OK: return "ok";

@@ -156,3 +156,84 @@ def test_sweep_points_cover_the_batch_grid():
 def test_sweep_regime_follows_the_larger_fraction():
     assert bench.regime(0.9, 0.1) == "hbm"
     assert bench.regime(0.4, 0.7) == "tensor"
+
+
+SMEM_OPTIN = 232448   # opt-in shared memory per block on GB300
+TMEM_COLS = 512
+
+
+def _plans():
+    for dtype in ("bf16", "fp8"):
+        for V, d in ((128256, 4096), (128256, 8192), (1000, 960), (33, 256)):
+            if dtype == "fp8" and d % 16:
+                continue
+            for B in range(1, 65):
+                for K in range(0, 8):
+                    if B * (K + 1) > sv.SV_MAX_ROWS_BF16:
+                        continue
+                    yield dtype, V, d, B, K, sv.spec_verify_plan(V, d, B, K, dtype)
+
+
+def test_contraction_plan_fits_the_gpu_for_every_shape(lib):
+    n = 0
+    for dtype, V, d, B, K, p in _plans():
+        n += 1
+        R = B * (K + 1)
+        npad_all = (R + 15) // 16 * 16
+        where = (dtype, V, d, B, K, p)
+        # shared memory: at least two stages, within the opt-in limit
+        assert p["stages"] >= 2 and p["smem_bytes"] <= SMEM_OPTIN, where
+        assert p["stage_bytes"] % 1024 == 0, where
+        assert p["stages"] * p["stage_bytes"] < p["smem_bytes"], where
+        # k blocks: 128-byte rows, whole chunks per stage
+        assert p["kblock_elems"] * (1 if dtype == "fp8" else 2) == 128, where
+        assert p["kblocks"] == -(-d // p["kblock_elems"]) and p["kblocks"] % p["chunks"] == 0
+        # tensor memory: a power-of-two allocation holding every accumulator
+        cols = p["tmem_cols"]
+        assert 32 <= cols <= TMEM_COLS and cols & (cols - 1) == 0, where
+        if p["drain_cols"]:
+            # drain mode up to 64 columns: a ring of slots of its width
+            assert npad_all <= 64 and p["drain_cols"] >= npad_all and not p["half"], where
+            assert p["tmem_slots"] * p["drain_cols"] <= cols, where
+        else:
+            assert npad_all > 64, where
+            per_buf = TMEM_COLS // p["tmem_buffers"]
+            assert 1 <= p["tmem_slots"] <= 4 and p["tmem_slots"] <= p["kblocks"], where
+            assert p["tmem_slots"] * p["npad"] <= per_buf or p["npad"] > 256, where
+            # column halves only above 256 columns, on an even grid
+            assert p["half"] == (npad_all > 256), where
+            if p["half"]:
+                assert p["grid"] % 2 == 0 and 2 * p["npad"] >= npad_all, where
+                assert p["npad"] % 16 == 0 and p["npad"] <= 256, where
+            else:
+                assert p["npad"] == npad_all, where
+        # at most one CTA per SM, no more CTAs than work
+        ntile = -(-V // 128)
+        assert 1 <= p["grid"] <= 152 and p["grid"] <= (2 * ntile if p["half"] else ntile), where
+    assert n > 500
+
+
+def test_contraction_plan_of_the_benchmark_shapes(lib):
+    p = sv.spec_verify_plan(128256, 4096, 1, 4)
+    assert (p["drain_cols"], p["chunks"], p["stages"], p["grid"]) == (16, 2, 5, 152)
+    p = sv.spec_verify_plan(128256, 4096, 8, 7)
+    assert p["drain_cols"] == 64 and p["tmem_slots"] == 8
+    p = sv.spec_verify_plan(128256, 4096, 64, 5)
+    assert p["half"] == 1 and p["npad"] == 192 and p["tmem_buffers"] == 2
+    p = sv.spec_verify_plan(128256, 4096, 1, 4, "fp8")
+    assert p["kblock_elems"] == 128 and p["kblocks"] == 32
+
+
+def test_contraction_plan_rejects_what_create_rejects(lib):
+    cfg = sv.sv_config_t(128256, 4096, 65, 5, sv.SV_BF16, None)   # 390 rows
+    out = sv.sv_plan_t()
+    assert lib.spec_verify_plan(ctypes.byref(cfg), 152, SMEM_OPTIN, ctypes.byref(out)) == \
+        sv.SV_ERR_SHAPE
+    cfg = sv.sv_config_t(128256, 4096, 1, 4, sv.SV_FP32, None)
+    assert lib.spec_verify_plan(ctypes.byref(cfg), 152, SMEM_OPTIN, ctypes.byref(out)) == \
+        sv.SV_ERR_ARG
+    assert lib.spec_verify_plan(None, 152, SMEM_OPTIN, ctypes.byref(out)) == sv.SV_ERR_ARG
+    # a GPU with too little shared memory for two stages
+    cfg = sv.sv_config_t(128256, 4096, 1, 4, sv.SV_BF16, None)
+    assert lib.spec_verify_plan(ctypes.byref(cfg), 152, 48 * 1024, ctypes.byref(out)) == \
+        sv.SV_ERR_SHAPE
