@@ -67,10 +67,10 @@ def _load():
             lib.sv_oracle_softmax.restype = None
             lib.sv_oracle_verify.argtypes = [i64, i64, i32, i32, i32, vp, vp,
                                              vp, vp, vp, dbl, vp, vp, vp, vp,
-                                             vp, vp]
+                                             vp, vp, vp, vp]
             lib.sv_oracle_verify.restype = ctypes.c_int
             lib.sv_oracle_rule_batch.argtypes = [i64, i32, vp, vp, i64, vp,
-                                                 vp, vp, vp, vp]
+                                                 vp, vp, vp, vp, vp, vp]
             lib.sv_oracle_rule_batch.restype = ctypes.c_int
             lib.sv_oracle_emitted_law.argtypes = [i64, vp, vp, vp]
             lib.sv_oracle_emitted_law.restype = dbl
@@ -87,7 +87,7 @@ def _load():
                                                   vp, vp, vp]
             lib.sv_oracle_tree_greedy.restype = ctypes.c_int
             lib.sv_oracle_verify_fp8.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, vp,
-                                                 vp, dbl, vp, vp, vp, vp, vp, vp]
+                                                 vp, dbl, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.sv_oracle_verify_fp8.restype = ctypes.c_int
             lib.sv_oracle_e4m3_decode.argtypes = [i64, vp, vp]
             lib.sv_oracle_e4m3_decode.restype = None
@@ -158,8 +158,9 @@ def verify(hidden, W, draft, q_logits, uniforms, temperature: float,
     draft [B, K] int32; q_logits [B, K, V] float32, or None for drafts
     proposed with certainty (point-mass q; a -1 then ends a draft early);
     uniforms [B, K+1] float32.
-    Returns tokens [B, K+1], n_accepted [B], dist [B], lse_p, lse_q, status
-    and (optionally) fp64 logits [B*(K+1), V].
+    Returns tokens [B, K+1], n_accepted [B], dist [B] (with its two parts
+    dist_accept [B], over the accept tests, and dist_draw [B], for the final
+    draw), lse_p, lse_q, status and (optionally) fp64 logits [B*(K+1), V].
     """
     hidden, dt = _matrix(hidden)
     W, dt2 = _matrix(W)
@@ -175,23 +176,29 @@ def verify(hidden, W, draft, q_logits, uniforms, temperature: float,
     tokens = np.empty((B, rows), dtype=np.int32)
     n_acc = np.empty((B,), dtype=np.int32)
     dist = np.empty((B,), dtype=np.float64)
+    dacc = np.empty((B,), dtype=np.float64)
+    ddraw = np.empty((B,), dtype=np.float64)
     lg = np.empty((B * rows, V), dtype=np.float64) if want_logits else None
     lse_p = np.full((B * rows,), np.nan)
     lse_q = np.full((max(B * K, 1),), np.nan)
     rc = _load().sv_oracle_verify(V, d, B, K, dt, _ptr(hidden), _ptr(W),
                                   _ptr(draft), _ptr(q), _ptr(u), T,
                                   _ptr(tokens), _ptr(n_acc), _ptr(dist),
-                                  _ptr(lg), _ptr(lse_p), _ptr(lse_q))
+                                  _ptr(lg), _ptr(lse_p), _ptr(lse_q),
+                                  _ptr(dacc), _ptr(ddraw))
     if rc not in (OK, ETOKEN):
         raise ValueError(f"sv_oracle_verify failed ({rc})")
-    return {"tokens": tokens, "n_accepted": n_acc, "dist": dist,
-            "logits": lg, "lse_p": lse_p, "lse_q": lse_q[:B * K], "status": rc}
+    return {"tokens": tokens, "n_accepted": n_acc, "dist": dist, "dist_accept": dacc,
+            "dist_draw": ddraw, "logits": lg, "lse_p": lse_p, "lse_q": lse_q[:B * K],
+            "status": rc}
 
 
-def rule_batch(p, q, x, u):
+def rule_batch(p, q, x, u, split: bool = False):
     """The accept / residual / bonus rule for n independent rounds that
     share p [K+1, V] and q [K, V] (probabilities; None for point-mass
-    drafts, where a -1 ends a draft early); x [n, K], u [n, K+1]."""
+    drafts, where a -1 ends a draft early); x [n, K], u [n, K+1].
+    Returns (tokens, n_accepted, dist), and with split=True also the two
+    parts of dist (accept tests, final draw)."""
     p = _c(p, np.float64)
     K1, V = p.shape
     K = K1 - 1
@@ -203,11 +210,15 @@ def rule_batch(p, q, x, u):
     tokens = np.empty((n, K1), dtype=np.int32)
     n_acc = np.empty((n,), dtype=np.int32)
     dist = np.empty((n,), dtype=np.float64)
+    dacc = np.empty((n,), dtype=np.float64)
+    ddraw = np.empty((n,), dtype=np.float64)
     rc = _load().sv_oracle_rule_batch(V, K, _ptr(p), _ptr(q), n, _ptr(x),
                                       _ptr(u), _ptr(tokens), _ptr(n_acc),
-                                      _ptr(dist))
+                                      _ptr(dist), _ptr(dacc), _ptr(ddraw))
     if rc not in (OK, ETOKEN):
         raise ValueError(f"sv_oracle_rule_batch failed ({rc})")
+    if split:
+        return tokens, n_acc, dist, dacc, ddraw
     return tokens, n_acc, dist
 
 
@@ -358,14 +369,17 @@ def verify_fp8(hidden8, hscale, W8, wscale, draft, q_logits, uniforms, temperatu
     tokens = np.empty((B, rows), dtype=np.int32)
     n_acc = np.empty((B,), dtype=np.int32)
     dist = np.empty((B,), dtype=np.float64)
+    dacc = np.empty((B,), dtype=np.float64)
+    ddraw = np.empty((B,), dtype=np.float64)
     lg = np.empty((B * rows, V), dtype=np.float64) if want_logits else None
     lse_p = np.full((B * rows,), np.nan)
     lse_q = np.full((max(B * K, 1),), np.nan)
     rc = _load().sv_oracle_verify_fp8(V, d, B, K, _ptr(hidden8), _ptr(hscale), _ptr(W8),
                                       _ptr(wscale), _ptr(draft), _ptr(q), _ptr(u), T,
                                       _ptr(tokens), _ptr(n_acc), _ptr(dist), _ptr(lg),
-                                      _ptr(lse_p), _ptr(lse_q))
+                                      _ptr(lse_p), _ptr(lse_q), _ptr(dacc), _ptr(ddraw))
     if rc not in (OK, ETOKEN):
         raise ValueError(f"sv_oracle_verify_fp8 failed ({rc})")
-    return {"tokens": tokens, "n_accepted": n_acc, "dist": dist, "logits": lg,
-            "lse_p": lse_p, "lse_q": lse_q[:B * K], "status": rc}
+    return {"tokens": tokens, "n_accepted": n_acc, "dist": dist, "dist_accept": dacc,
+            "dist_draw": ddraw, "logits": lg, "lse_p": lse_p, "lse_q": lse_q[:B * K],
+            "status": rc}

@@ -239,7 +239,11 @@ static int32_t inverse_cdf(int64_t V, const double *w, double S, double u,
  * the number of accepted draft tokens, or SV_ORACLE_ETOKEN.
  * *dist = the smallest distance between a uniform and the threshold of a
  * decision this round actually took (accept tests use |u - t|, the final
- * draw its inverse-CDF interval edges).
+ * draw its inverse-CDF interval edges); the two parts are also returned
+ * apart: *dist_accept over the accept tests only (INFINITY if none ran) and
+ * *dist_draw for the final draw, so that a caller can tell a uniform close
+ * to one of the K thresholds p/q from one close to one of the V edges of
+ * the final draw's CDF.
  * `scratch` must hold V doubles.
  * ---------------------------------------------------------------------- */
 /* Number of proposed tokens of a draft x[0..K-1] (R7, R9): K if every id
@@ -261,9 +265,12 @@ static int32_t draft_length(int64_t V, int32_t K, const int32_t *x, int point_ma
 static int32_t rule_one_sequence(int64_t V, int32_t K, const double *p,
                                  const double *q, const int32_t *x,
                                  const double *u, int32_t *tokens,
-                                 double *dist, double *scratch) {
+                                 double *dist, double *dist_accept,
+                                 double *dist_draw, double *scratch) {
   double best = INFINITY;
   for (int32_t i = 0; i <= K; ++i) tokens[i] = -1;
+  *dist_accept = INFINITY;
+  *dist_draw = INFINITY;
   /* q == NULL: the draft was proposed with certainty (R8, R9) */
   const int32_t kb = draft_length(V, K, x, q == NULL);
   if (kb < 0) {
@@ -316,7 +323,9 @@ static int32_t rule_one_sequence(int64_t V, int32_t K, const double *p,
       S += pj[v];
     }
   }
+  *dist_accept = best; /* the accept tests only */
   tok = inverse_cdf(V, scratch, S, uf, &dfinal);
+  *dist_draw = dfinal;
   if (dfinal < best) best = dfinal;
   tokens[j] = tok;
   *dist = best;
@@ -373,6 +382,9 @@ static int32_t greedy_one_sequence(int64_t V, int32_t K, const double *L,
  * Optional outputs (may be NULL):
  *   dist   [B]            threshold distance (probability units when T > 0,
  *                         logit gap when T == 0)
+ *   dist_accept [B]       the same over the accept tests only (T == 0: the
+ *                         logit gap; INFINITY if no test ran)
+ *   dist_draw   [B]       the same for the final draw only (T == 0: INFINITY)
  *   logits [B*(K+1), V]   fp64 logits
  *   lse_p  [B*(K+1)]      log-sum-exp of logits / T   (T > 0)
  *   lse_q  [B*K]          log-sum-exp of q_logits / T (T > 0)
@@ -384,16 +396,18 @@ static int verify_impl(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype
                        const void *hidden, const float *hscale, const void *W,
                        const float *wscale, const int32_t *draft, const float *q_logits,
                        const float *u, double T, int32_t *out_tokens, int32_t *out_n,
-                       double *dist, double *logits, double *lse_p, double *lse_q);
+                       double *dist, double *logits, double *lse_p, double *lse_q,
+                       double *dist_accept, double *dist_draw);
 
 int sv_oracle_verify(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
                      const void *hidden, const void *W, const int32_t *draft,
                      const float *q_logits, const float *u, double T,
                      int32_t *out_tokens, int32_t *out_n, double *dist,
-                     double *logits, double *lse_p, double *lse_q) {
+                     double *logits, double *lse_p, double *lse_q,
+                     double *dist_accept, double *dist_draw) {
   if (dtype != 0 && dtype != 1) return SV_ORACLE_EARG;
   return verify_impl(V, d, B, K, dtype, hidden, NULL, W, NULL, draft, q_logits, u, T,
-                     out_tokens, out_n, dist, logits, lse_p, lse_q);
+                     out_tokens, out_n, dist, logits, lse_p, lse_q, dist_accept, dist_draw);
 }
 
 /* The step with an FP8 LM head (R13): hidden8 [B, K+1, d] and W8 [V, d]
@@ -403,17 +417,19 @@ int sv_oracle_verify_fp8(int64_t V, int64_t d, int32_t B, int32_t K, const void 
                          const float *hscale, const void *W8, const float *wscale,
                          const int32_t *draft, const float *q_logits, const float *u,
                          double T, int32_t *out_tokens, int32_t *out_n, double *dist,
-                         double *logits, double *lse_p, double *lse_q) {
+                         double *logits, double *lse_p, double *lse_q,
+                         double *dist_accept, double *dist_draw) {
   if (!hscale || !wscale) return SV_ORACLE_EARG;
   return verify_impl(V, d, B, K, 2, hidden8, hscale, W8, wscale, draft, q_logits, u, T,
-                     out_tokens, out_n, dist, logits, lse_p, lse_q);
+                     out_tokens, out_n, dist, logits, lse_p, lse_q, dist_accept, dist_draw);
 }
 
 static int verify_impl(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
                        const void *hidden, const float *hscale, const void *W,
                        const float *wscale, const int32_t *draft, const float *q_logits,
                        const float *u, double T, int32_t *out_tokens, int32_t *out_n,
-                       double *dist, double *logits, double *lse_p, double *lse_q) {
+                       double *dist, double *logits, double *lse_p, double *lse_q,
+                       double *dist_accept, double *dist_draw) {
   if (V < 1 || d < 1 || B < 1 || K < 0 || dtype < 0 || dtype > 2 ||
       !hidden || !W || !out_tokens || !out_n || !(T >= 0.0) || T == INFINITY)
     return SV_ORACLE_EARG;
@@ -447,10 +463,12 @@ static int verify_impl(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype
              sizeof(double) * (size_t)(rows * V));
     const int32_t *xb = K > 0 ? draft + (int64_t)b * K : NULL;
     int32_t *tb = out_tokens + (int64_t)b * rows;
-    double dd;
+    double dd, da, dw;
     int32_t n;
     if (T == 0.0) {
       n = greedy_one_sequence(V, K, L, xb, point_mass, tb, &dd);
+      da = dd;
+      dw = INFINITY;
     } else {
       for (int64_t i = 0; i < rows; ++i) {
         const double lse = sv_oracle_lse(V, L + i * V, T);
@@ -465,7 +483,8 @@ static int verify_impl(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype
         for (int64_t v = 0; v < V; ++v) q[i * V + v] = exp(qrow[v] / T - lse);
       }
       for (int64_t i = 0; i < rows; ++i) ud[i] = (double)u[(int64_t)b * rows + i];
-      n = rule_one_sequence(V, K, p, point_mass ? NULL : q, xb, ud, tb, &dd, scratch);
+      n = rule_one_sequence(V, K, p, point_mass ? NULL : q, xb, ud, tb, &dd, &da, &dw,
+                            scratch);
     }
     if (n == SV_ORACLE_ETOKEN) {
       status = SV_ORACLE_ETOKEN;
@@ -475,6 +494,8 @@ static int verify_impl(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype
       out_n[b] = n;
     }
     if (dist) dist[b] = dd;
+    if (dist_accept) dist_accept[b] = da;
+    if (dist_draw) dist_draw[b] = dw;
   }
   free(L); free(p); free(q); free(qrow); free(scratch); free(ud);
   return status;
@@ -486,11 +507,13 @@ static int verify_impl(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype
  * the math honestly", [P3] three-token example):
  *   p [K+1, V], q [K, V] probabilities (q == NULL: point-mass drafts, R8,
  *   R9); x [n, K]; u [n, K+1]
- * Outputs tokens [n, K+1], n_accepted [n], dist [n] (may be NULL).
+ * Outputs tokens [n, K+1], n_accepted [n], dist [n], and its parts
+ * dist_accept [n] and dist_draw [n] (each may be NULL).
  * ---------------------------------------------------------------------- */
 int sv_oracle_rule_batch(int64_t V, int32_t K, const double *p, const double *q,
                          int64_t n, const int32_t *x, const double *u,
-                         int32_t *out_tokens, int32_t *out_n, double *dist) {
+                         int32_t *out_tokens, int32_t *out_n, double *dist,
+                         double *dist_accept, double *dist_draw) {
   if (V < 1 || K < 0 || n < 0 || !p || (K > 0 && !x) || !u ||
       !out_tokens || !out_n)
     return SV_ORACLE_EARG;
@@ -498,10 +521,10 @@ int sv_oracle_rule_batch(int64_t V, int32_t K, const double *p, const double *q,
   if (!scratch) return SV_ORACLE_ENOMEM;
   int status = SV_ORACLE_OK;
   for (int64_t r = 0; r < n; ++r) {
-    double dd;
+    double dd, da, dw;
     int32_t *tr = out_tokens + r * (K + 1);
     int32_t k = rule_one_sequence(V, K, p, q, K > 0 ? x + r * K : NULL,
-                                  u + r * (K + 1), tr, &dd, scratch);
+                                  u + r * (K + 1), tr, &dd, &da, &dw, scratch);
     if (k == SV_ORACLE_ETOKEN) {
       status = SV_ORACLE_ETOKEN;
       out_n[r] = -1;
@@ -509,6 +532,8 @@ int sv_oracle_rule_batch(int64_t V, int32_t K, const double *p, const double *q,
       out_n[r] = k;
     }
     if (dist) dist[r] = dd;
+    if (dist_accept) dist_accept[r] = da;
+    if (dist_draw) dist_draw[r] = dw;
   }
   free(scratch);
   return status;
@@ -718,7 +743,7 @@ int sv_oracle_verify_truncated(int64_t V, int64_t d, int32_t B, int32_t K, int32
                                double *trunc_sens, double *trunc_xgap) {
   if (T == 0.0)
     return sv_oracle_verify(V, d, B, K, dtype, hidden, W, draft, q_logits, u, T, out_tokens,
-                            out_n, dist, NULL, NULL, NULL);
+                            out_n, dist, NULL, NULL, NULL, NULL, NULL);
   if (V < 1 || d < 1 || B < 1 || K < 0 || (dtype != 0 && dtype != 1) || !hidden || !W ||
       !out_tokens || !out_n || !(T > 0.0) || T == INFINITY || !u || (K > 0 && !draft) ||
       p_top_k < 0 || q_top_k < 0 || !(p_top_p > 0.0) || p_top_p > 1.0 ||
@@ -776,9 +801,9 @@ int sv_oracle_verify_truncated(int64_t V, int64_t d, int32_t B, int32_t K, int32
     for (int64_t i = 0; i < rows; ++i) ud[i] = (double)u[(int64_t)b * rows + i];
     const int32_t *xb = K > 0 ? draft + (int64_t)b * K : NULL;
     int32_t *tb = out_tokens + (int64_t)b * rows;
-    double dd;
+    double dd, da, dw;
     const int32_t n = rule_one_sequence(V, K, p, point_mass ? NULL : q, xb, ud, tb, &dd,
-                                        scratch);
+                                        &da, &dw, scratch);
     if (n == SV_ORACLE_ETOKEN) {
       status = SV_ORACLE_ETOKEN;
       for (int64_t i = 0; i < rows; ++i) tb[i] = -1;

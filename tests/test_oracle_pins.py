@@ -350,6 +350,29 @@ def test_strict_accept_test_and_threshold_distance():
     assert abs(dist[1] - 1e-4) < 1e-12
 
 
+def test_threshold_distance_parts():
+    # The round's distance splits into its accept tests (|u_i - p/q|) and its
+    # final draw (the chosen token's CDF interval edges).  Two-token p, q:
+    # t = p(0)/q(0) = 0.5 for draft token 0; the bonus is drawn from p with
+    # edges 0, 0.5, 1; after a rejection the residual max(0, p - q) = (0, 0.5)
+    # normalises to (0, 1), edges 0 and 1.
+    P, Q = np.array([0.5, 0.5]), np.array([1.0, 0.0])
+    u = np.array([[0.4999, 0.2],          # accepted 1e-4 below t; bonus 0.2 into [0, 0.5)
+                  [0.3, 0.5 + 3e-7],      # accepted; bonus 3e-7 above the edge at 0.5
+                  [0.9, 0.75]])           # rejected 0.4 above t; residual draw at 0.75
+    tokens, n_acc, dist, dacc, ddraw = oracle.rule_batch(
+        np.stack([P, P]), Q[None, :], np.zeros((3, 1), np.int32), u, split=True)
+    assert list(n_acc) == [1, 1, 0]
+    assert tokens.tolist() == [[0, 0], [0, 1], [1, -1]]
+    np.testing.assert_allclose(dacc, [1e-4, 0.2, 0.4], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ddraw, [0.2, 3e-7, 0.25], rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(dist, np.minimum(dacc, ddraw))
+    # no accept test at all (K = 0): only the draw counts
+    _, _, dist0, dacc0, ddraw0 = oracle.rule_batch(P[None, :], None, np.zeros((1, 0), np.int32),
+                                                   np.array([[0.7]]), split=True)
+    assert dacc0[0] == np.inf and abs(ddraw0[0] - 0.2) < 1e-12 and dist0[0] == ddraw0[0]
+
+
 def test_zero_residual_falls_back_to_p():
     # p <= q everywhere with a rejection: the residual is empty, the
     # replacement is drawn from p itself (the zero-residual fallback)
