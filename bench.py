@@ -285,6 +285,76 @@ def oracle_rate(wl, W_np, inputs, budget_s, w_scale=None):
                        f"({frac:.3f} of a round), scaled to one round"), frac
 
 
+def host_cpu():
+    """CPU model and logical core count of the host running the oracle."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        import platform
+        model = platform.processor() or platform.machine()
+    return {"cpu_model": model, "nproc": os.cpu_count()}
+
+
+def parity_sample(wl, W_np, sets, out_tok, out_n, ran, T, w_scale=None, max_sets=32):
+    """The oracle on up to max_sets of the rounds this run timed, in parallel
+    on the host's cores (one round per thread).  Returns the rounds' parity
+    against the GPU's outputs with the flagged rounds (a uniform within 1e-6
+    of an accept threshold, or of an edge of the final draw's CDF) and the
+    oracle's all-core rate."""
+    import concurrent.futures
+    import numpy as np
+    import oracle
+    import spec_inputs as si
+    idx = list(ran)[:max(1, min(max_sets, 2 * (os.cpu_count() or 1)))]
+    host = []
+    for i in idx:
+        s = sets[i]
+        h = {k: si.to_oracle(s[k]) for k in ("draft", "q_logits", "uniforms")}
+        if w_scale is not None:
+            h["hidden8"], h["h_scale"] = si.to_oracle(s["hidden8"]), si.to_oracle(s["h_scale"])
+        else:
+            h["hidden"] = si.to_oracle(s["hidden"])
+        host.append(h)
+    ws = None if w_scale is None else si.to_oracle(w_scale)
+
+    def one(h):
+        if ws is not None:
+            return oracle.verify_fp8(h["hidden8"], h["h_scale"], W_np, ws, h["draft"],
+                                     h["q_logits"], h["uniforms"], T)
+        return oracle.verify(h["hidden"], W_np, h["draft"], h["q_logits"], h["uniforms"], T)
+
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+        refs = list(ex.map(one, host))
+    el = time.perf_counter() - t0
+    band = 1e-6 if T > 0 else 1e-7
+    rounds = mism = unflagged = fa = fd = 0
+    for i, ref in zip(idx, refs):
+        gt, gn = out_tok[i].cpu().numpy(), out_n[i].cpu().numpy()
+        bad = np.any(gt != ref["tokens"], axis=1) | (gn != ref["n_accepted"])
+        flag = ref["dist"] <= band
+        rounds += len(gn)
+        mism += int(bad.sum())
+        unflagged += int((bad & ~flag).sum())
+        fa += int((ref["dist_accept"] <= band).sum())
+        fd += int((ref["dist_draw"] <= band).sum())
+    parity = {"rounds": rounds, "mismatched_rounds": mism, "unflagged_mismatches": unflagged,
+              "flagged_accept": fa, "flagged_draw": fd, "flag_band": band,
+              "note": "sample of this run's timed rounds; the large-sample rates come from "
+                      "the parity tests"}
+    all_cores = {"value": len(idx) / el, "unit": UNIT, "threads": threads,
+                 "sample": f"{len(idx)} full oracle rounds, one per thread"}
+    return parity, all_cores
+
+
 def reference_arm(args, wl, dev):
     import torch
     import spec_inputs as si
@@ -325,8 +395,8 @@ def reference_arm(args, wl, dev):
             "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(wl),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": dict({"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                  "sample": sample}, **host_cpu()),
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -470,7 +540,6 @@ def main():
     ap.add_argument("--top-p", type=float, default=1.0)
     ap.add_argument("--tree", action="store_true")
     ap.add_argument("--fp8", action="store_true")
-    ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--clock-log", default=None)
     ap.add_argument("--sweep", action="store_true")
@@ -580,32 +649,8 @@ def main():
     truncated = T > 0 and (0 < args.top_k < wl.V or args.top_p < 1.0)
     launches_per_run = (sv.spec_verify_launches_per_run(eng.h, T) + (1 if ngram else 0)
                         + (1 if truncated else 0))
-    # warm-up (also the first use of every input set)
-    with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, nsets)):
-            run_set(i % nsets)
-    stream.synchronize()
-    code = eng.status()
-    if code != sv.SV_OK:
-        raise RuntimeError(f"device status after warm-up: {sv.spec_verify_strerror(code)}")
-
-    graph = None
-    if not args.no_graph:
-        try:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                for i in range(nsets):
-                    run_set(i)
-            stream.synchronize()
-            with torch.cuda.stream(stream):
-                graph.replay()
-            stream.synchronize()
-        except Exception as exc:  # capture unsupported: launch directly
-            print(f"[bench] graph capture failed ({exc}); direct launches", file=sys.stderr)
-            graph = None
-    reps = max(1, round(args.steps / nsets)) if graph is not None else 0
-    steps = reps * nsets if graph is not None else args.steps
-
+    # the clocks are sampled from before the warm-up to after the kernel
+    # timing pass, so that a short timed region still has samples around it
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -613,34 +658,57 @@ def main():
         uuid = None
     sampler = ClockSampler(args.clock_log)
     sampler.start(uuid)
-    time.sleep(0.4)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    time.sleep(0.3)
+
+    # warm-up: exactly args.warmup untimed rounds, cycling through the sets
+    used = set()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            run_set(i % nsets)
+            used.add(i % nsets)
+    stream.synchronize()
+    code = eng.status()
+    if code != sv.SV_OK:
+        raise RuntimeError(f"device status after warm-up: {sv.spec_verify_strerror(code)}")
+
+    # timed: exactly args.steps rounds (the sets after the warm-up's, so a
+    # round does not find its inputs in L2), in up to five contiguous
+    # windows whose rates give the median and spread
+    steps = args.steps
+    nwin = min(5, steps)
+    bounds = [steps * w // nwin for w in range(nwin + 1)]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nwin + 1)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        e0.record(stream)
-        if graph is not None:
-            for _ in range(reps):
-                graph.replay()
-        else:
-            for i in range(steps):
-                run_set(i % nsets)
-        e1.record(stream)
+        evs[0].record(stream)
+        for w in range(nwin):
+            for i in range(bounds[w], bounds[w + 1]):
+                j = (args.warmup + i) % nsets
+                run_set(j)
+                used.add(j)
+            evs[w + 1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    elapsed = e0.elapsed_time(e1) / 1e3
-    clocks = sampler.stop()
+    elapsed = evs[0].elapsed_time(evs[-1]) / 1e3
+    win_rates = [(bounds[w + 1] - bounds[w]) / (evs[w].elapsed_time(evs[w + 1]) / 1e3)
+                 for w in range(nwin)]
     code = eng.status()
     if code != sv.SV_OK:
         raise RuntimeError(f"device status after timing: {sv.spec_verify_strerror(code)}")
     max_el, total_rounds = aggregate(elapsed, steps)
     value = total_rounds / max_el
+    windows = {"windows": nwin, "rounds_per_window": [bounds[w + 1] - bounds[w]
+                                                      for w in range(nwin)],
+               "median_rounds_per_s": statistics.median(win_rates),
+               "min_rounds_per_s": min(win_rates), "max_rounds_per_s": max(win_rates),
+               "note": "rank-local windows of the one timed region"}
 
     # emitted tokens per round over the input sets
-    n_host = torch.stack(out_n).cpu().numpy()   # [sets, B]
+    ran = sorted(used)
+    n_host = torch.stack([out_n[i] for i in ran]).cpu().numpy()   # [sets run, B]
     tokens_per_round = float((n_host + 1).sum(axis=1).mean())
 
     # contraction kernel timing (CUDA events on the launching stream)
@@ -651,6 +719,7 @@ def main():
             run_set(i % nsets)
     ms_k1, n_k1 = sv.spec_verify_timing_read(eng.h)
     sv.spec_verify_timing(eng.h, False)
+    clocks = sampler.stop()
     k1_s = ms_k1 / 1e3 / n_k1
     peaks, peak_src = measured_peaks()
     k1_bytes = contraction_bytes(wl.V, wl.d, wl.B, wl.K, greedy=T == 0, point_mass=ngram,
@@ -759,16 +828,24 @@ def main():
     d2h = ht.numel() * 4 + hn.numel() * 4
 
     cpu = None
+    parity = None
     if rank == 0:
         W_np = si.to_oracle(W)
         rate, sample, _ = oracle_rate(wl, W_np, sets[0], args.cpu_budget,
                                       w_scale=w_scale if fp8 else None)
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+        cpu.update(host_cpu())
+        if not (ngram or truncated or args.tree):
+            # the oracle on a sample of this run's own rounds, one round per
+            # host thread: the rounds' parity and flags, and an all-core rate
+            parity, all_cores = parity_sample(wl, W_np, sets, out_tok, out_n, ran, T,
+                                              w_scale if fp8 else None)
+            cpu["all_cores"] = all_cores
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": steps, "warmup": max(args.warmup, nsets),
+            "steps": steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * max_el / steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 (fp32 accumulate)" if fp8 else "bf16",
@@ -776,7 +853,7 @@ def main():
             "config": workload_config(wl, {
                 "l2": f"inputs larger than L2: W_lm {2 * wl.V * wl.d} B per round plus "
                       f"{nsets} rotating input sets ({nsets * set_bytes} B)",
-                "graph": graph is not None,
+                "launch": "direct launches on one stream (programmatic dependent launch)",
                 "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
                 drafts=args.drafts, top_k=args.top_k, top_p=args.top_p, tree=args.tree,
                 fp8=fp8),
@@ -784,6 +861,8 @@ def main():
             "emitted_tokens_per_s": value * tokens_per_round,
             "roofline": roofline,
             "cpu_baseline": cpu,
+            "timed_windows": windows,
+            "parity_sample": parity,
             "e2e": {"value": e2e_total / e2e_max, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_run * steps,

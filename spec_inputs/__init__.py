@@ -166,6 +166,36 @@ def make_round(wl: Workload, W: torch.Tensor, seed: int, device=None,
             "uniforms": uniforms, "sigma": sigmas}
 
 
+def draw_drafts(q_logits: torch.Tensor, T: float, n: int, seed: int) -> torch.Tensor:
+    """n more draft proposals for the same draft logits q_logits [B, K, V]:
+    each x_i drawn from softmax(q_logits_i / T) by the Gumbel-max trick (the
+    draft model's own sampling, as in make_round; argmax at T == 0).
+    Returns int32 [n, B, K]."""
+    g = _gen(seed, q_logits.device)
+    B, K, V = q_logits.shape
+    out = torch.empty((n, B, K), dtype=torch.int32, device=q_logits.device)
+    if K == 0:
+        return out
+    scaled = q_logits / T if T > 0 else q_logits
+    chunk = max(1, (1 << 27) // max(1, B * K * V))   # ~0.5 GB of noise at a time
+    for i0 in range(0, n, chunk):
+        m = min(chunk, n - i0)
+        if T > 0:
+            gum = torch.rand((m, B, K, V), generator=g, device=q_logits.device).clamp_min(1e-30)
+            out[i0:i0 + m] = torch.argmax(scaled.unsqueeze(0) - torch.log(-torch.log(gum)),
+                                          dim=-1).to(torch.int32)
+        else:
+            out[i0:i0 + m] = torch.argmax(scaled, dim=-1).to(torch.int32).unsqueeze(0)
+    return out
+
+
+def draw_uniforms(n: int, B: int, K: int, seed: int, device="cpu") -> torch.Tensor:
+    """n more sets of uniforms [n, B, K+1] on the 2^-24 grid (exact fp32)."""
+    g = _gen(seed, device)
+    return (torch.randint(0, 1 << 24, (n, B, K + 1), generator=g, device=device)
+            .to(torch.float32) * (2.0 ** -24)).contiguous()
+
+
 def to_oracle(t: torch.Tensor):
     """Host numpy view for the oracle: bf16 as uint16 bit patterns."""
     t = t.detach().cpu().contiguous()

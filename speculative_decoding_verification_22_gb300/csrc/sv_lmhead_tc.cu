@@ -29,6 +29,8 @@
 //    fp32 logits with a TMA store, and computes the per-32-entry (max,
 //    sum-exp) partials of logits / T (or the max for T == 0); four more
 //    warps stream the draft logits q / T of the tile for the same partials.
+#include <atomic>
+
 #include "sv_internal.cuh"
 #include "sv_kernels.h"
 
@@ -821,7 +823,12 @@ TcPlan plan_tc(const Dims &dims, int num_sms, int smem_optin, int elt) {
   return pl;
 }
 
-static int g_attr_smem[4] = {0, 0, 0, 0};
+// Dynamic shared memory each kernel variant has been opted in to, per
+// device (the attribute is a per-device setting).  Atomics: handles on
+// several host threads may launch at once; two threads that both raise the
+// attribute set the same value.
+constexpr int kAttrDevices = 64;
+static std::atomic<int> g_attr_smem[kAttrDevices][4];
 
 cudaError_t launch_tc(const TcPlan &pl, const TcParams &P, const CUtensorMap &tmW,
                       const CUtensorMap &tmH, const CUtensorMap &tmL, cudaStream_t stream) {
@@ -833,10 +840,18 @@ cudaError_t launch_tc(const TcPlan &pl, const TcParams &P, const CUtensorMap &tm
     case 64: fn = reinterpret_cast<const void *>(&tc::lmhead_tc_kernel<64>); which = 2; break;
     default: fn = reinterpret_cast<const void *>(&tc::lmhead_tc_kernel<0>); which = 3; break;
   }
-  if (g_attr_smem[which] < pl.smem) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::atomic<int> *done = dev < kAttrDevices ? &g_attr_smem[dev][which] : nullptr;
+  if (!done || done->load(std::memory_order_acquire) < pl.smem) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
     if (e != cudaSuccess) return e;
-    g_attr_smem[which] = pl.smem;
+    if (done) {
+      int cur = done->load(std::memory_order_relaxed);
+      while (cur < pl.smem && !done->compare_exchange_weak(cur, pl.smem)) {
+      }
+    }
   }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -62,18 +62,25 @@ struct Carver {
   }
 };
 
-int encode_w_local(CUtensorMap *map, const void *ptr, int64_t inner, int64_t outer,
-                   uint32_t box_rows, int chunks) {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+// cuTensorMapEncodeTiled from the driver, looked up once per process (a
+// function-local static: its initialisation is thread-safe).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_local() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void *p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess)
-      return SV_ERR_CUDA;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+int encode_w_local(CUtensorMap *map, const void *ptr, int64_t inner, int64_t outer,
+                   uint32_t box_rows, int chunks) {
+  const auto fn = encode_fn_local();
+  if (!fn) return SV_ERR_CUDA;
   CUresult r;
   if (chunks > 1) {  // same 3-D view as the handle path
     cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(outer), static_cast<cuuint64_t>(inner / 64)};
@@ -97,13 +104,8 @@ int encode_w_local(CUtensorMap *map, const void *ptr, int64_t inner, int64_t out
 
 // TMA store map of the fp32 logits scratch (same box as the handle path).
 int encode_logits_local(CUtensorMap *map, float *base, int64_t V, int64_t R) {
-  void *p = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                       &q) != cudaSuccess ||
-      q != cudaDriverEntryPointSuccess)
-    return SV_ERR_CUDA;
-  auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  const auto fn = encode_fn_local();
+  if (!fn) return SV_ERR_CUDA;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(R)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 4};
   cuuint32_t box[2] = {32, 16};

@@ -38,7 +38,7 @@ def oracle_verify(hidden, W_np, draft, q_logits, uniforms, T, want_logits=False,
 
     res = list(_POOL.map(one, seqs))
     out = {k: np.concatenate([r[k] for r in res]) for k in
-           ("tokens", "n_accepted", "dist", "lse_p")}
+           ("tokens", "n_accepted", "dist", "dist_accept", "dist_draw", "lse_p")}
     out["lse_q"] = np.concatenate([r["lse_q"] for r in res])
     if want_logits:
         out["logits"] = np.concatenate([r["logits"] for r in res])

@@ -1,0 +1,252 @@
+"""Parity at scale: the CUDA path against the oracle over 10^4..10^5 rounds
+per configuration, with the flagged rounds counted and reported.
+
+The comparison rule ("Speculative Decoding: Two Models, One Voice", "The
+idea", step 3; "Speculative Decoding: Guess Several Tokens, Check Them in
+One Pass", Step 3): token ids and accept counts must equal the oracle's in
+every round, except rounds in which a uniform lies within 1e-6 of a
+threshold it was compared with.  The oracle reports that distance in two
+parts:
+
+* dist_accept -- the K accept tests, u_i against p_i(x)/q_i(x).  A test
+  whose uniform is independent of its threshold is flagged with
+  probability at most 2e-6 (the uniforms sit on the 2^-24 grid), so the
+  expected flagged rate is at most 2e-6 times the mean number of tests a
+  round takes: below 1e-5 whenever a round takes fewer than five tests on
+  average.  Both the bound and the measured count are checked.
+* dist_draw -- the final inverse-CDF draw, u against the V edges of the
+  CDF.  The fraction of [0, 1) within 1e-6 of one of them is
+  sum_v min(w_v, 2e-6): about 2e-3 at V = 1000 and 0.2 at V = 128256.
+  These rounds are counted and reported; a mismatch must fall in one.
+
+Each configuration runs `nsets` input sets (own hidden states, draft logits,
+drafts, uniforms: a full oracle round each, with logits and normalisers
+compared) and, per set, `nvar` more rounds on the same hidden states and
+draft logits with fresh draft tokens (drawn from q) and uniforms, which the
+oracle's rule decides from its own fp64 p and q of that set.
+
+SV_PARITY_REPORT=<path> appends one JSON line per configuration.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import spec_inputs as si
+import speculative_decoding_verification_22_gb300 as sv
+from gpu_common import _POOL, FLAG_GREEDY, FLAG_SAMPLED
+
+pytestmark = pytest.mark.gpu
+
+ACCEPT_RATE_BOUND = 1e-5
+
+
+def _report(rec):
+    line = json.dumps(rec, sort_keys=True)
+    print(line)
+    path = os.environ.get("SV_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(line + "\n")
+
+
+def _pad4(n):
+    return (n + 3) // 4 * 4
+
+
+def _poisson_upper(mean, p=1e-3):
+    """Smallest c with P(Poisson(mean) > c) < p."""
+    c, term, cdf = 0, math.exp(-mean), math.exp(-mean)
+    while 1.0 - cdf >= p:
+        c += 1
+        term *= mean / c
+        cdf += term
+    return c
+
+
+class Tally:
+    def __init__(self, T):
+        self.T = T
+        self.rounds = self.mismatch = self.unflagged_mismatch = 0
+        self.flag_accept = self.flag_draw = self.flag_any = 0
+        self.tests = 0
+        self.worst_mismatch_dist = 0.0
+        self.max_dlse_p = self.max_dlse_q = self.max_dlogit = 0.0
+
+    def add(self, gt, gn, rt, rn, dist, dacc, ddraw, K):
+        band = FLAG_SAMPLED if self.T > 0 else FLAG_GREEDY
+        mism = np.any(gt != rt, axis=1) | (gn != rn)
+        flag = dist <= band
+        self.rounds += len(rn)
+        self.mismatch += int(mism.sum())
+        self.unflagged_mismatch += int((mism & ~flag).sum())
+        self.flag_any += int(flag.sum())
+        self.flag_accept += int((dacc <= band).sum())
+        self.flag_draw += int((ddraw <= band).sum())
+        # accept tests taken: the accepted ones, plus the rejecting one
+        self.tests += int(np.where(rn < K, rn + 1, rn).sum())
+        if mism.any():
+            self.worst_mismatch_dist = max(self.worst_mismatch_dist, float(dist[mism].max()))
+
+    def record(self, name, **extra):
+        r = max(self.rounds, 1)
+        rec = {"config": name, "T": self.T, "rounds": self.rounds,
+               "mismatched_rounds": self.mismatch,
+               "unflagged_mismatches": self.unflagged_mismatch,
+               "flagged_rounds": self.flag_any, "flagged_rate": self.flag_any / r,
+               "flagged_accept": self.flag_accept, "flagged_accept_rate": self.flag_accept / r,
+               "accept_flag_rate_bound": 2e-6 * self.tests / r,
+               "flagged_draw": self.flag_draw, "flagged_draw_rate": self.flag_draw / r,
+               "mismatch_rate": self.mismatch / r,
+               "largest_dist_of_a_mismatch": self.worst_mismatch_dist,
+               "max_abs_dlse_p": self.max_dlse_p, "max_abs_dlse_q": self.max_dlse_q,
+               "max_abs_dlogit": self.max_dlogit}
+        rec.update(extra)
+        _report(rec)
+        return rec
+
+
+def _oracle_sequence(Hb, W_np, Xb, Qb, Ub, T, xs, us, glog_b):
+    """The oracle on one sequence's own round and, if xs is given, its rule
+    on the nvar further rounds of that sequence (fresh drafts xs [nvar, K],
+    uniforms us [nvar, K+1]) with the same fp64 p and q.  glog_b holds the
+    GPU's logits of the sequence's rows; only their largest error is kept."""
+    ref = oracle.verify(Hb, W_np, Xb, Qb, Ub, T, want_logits=True)
+    L = ref.pop("logits")
+    out = {"own": ref, "dlogit": float(np.abs(glog_b.astype(np.float64) - L).max())}
+    if xs is not None:
+        K = Xb.shape[1]
+        p = np.stack([oracle.softmax(L[i], T) for i in range(K + 1)])
+        q = np.stack([oracle.softmax(Qb[0, i].astype(np.float64), T) for i in range(K)])
+        out["var"] = oracle.rule_batch(p, q, xs, us.astype(np.float64), split=True)
+    return out
+
+
+def _collect(tally, own, fs, var, K, T):
+    res = [f.result() for f in fs]
+    gt, gn, glse = own
+    R = gt.shape[0] * (K + 1)
+    cat = lambda k: np.concatenate([r["own"][k] for r in res])
+    tally.add(gt, gn, cat("tokens"), cat("n_accepted"), cat("dist"), cat("dist_accept"),
+              cat("dist_draw"), K)
+    tally.max_dlogit = max(tally.max_dlogit, max(r["dlogit"] for r in res))
+    if T > 0:
+        tally.max_dlse_p = max(tally.max_dlse_p, float(np.abs(glse[:R] - cat("lse_p")).max()))
+        if K > 0:
+            tally.max_dlse_q = max(tally.max_dlse_q, float(np.abs(glse[R:] - cat("lse_q")).max()))
+    if var is not None:
+        vt, vn = var
+        for b, r in enumerate(res):
+            tk, na, dist, dacc, ddraw = r["var"]
+            tally.add(vt[:, b], vn[:, b], tk, na, dist, dacc, ddraw, K)
+
+
+def _run_config(dev, name, over, T, nsets, nvar, seed, W=None):
+    wl = si.workload(name, **over)
+    if W is None:
+        W = si.make_weights(wl, seed=seed, device=dev)
+    W_np = si.to_oracle(W)
+    B, K, V = wl.B, wl.K, wl.V
+    eng = sv.SpecVerify(V, wl.d, B, K, wl.dtype, device=dev)
+    tally = Tally(T)
+    pending = []
+    # padded per-round buffers: each round's slice starts on 16 bytes
+    rt, rn = _pad4(B * (K + 1)), _pad4(B)
+    nv = max(nvar, 1)
+    ot = torch.empty((nv, rt), dtype=torch.int32, device=dev)
+    on = torch.empty((nv, rn), dtype=torch.int32, device=dev)
+    u_pad = torch.zeros((nv, rt), dtype=torch.float32, device=dev)
+    for s in range(nsets):
+        inp = si.make_round(wl, W, seed=seed + 1 + s, T=T)
+        tok, n = eng.run(inp["hidden"], W, inp["draft"], inp["q_logits"], inp["uniforms"], T)
+        assert eng.status() == sv.SV_OK
+        own = (tok.cpu().numpy(), n.cpu().numpy(), eng.lse().cpu().numpy())
+        glog = eng.logits().cpu().numpy().reshape(B, K + 1, V)
+        xs = us = var = None
+        if nvar > 0 and T > 0:
+            xd = si.draw_drafts(inp["q_logits"], T, nvar, seed=seed + 100_000 + s)
+            ud = si.draw_uniforms(nvar, B, K, seed=seed + 200_000 + s, device=dev)
+            u_pad[:, :B * (K + 1)] = ud.reshape(nvar, -1)
+            for v in range(nvar):
+                sv.spec_verify_run(eng.h, inp["hidden"], W, xd[v], inp["q_logits"],
+                                   u_pad[v], T, ot[v], on[v])
+            assert eng.status() == sv.SV_OK
+            var = (ot[:nvar, :B * (K + 1)].reshape(nvar, B, K + 1).cpu().numpy(),
+                   on[:nvar, :B].cpu().numpy())
+            xs, us = xd.cpu().numpy(), ud.cpu().numpy()
+        H = si.to_oracle(inp["hidden"])
+        X = si.to_oracle(inp["draft"])
+        Q = si.to_oracle(inp["q_logits"])
+        U = si.to_oracle(inp["uniforms"])
+        fs = [_POOL.submit(_oracle_sequence, H[b:b + 1], W_np, X[b:b + 1],
+                           Q[b:b + 1] if K > 0 else None, U[b:b + 1], T,
+                           None if xs is None else xs[:, b], None if us is None else us[:, b],
+                           glog[b])
+              for b in range(B)]
+        pending.append((own, fs, var))
+        # fold finished sets as they come, so host memory stays bounded
+        while pending and all(f.done() for f in pending[0][1]):
+            _collect(tally, *pending.pop(0), K, T)
+    for item in pending:
+        _collect(tally, *item, K, T)
+    eng.close()
+    return tally, wl
+
+
+CASES = [
+    # tiny oracle case: fp32, V=1000, d=256, K=4, 1000 sequences per launch
+    ("tiny", dict(B=1000), 1.0, 100, 0, 4000),
+    # the same shape through the bf16 tensor-core path (320 rows: column halves)
+    ("tiny", dict(dtype="bf16", B=64, w_std=1 / 16), 1.0, 8, 100, 4100),
+    # Llama-3.1-8B-shaped head, B=1, K=4, T=1 (16-column drain mode)
+    ("llama8b", {}, 1.0, 200, 500, 4200),
+    # B=8, K=7, T=0.7, per-sequence acceptance (64-column drain mode)
+    ("llama8b_b8k7", {}, 0.7, 10, 500, 4300),
+    # 70B-shaped head, B=4, K=4 (d = 8192, 32-column drain mode)
+    ("llama70b", {}, 1.0, 10, 1000, 4400),
+]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+@pytest.mark.parametrize("name,over,T,nsets,nvar,seed", CASES)
+def test_parity_and_flag_rate_at_scale(dev, name, over, T, nsets, nvar, seed):
+    tally, wl = _run_config(dev, name, over, T, nsets, nvar, seed)
+    rec = tally.record(f"{name} {over}".strip(), nsets=nsets, nvar=nvar)
+    assert tally.unflagged_mismatch == 0
+    # the accept tests: bound on the expected flagged rate, and the count
+    assert rec["accept_flag_rate_bound"] < ACCEPT_RATE_BOUND
+    assert tally.flag_accept <= _poisson_upper(ACCEPT_RATE_BOUND * tally.rounds)
+    # normalisers: well inside the 1e-6 band the thresholds are judged by
+    assert tally.max_dlse_p <= 1e-6 and tally.max_dlse_q <= 1e-6
+    assert tally.max_dlogit <= 2e-2
+
+
+@pytest.mark.parametrize("T", [0.0])
+def test_greedy_parity_b8_k7(dev, T):
+    # greedy at B=8, K=7: every round compared; a round is flagged when the
+    # top two exact logits of a deciding row are within 1e-7
+    tally, _ = _run_config(dev, "llama8b_b8k7", {}, T, 8, 0, 4500)
+    tally.record("llama8b_b8k7 greedy", nsets=8, nvar=0)
+    assert tally.unflagged_mismatch == 0
+
+
+@pytest.mark.parametrize("B,K", [(16, 4), (32, 3), (64, 3), (64, 5)])
+def test_every_sequence_in_direct_mode(dev, B, K):
+    # 80, 128, 256 and 384 rows: the direct-mode accumulators (column halves
+    # above 256); every sequence of the launch against the oracle, and the
+    # normalisers' error next to the 1e-6 flag band
+    tally, _ = _run_config(dev, "sweep", dict(B=B, K=K), 1.0, 1, 0, 4600 + 10 * B + K)
+    tally.record(f"sweep B={B} K={K}", nsets=1, nvar=0)
+    assert tally.unflagged_mismatch == 0
+    assert tally.max_dlogit <= 2e-2
+    assert tally.max_dlse_p <= 2e-6 and tally.max_dlse_q <= 1e-6
