@@ -169,6 +169,15 @@ int spec_verify_debug_lse(spec_verify_t *h, double *dst);
  * not already satisfied give up at once (used to test that path). */
 int spec_verify_set_wait_limit(spec_verify_t *h, uint64_t limit_ns);
 
+/* For tests of the timeout path: while enabled (enable != 0), every run's
+ * decision/selection kernel first waits for a device flag that nothing
+ * sets.  The wait gives up after the handle's wait limit
+ * (spec_verify_set_wait_limit), the run reports SV_ERR_TIMEOUT through the
+ * status word, and sequence 0 of that run is withdrawn (out_tokens and
+ * out_n_accepted -1) when T > 0; the other sequences are verified as usual.
+ * Nothing faults or hangs.  Returns SV_OK or SV_ERR_ARG (null handle). */
+int spec_verify_debug_stall(spec_verify_t *h, int enable);
+
 /* Kernel timing for the benchmark: while enabled, each run records CUDA
  * events on the handle's stream around the LM-head contraction kernel.
  * spec_verify_timing_read synchronises and returns the summed duration in

@@ -42,7 +42,8 @@ EXPORTS = ("spec_verify_create", "spec_verify_run", "spec_verify_run_host",
            "spec_verify_timing_read", "spec_verify_launches_per_run",
            "spec_verify_strerror", "spec_verify_destroy",
            "spec_verify_run_noalloc", "spec_ngram_draft", "spec_verify_run_truncated",
-           "spec_verify_tree_greedy", "spec_verify_run_fp8", "spec_verify_plan")
+           "spec_verify_tree_greedy", "spec_verify_run_fp8", "spec_verify_plan",
+           "spec_verify_debug_stall")
 
 
 class sv_plan_t(ctypes.Structure):
@@ -86,6 +87,7 @@ def load_library():
         lib.spec_verify_debug_logits.argtypes = [vp, vp]
         lib.spec_verify_debug_lse.argtypes = [vp, vp]
         lib.spec_verify_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
+        lib.spec_verify_debug_stall.argtypes = [vp, ctypes.c_int]
         lib.spec_verify_timing.argtypes = [vp, ctypes.c_int]
         lib.spec_verify_timing_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double),
                                                 ctypes.POINTER(i64)]
@@ -201,6 +203,13 @@ def spec_verify_debug_lse(h, dst) -> None:
 def spec_verify_set_wait_limit(h, limit_ns: int) -> None:
     _check(load_library().spec_verify_set_wait_limit(h, int(limit_ns)),
            "spec_verify_set_wait_limit")
+
+
+def spec_verify_debug_stall(h, enable: bool) -> None:
+    """Tests only: every run first waits for a flag nothing sets (bounded by
+    the wait limit), so it reports SV_ERR_TIMEOUT and withdraws sequence 0."""
+    _check(load_library().spec_verify_debug_stall(h, int(bool(enable))),
+           "spec_verify_debug_stall")
 
 
 def spec_verify_timing(h, enable: bool) -> None:

@@ -40,6 +40,7 @@ struct spec_verify {
   int device = 0;
   int num_sms = 0;
   int smem_optin = 0;
+  int tail_resident = 0;  // tail-kernel CTAs that fit on the GPU at once
   cudaStream_t stream = nullptr;
   sv::Dims dims{};
   sv::Work w{};
@@ -61,6 +62,7 @@ struct spec_verify {
   bool tma_logits = false;
   // kernel timing
   bool timing = false;
+  bool debug_stall = false;
   std::vector<cudaEvent_t> ev0, ev1;
   int64_t timed = 0, folded = 0;
   double timed_ms = 0.0;
@@ -76,7 +78,8 @@ void free_all(spec_verify *h) {
                   h->w.split_cnt, h->w.status,      h->w.abort_epoch, h->w.ticket,
                   h->w.finished,  h->w.row_count,   h->w.chunk_count, h->w.seq_flag,
                   h->w.seq_final,
-                  h->w.cand,      h->w.draft_logit, h->w.row_tau,
+                  h->w.cand,      h->w.draft_logit, h->w.row_tau,   h->w.rowpart,
+                  h->w.draft_q,   h->w.chunk_done,  h->w.never,
                   h->st_hidden,   h->st_draft,      h->st_q,        h->st_u,
                   h->st_tokens,   h->st_n};
   for (void *p : ptrs)
@@ -240,6 +243,7 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
   h->device = dev;
   h->num_sms = prop.multiProcessorCount;
   h->smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
+  h->tail_resident = sv::tail_resident_ctas(h->num_sms);
   h->stream = static_cast<cudaStream_t>(cfg->stream);
 
   sv::Dims &D = h->dims;
@@ -275,7 +279,11 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
             dalloc(&h->w.cand, static_cast<size_t>(R) * (1 + sv::kMaxCand)) &&
             dalloc(&h->w.row_tau, static_cast<size_t>(R + D.RQ)) &&
             dalloc(&h->w.draft_logit, static_cast<size_t>(D.RQ)) &&
-            dalloc(&h->w.chunk_mass, static_cast<size_t>(D.B) * D.nchunk) &&
+            dalloc(&h->w.draft_q, static_cast<size_t>(D.RQ)) &&
+            dalloc(&h->w.chunk_done, D.B) && dalloc(&h->w.never, 1) &&
+            (cfg->dtype == SV_FP32 || h->plan.ncol == 0 ||
+             dalloc(&h->w.rowpart, static_cast<size_t>(R + D.RQ) * h->plan.grid)) &&
+            dalloc(&h->w.chunk_mass, 2 * static_cast<size_t>(D.B) * D.nchunk) &&
             dalloc(&h->w.split_buf, split_floats) &&
             dalloc(&h->w.split_cnt, static_cast<size_t>(h->num_sms) * 4) &&
             dalloc(&h->w.status, 1) && dalloc(&h->w.abort_epoch, 1) &&
@@ -293,6 +301,8 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
          cudaMemset(h->w.finished, 0, sizeof(unsigned)) == cudaSuccess &&
          cudaMemset(h->w.row_count, 0, sizeof(int) * D.B) == cudaSuccess &&
          cudaMemset(h->w.chunk_count, 0, sizeof(int) * D.B) == cudaSuccess &&
+         cudaMemset(h->w.chunk_done, 0, sizeof(int) * D.B) == cudaSuccess &&
+         cudaMemset(h->w.never, 0, sizeof(int)) == cudaSuccess &&
          cudaMemset(h->w.seq_flag, 0, sizeof(unsigned) * D.B) == cudaSuccess &&
          cudaMemset(h->w.seq_final, 0, sizeof(int) * D.B) == cudaSuccess &&
          cudaDeviceSynchronize() == cudaSuccess;
@@ -434,6 +444,12 @@ int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
 
   cudaStream_t st = h->stream;
   const unsigned epoch = ++h->epoch;
+  // Fast tail: the contraction (drain mode) leaves per-CTA row statistics
+  // and the draft logits at the draft tokens, and one CTA per sequence
+  // decides from them.  Truncated rows, greedy and tree verification keep
+  // the per-row path.
+  const bool fast = h->w.rowpart != nullptr && !greedy && !tr.p_cut && !tr.q_cut &&
+                    !tr.parents && h->plan.grid <= 256;
   const float inv_t = greedy ? 1.0f : static_cast<float>(1.0 / static_cast<double>(temperature));
   cudaError_t e = cudaSuccess;
 
@@ -482,6 +498,7 @@ int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
     P.tmem_cols = pl.tmem_cols;
     P.wait_limit_ns = h->wait_limit_ns;
     P.epoch = epoch;
+    P.row_stats = fast ? 1 : 0;
     P.H = hidden;
     P.W = W_lm;
     P.draft = draft_tokens;
@@ -521,6 +538,12 @@ int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
   T.wait_limit_ns = h->wait_limit_ns;
   T.split_cnt_n = h->num_sms * 4;
   T.draft_logits_ready = h->cfg.dtype != SV_FP32 ? 1 : 0;
+  T.fast = fast ? 1 : 0;
+  T.stall = h->debug_stall ? 1 : 0;
+  T.grid_parts = h->plan.grid;
+  // every chunk CTA of a sequence waits for the others' masses: only when
+  // the whole tail grid (nchunk chunk CTAs per sequence) is resident at once
+  T.coop = (fast && static_cast<int64_t>(D.B) * D.nchunk <= h->tail_resident) ? 1 : 0;
   T.h_scale = tr.h_scale;
   T.w_scale = tr.w_scale;
   T.p_cut = tr.p_cut;
@@ -634,6 +657,12 @@ int spec_verify_debug_lse(spec_verify_t *h, double *dst) {
   return cudaMemcpy(dst, lse.data(), n * sizeof(double), cudaMemcpyDefault) == cudaSuccess
              ? SV_OK
              : SV_ERR_CUDA;
+}
+
+int spec_verify_debug_stall(spec_verify_t *h, int enable) {
+  if (!h) return SV_ERR_ARG;
+  h->debug_stall = enable != 0;
+  return SV_OK;
 }
 
 int spec_verify_timing(spec_verify_t *h, int enable) {

@@ -80,6 +80,12 @@ struct Work {
   int *cand;           // [R, 1 + kMaxCand] greedy: count, then subtile ids
   float *row_tau;      // [R + RQ] truncated sampling: the row's cut logit
   float2 *draft_logit; // [RQ]  exact logit of each draft token (float-float)
+  float4 *rowpart;     // [R + RQ, grid] per contraction CTA and row: (max M,
+                       //   sum S = sum exp(x - M) as hi, lo, 1 if a NaN/+inf
+                       //   entry was seen) of logits / T and q_logits / T
+  float *draft_q;      // [RQ]  q_logits at each draft token (contraction)
+  int *chunk_done;     // [B]   chunk CTAs past the cooperative selection
+  int *never;          // [1]   0, never written: the flag of the test stall
 };
 
 // ---------------------------------------------------------------------------
@@ -97,6 +103,12 @@ __device__ __forceinline__ void pdl_wait() {
 }
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Barrier among the first-come nthreads threads (whole warps) that use
+// barrier id (1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -505,6 +517,21 @@ __device__ __forceinline__ ff warp_sum_ff(ff x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = ff_add(x, ff_shfl_xor(x, o));
   return x;
+}
+
+// Folds the (max, sum-exp) pair (m, s) of some entries into the running
+// pair (M, S) of a row: M becomes max(M, m) and both sums are taken relative
+// to it.  A pair with m = -inf holds no mass (so does a NaN m: callers track
+// NaN and +inf entries separately).  The result does not depend on which
+// pair is the running one.
+__device__ __forceinline__ void lse_fold(float m, ff s, float &M, ff &S) {
+  if (!(m > -INFINITY)) return;
+  if (m > M) {
+    S = M > -INFINITY ? ff_add(ff_mul_f(S, expf(M - m)), s) : s;
+    M = m;
+  } else {
+    S = ff_add(S, m == M ? s : ff_mul_f(s, expf(m - M)));
+  }
 }
 
 // Accumulates a * b exactly into the pair (s, c): the product's rounding

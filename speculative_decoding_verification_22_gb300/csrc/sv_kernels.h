@@ -31,6 +31,7 @@ struct TcParams {
   uint32_t tmem_cols;      // TMEM columns allocated per CTA
   uint64_t wait_limit_ns;  // bound of every device-side wait
   unsigned epoch;          // run counter (stamps an abort)
+  int row_stats;           // drain mode, T > 0: write w.rowpart (per-CTA row pairs)
   const void *H;           // [R, d] bf16 / FP8 hidden states (draft-token logits)
   const void *W;           // [V, d] bf16 / FP8 LM head
   const int32_t *draft;    // [B, K]
@@ -80,6 +81,12 @@ struct TailParams {
   uint64_t wait_limit_ns;  // bound of the wait for a sequence's decision
   int split_cnt_n;         // entries of w.split_cnt
   int draft_logits_ready;  // w.draft_logit was written by the contraction
+  int fast;                // one decision CTA per sequence from w.rowpart and
+                           // w.draft_q (the contraction ran with row_stats)
+  int grid_parts;          // contraction CTAs: pairs per row in w.rowpart
+  int stall;               // tests: CTA 0 first waits for w.never (bounded)
+  int coop;                // cooperative selection: the whole tail grid fits
+                           // on the GPU at once (see tail_resident_ctas)
   int p_cut, q_cut;        // truncated target / draft rows: (M, S, cut) are given
   const int32_t *parents;  // greedy tree verification: [B, K] node parents (else null)
   const float *h_scale;    // FP8 (dtype SV_FP8): [R] hidden-row scales
@@ -87,6 +94,8 @@ struct TailParams {
   int32_t *out_nodes;      // tree: [B, K] accepted path's nodes (may be null)
 };
 cudaError_t launch_tail(const TailParams &P, cudaStream_t stream);
+// CTAs of the tail kernel that fit on the GPU at once (0 if unknown).
+int tail_resident_ctas(int num_sms);
 
 // ---- truncated sampling: (M, S, cut) of every truncated row --------------
 struct TruncParams {

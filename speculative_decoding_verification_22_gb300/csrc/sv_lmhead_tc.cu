@@ -13,7 +13,8 @@
 //  * persistent grid, one CTA per SM, stream-K split of the
 //    (tile, 64-wide k block) units so every SM streams the same number of
 //    bytes; a tile cut between two CTAs is finished by whichever CTA
-//    completes its part second;
+//    completes its part second (drain mode: always by the CTA holding its
+//    first k block);
 //  * warp 0 issues TMA loads (128B swizzle, W evict-first in L2) into a
 //    ring of shared-memory stages; warp 1 issues tcgen05.mma (kind::f16,
 //    M=128, K=16) into TMEM; warps 2..5 drain TMEM and run the epilogue;
@@ -96,7 +97,12 @@ constexpr uint64_t kCleanupLimitNs = 2000000000ull;
 constexpr int kBoxFloats = 16 * 32;
 constexpr int kEpiBytes = kNumEpiWarps * kBoxFloats * 4;
 
+// Draft rows whose per-CTA (max, sum-exp) the draft-logit warps keep in
+// shared memory (drain mode: fewer than 64 rows).
+constexpr int kQaccRows = 64;
+
 struct Ctl {
+  float4 qacc[kQaccRows];  // (M, S hi, S lo, bad) of this CTA's entries per draft row
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint64_t tfull[kMaxDrainSlots];
@@ -134,7 +140,7 @@ constexpr int kQBatch = 8;
 // three shuffle levels per reduction and a batch keeps 8 x 512 bytes of
 // each warp's loads in flight.
 __device__ __forceinline__ void q_partials(const TcParams &P, int t, int rfirst, int rstep,
-                                           int lane) {
+                                           int lane, float4 *qacc) {
   const int RQ = P.dims.RQ;
   const int64_t V = P.dims.V;
   const int64_t v0 = static_cast<int64_t>(t) * kTileM + lane * 4;
@@ -184,6 +190,33 @@ __device__ __forceinline__ void q_partials(const TcParams &P, int t, int rfirst,
         P.w.part_q[static_cast<int64_t>(r) * P.dims.nsub + sub] =
             sub_bad ? make_float2(NAN, NAN) : make_float2(m, s);
       }
+      if (qacc) {
+        // this CTA's running (max, sum-exp) of the row: the tile's four
+        // subtiles (one per group of eight lanes) combined, then folded
+        float tm = m, ts = s;
+#pragma unroll
+        for (int o = 8; o < 32; o <<= 1) {
+          const float om = __shfl_xor_sync(0xffffffffu, tm, o);
+          const float os = __shfl_xor_sync(0xffffffffu, ts, o);
+          const float mm = fmaxf(tm, om);
+          ts = mm > -INFINITY ? (tm > -INFINITY ? ts * expf(tm - mm) : 0.0f) +
+                                    (om > -INFINITY ? os * expf(om - mm) : 0.0f)
+                              : 0.0f;
+          tm = mm;
+        }
+        if (lane == 0) {
+          float4 a = qacc[r];
+          if (bmask) {
+            a.w = 1.0f;
+          } else {
+            float M = a.x;
+            ff S{a.y, a.z};
+            lse_fold(tm, ff_make(ts), M, S);
+            a = make_float4(M, S.hi, S.lo, a.w);
+          }
+          qacc[r] = a;
+        }
+      }
     }
   }
 }
@@ -202,9 +235,13 @@ struct EpiBox {
 // each) and the partial pass's 16-byte reads (half a column each) are free
 // of bank conflicts.  One TMA store then writes the box to the logits; the
 // partials need one shuffle per reduction instead of a butterfly.
+// With P.row_stats the lane pair of column c also folds the subtile's
+// (max, sum-exp) into this warp's running pair of the column (accM, accS;
+// accBad for NaN or +inf entries).
 __device__ __forceinline__ void finish_group(const TcParams &P, const CUtensorMap *tmL,
                                              const EpiBox &bx, const float (&x)[16], int n0,
-                                             int64_t vw, int sub, int lane) {
+                                             int64_t vw, int sub, int lane, float &accM,
+                                             ff &accS, bool &accBad) {
   const int64_t V = P.dims.V;
   const int R = P.dims.R;
   const bool greedy = P.greedy != 0;
@@ -276,10 +313,15 @@ __device__ __forceinline__ void finish_group(const TcParams &P, const CUtensorMa
   }
   const unsigned bmask = __ballot_sync(0xffffffffu, bad);
   const int n = n0 + c;
+  const bool sub_bad = ((bmask >> (2 * c)) & 3u) != 0;
   // the last tile may end inside a subtile row
   if (h == 0 && n < R && sub < P.dims.nsub)
     P.w.part_p[static_cast<int64_t>(n) * P.dims.nsub + sub] =
-        ((bmask >> (2 * c)) & 3u) ? make_float2(NAN, NAN) : make_float2(m, sum);
+        sub_bad ? make_float2(NAN, NAN) : make_float2(m, sum);
+  if (P.row_stats && !greedy && sub < P.dims.nsub) {
+    if (sub_bad) accBad = true;
+    else lse_fold(m, ff_make(sum), accM, accS);
+  }
 }
 
 // Split-tile hand-off, per warp (each warp owns 32 vocab rows of the tile and
@@ -299,6 +341,45 @@ __device__ __forceinline__ bool split_publish(const TcParams &P, int bidx, int q
 
 __device__ __forceinline__ void split_reset(const TcParams &P, int bidx, int quad, int lane) {
   if (lane == 0) P.w.split_cnt[bidx * 4 + quad] = 0;
+}
+
+// Drain mode hands a split tile over in one direction only, so that the
+// CTA holding the tile's first k block always finishes it (and the tiles
+// each CTA finishes, and the order it finishes them in, do not depend on
+// timing).  The later part (published by the next CTA at the start of its
+// work) is stored, then flagged; the earlier part waits for the flag
+// (bounded; in practice it has long been set) and clears it.
+__device__ __forceinline__ void split_hand_over(const TcParams &P, int bidx, int quad, int lane) {
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) atomicExch(&P.w.split_cnt[bidx * 4 + quad], 1);
+}
+
+__device__ __forceinline__ bool split_take(const TcParams &P, int bidx, int quad, int lane,
+                                           const volatile int *abort) {
+  int ok = 1;
+  if (lane == 0) {
+    const int *flag = &P.w.split_cnt[bidx * 4 + quad];
+    auto load = [flag]() {
+      int v;
+      asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+      return v;
+    };
+    if (load() == 0) {
+      const uint64_t t0 = globaltimer();
+      while (load() == 0) {
+        if (*abort || globaltimer() - t0 >= P.wait_limit_ns) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    if (ok) P.w.split_cnt[bidx * 4 + quad] = 0;
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) __threadfence();
+  return ok != 0;
 }
 
 template <int NCOL>
@@ -555,23 +636,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- draft-logit partials (independent of the GEMM) -------
     if (!P.greedy && P.dims.RQ > 0) {
       const int quad = (warp - 2 - kNumEpiWarps) & 3;
-      // no draft distribution (point-mass drafts): nothing to normalise
-      for (int t = t_first; t <= t_last && P.q_logits != nullptr; ++t) {
-        int kb0, kb1;
-        tile_range(t, u0, u1, ngr, C, kb0, kb1);
-        if (kb0 != 0) continue;  // the CTA holding a tile's first k block does it
-        q_partials(P, t, quad + 4 * hsel, P.half ? 8 : 4, lane);
-      }
       // the exact logit of every draft token (one warp each, spread over
-      // the grid); the decision pass reads them instead of recomputing
+      // the grid) and the draft logit at that token; the decision pass reads
+      // them instead of recomputing.  First, so that these dependent loads
+      // overlap the stream rather than trail it.
       const int K = P.dims.K;
       const int64_t n16 = P.dims.d / (P.fp8 ? 16 : 8);
       for (int idx = static_cast<int>(blockIdx.x) * kNumQWarps + quad; idx < P.dims.RQ;
            idx += static_cast<int>(gridDim.x) * kNumQWarps) {
         const int b = idx / K, i = idx - b * K;
         const int x = P.draft[idx];
+        const bool valid = x >= 0 && static_cast<int64_t>(x) < P.dims.V;
+        float qx = 0.0f;
+        if (lane == 0 && valid && P.q_logits != nullptr)
+          qx = __ldg(&P.q_logits[static_cast<int64_t>(idx) * P.dims.V + x]);
         ff l = ff_make(NAN);
-        if (x >= 0 && static_cast<int64_t>(x) < P.dims.V) {
+        if (valid) {
           const uint4 *h = static_cast<const uint4 *>(P.H) +
                            (static_cast<int64_t>(b) * (K + 1) + i) * n16;
           const uint4 *w = static_cast<const uint4 *>(P.W) + static_cast<int64_t>(x) * n16;
@@ -583,8 +663,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             l = dot_bf16_warp(h, w, 0, n16, lane);
           }
         }
-        if (lane == 0) P.w.draft_logit[idx] = make_float2(l.hi, l.lo);
+        if (lane == 0) {
+          P.w.draft_logit[idx] = make_float2(l.hi, l.lo);
+          if (P.w.draft_q) P.w.draft_q[idx] = qx;
+        }
       }
+      // row statistics: this warp's draft rows (quad, quad + 4, ...) start
+      // empty in shared memory (row_stats runs in drain mode only, where
+      // RQ < kQaccRows and no CTA pair splits the columns)
+      const bool qstats = P.row_stats && P.q_logits != nullptr;
+      float4 *qacc = qstats ? ctl->qacc : nullptr;
+      if (qstats && lane == 0)
+        for (int r = quad; r < P.dims.RQ; r += 4) qacc[r] = make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
+      __syncwarp();
+      // no draft distribution (point-mass drafts): nothing to normalise
+      for (int t = t_first; t <= t_last && P.q_logits != nullptr; ++t) {
+        int kb0, kb1;
+        tile_range(t, u0, u1, ngr, C, kb0, kb1);
+        if (kb0 != 0) continue;  // the CTA holding a tile's first k block does it
+        q_partials(P, t, quad + 4 * hsel, P.half ? 8 : 4, lane, qacc);
+      }
+      __syncwarp();
+      if (qstats)
+        for (int r = quad + 4 * lane; r < P.dims.RQ; r += 128)
+          P.w.rowpart[static_cast<int64_t>(P.dims.R + r) * gridDim.x + blockIdx.x] = qacc[r];
     }
   } else {
     // ---------------- epilogue warps ----------------
@@ -593,6 +695,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t box_off = epi_off + static_cast<uint32_t>(quad * kBoxFloats * 4);
     const EpiBox bx{reinterpret_cast<float *>(smem_raw + box_off), raw + box_off};
+    // drain mode with row_stats: this warp's running (max, sum-exp) of each
+    // column over the tiles it finishes (lane pair 2c, 2c+1 holds column c
+    // of each 16-column group)
+    constexpr int kGroups = NCOL != 0 ? NCOL / 16 : 1;
+    float accM[kGroups];
+    ff accS[kGroups];
+    bool accBad[kGroups];
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+      accM[g] = -INFINITY;
+      accS[g] = ff_make(0.0f);
+      accBad[g] = false;
+    }
     int slot = 0;
     uint32_t tphase = 0;
     for (int t = t_first; t <= t_last; ++t) {
@@ -646,21 +761,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int n = 0; n < NCOL; ++n) val[n] = acc[n];
         if (split) {
+          if (part == 1) {
+            // the tile's later k blocks: handed to the CTA that holds its
+            // first k block, which finishes the tile
 #pragma unroll
-          for (int n = 0; n < NCOL; ++n)
-            if (n < P.npad) mine[n * kTileM + row_in_tile] = val[n];
-          if (!split_publish(P, bidx, quad, lane)) continue;
+            for (int n = 0; n < NCOL; ++n)
+              if (n < P.npad) mine[n * kTileM + row_in_tile] = val[n];
+            split_hand_over(P, bidx, quad, lane);
+            continue;
+          }
+          if (!split_take(P, bidx, quad, lane, abort)) {
+            if (lane == 0) raise_abort(ctl, P);
+            break;
+          }
 #pragma unroll
           for (int n = 0; n < NCOL; ++n)
             if (n < P.npad) val[n] = val[n] + __ldcg(&other[n * kTileM + row_in_tile]);
-          split_reset(P, bidx, quad, lane);
         }
 #pragma unroll
         for (int g = 0; g < NCOL / 16; ++g) {
           float x[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) x[i] = val[g * 16 + i];
-          finish_group(P, &tmL, bx, x, col0 + g * 16, vw, sub, lane);
+          finish_group(P, &tmL, bx, x, col0 + g * 16, vw, sub, lane, accM[g], accS[g],
+                       accBad[g]);
         }
       } else {
         // direct mode: sum the tile's accumulators column group by group
@@ -701,7 +825,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) mine[(g * 16 + i) * kTileM + row_in_tile] = x[i];
           } else {
-            finish_group(P, &tmL, bx, x, col0 + g * 16, vw, sub, lane);
+            finish_group(P, &tmL, bx, x, col0 + g * 16, vw, sub, lane, accM[0], accS[0],
+                         accBad[0]);
           }
         }
         tc_fence_before();
@@ -718,7 +843,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int idx = (g * 16 + i) * kTileM + row_in_tile;
               x[i] = __ldcg(&mine[idx]) + __ldcg(&other[idx]);
             }
-            finish_group(P, &tmL, bx, x, col0 + g * 16, vw, sub, lane);
+            finish_group(P, &tmL, bx, x, col0 + g * 16, vw, sub, lane, accM[0], accS[0],
+                         accBad[0]);
           }
           split_reset(P, bidx, quad, lane);
         }
@@ -728,6 +854,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     // before the kernel ends
     if (P.tma_logits && lane == 0) bulk_wait_all();
     __syncwarp();
+    if constexpr (NCOL != 0) {
+      if (P.row_stats && !P.greedy) {
+        // the four warps' running pairs through their (now idle) staging
+        // boxes; thread i of the four warps then writes column i's pair for
+        // this CTA
+        float4 *mine4 = reinterpret_cast<float4 *>(bx.buf);
+        if ((lane & 1) == 0) {
+#pragma unroll
+          for (int g = 0; g < kGroups; ++g)
+            mine4[g * 16 + (lane >> 1)] =
+                make_float4(accM[g], accS[g].hi, accS[g].lo, accBad[g] ? 1.0f : 0.0f);
+        }
+        named_bar_sync(1, 32 * kNumEpiWarps);
+        const int i = (warp - 2) * 32 + lane;
+        if (i < NCOL && col0 + i < P.dims.R) {
+          float M = -INFINITY;
+          ff S = ff_make(0.0f);
+          bool bad = false;
+#pragma unroll
+          for (int w = 0; w < kNumEpiWarps; ++w) {
+            const float4 e =
+                reinterpret_cast<const float4 *>(smem_raw + epi_off + w * kBoxFloats * 4)[i];
+            bad |= e.w != 0.0f;
+            lse_fold(e.x, ff{e.y, e.z}, M, S);
+          }
+          P.w.rowpart[static_cast<int64_t>(col0 + i) * gridDim.x + blockIdx.x] =
+              make_float4(M, S.hi, S.lo, bad ? 1.0f : 0.0f);
+        }
+      }
+    }
   }
 
   // ---------------- teardown ----------------

@@ -179,6 +179,7 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
   w.chunk_count = c.take<int>(D.B);
   w.seq_flag = c.take<unsigned>(D.B);
   w.seq_final = c.take<int>(D.B);
+  w.chunk_done = c.take<int>(D.B);
   const size_t zero_bytes = c.off;
   w.logits = c.take<float>(static_cast<size_t>(R) * D.V);
   w.part_p = c.take<float2>(static_cast<size_t>(R) * D.nsub);
@@ -186,9 +187,13 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
   w.row_m = c.take<float>(static_cast<size_t>(R + D.RQ));
   w.row_s = c.take<float2>(static_cast<size_t>(R + D.RQ));
   w.seq = c.take<sv::SeqState>(D.B);
-  w.chunk_mass = c.take<float2>(static_cast<size_t>(D.B) * D.nchunk);
+  w.chunk_mass = c.take<float2>(2 * static_cast<size_t>(D.B) * D.nchunk);
   w.cand = c.take<int>(static_cast<size_t>(R) * (1 + sv::kMaxCand));
   w.draft_logit = c.take<float2>(static_cast<size_t>(D.RQ));
+  w.draft_q = c.take<float>(static_cast<size_t>(D.RQ));
+  // per-CTA row statistics of the drain-mode contraction (fast tail)
+  const bool fast = cfg->dtype == SV_BF16 && plan.ncol != 0 && !greedy && plan.grid <= 256;
+  w.rowpart = fast ? c.take<float4>(static_cast<size_t>(R + D.RQ) * plan.grid) : nullptr;
   w.split_buf = c.take<float>(cfg->dtype == SV_BF16
                                   ? static_cast<size_t>(plan.grid) * 2 * sv::kTileM * plan.npad
                                   : 1);
@@ -231,6 +236,7 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
     P.tmem_cols = plan.tmem_cols;
     P.wait_limit_ns = wait_limit_ns;
     P.epoch = epoch;
+    P.row_stats = fast ? 1 : 0;
     P.H = hidden;
     P.W = W_lm;
     P.draft = draft_tokens;
@@ -265,5 +271,8 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
   T.wait_limit_ns = wait_limit_ns;
   T.split_cnt_n = sms * 4;
   T.draft_logits_ready = cfg->dtype == SV_BF16 ? 1 : 0;
+  T.fast = fast ? 1 : 0;
+  T.grid_parts = plan.grid;
+  T.coop = (fast && static_cast<int64_t>(D.B) * D.nchunk <= sv::tail_resident_ctas(sms)) ? 1 : 0;
   return sv::launch_tail(T, st) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

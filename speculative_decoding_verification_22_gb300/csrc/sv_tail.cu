@@ -292,8 +292,75 @@ __device__ __forceinline__ int arrive_final(const TailParams &P, int b) {
   return (prev & kPoisoned) ? kFinPoison : kFinSelect;
 }
 
+// Row statistics of sequence b from the contraction's per-CTA pairs (fast
+// mode): target rows i = 0..K and, with draft logits, draft rows 0..K-1.
+// Warps 2.. take the rows (warps 0 and 1 load the decision's other inputs
+// meanwhile); a warp folds the grid_parts pairs of its row (up to eight per
+// lane, loaded at once) and then across lanes.  The results go to shared
+// memory and to row_m / row_s (which spec_verify_debug_lse reads).  A NaN
+// or +inf entry anywhere in a row makes its maximum NaN.
+constexpr int kMaxParts = 256;
+__device__ void fast_row_stats(const TailParams &P, int b, float *s_lp_m, ff *s_lp_s,
+                               float *s_lq_m, ff *s_lq_s) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = P.dims.K, R = P.dims.R, G = P.grid_parts;
+  const int nstat = P.q_logits ? 2 * K + 1 : K + 1;
+  constexpr int kStatWarps = kTailWarps - 2;
+  for (int j = warp - 2; j >= 0 && j < nstat; j += kStatWarps) {
+    const int64_t row = j <= K ? static_cast<int64_t>(b) * (K + 1) + j
+                               : static_cast<int64_t>(R) + static_cast<int64_t>(b) * K + (j - K - 1);
+    const float4 *src = P.w.rowpart + row * G;
+    float4 e[kMaxParts / 32];
+#pragma unroll
+    for (int k = 0; k < kMaxParts / 32; ++k) {
+      const int c = lane + 32 * k;
+      e[k] = c < G ? __ldcg(&src[c]) : make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
+    }
+    float M = -INFINITY;
+    ff S = ff_make(0.0f);
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < kMaxParts / 32; ++k) {
+      bad |= e[k].w != 0.0f;
+      lse_fold(e[k].x, ff{e[k].y, e[k].z}, M, S);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, M, o);
+      const ff os = ff_shfl_xor(S, o);
+      lse_fold(om, os, M, S);
+    }
+    if (__any_sync(0xffffffffu, bad)) M = NAN;
+    if (lane == 0) {
+      if (j <= K) {
+        s_lp_m[j] = M;
+        s_lp_s[j] = S;
+      } else {
+        s_lq_m[j - K - 1] = M;
+        s_lq_s[j - K - 1] = S;
+      }
+      P.w.row_m[row] = M;
+      st_ff(&P.w.row_s[row], S);
+    }
+  }
+  if (!P.q_logits && warp == 1) {
+    // drafts proposed with certainty: the draft rows are neutral (M = 0, S = 1)
+    for (int i = lane; i < K; i += 32) {
+      const int64_t row = static_cast<int64_t>(R) + static_cast<int64_t>(b) * K + i;
+      s_lq_m[i] = 0.0f;
+      s_lq_s[i] = ff_make(1.0f);
+      P.w.row_m[row] = 0.0f;
+      st_ff(&P.w.row_s[row], ff_make(1.0f));
+    }
+  }
+}
+
 // Returns (to every thread of the block) what this CTA must finalise.
-__device__ int decide(const TailParams &P, int b) {
+// With `local` (cooperative selection: every chunk CTA of the sequence
+// takes the same decision from the same inputs) the decision goes to that
+// shared-memory state instead of being published, and the accepted prefix
+// and count are written only if `emit` (by one of the CTAs).
+__device__ int decide(const TailParams &P, int b, SeqState *local = nullptr, bool emit = true) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = P.dims.K, rows = K + 1;
   const int64_t V = P.dims.V;
@@ -315,18 +382,24 @@ __device__ int decide(const TailParams &P, int b) {
   __shared__ int s_depth[SV_MAX_K + 1];         // tree: depth of root / nodes
   __shared__ unsigned char s_match[SV_MAX_K + 1];
 
+  // fast mode: this CTA computes the row statistics itself (warps 2..)
+  const bool fast = P.fast != 0;
   if (threadIdx.x == 0) s_err = 0;
   __syncthreads();
   // everything the walk needs, loaded in parallel
   if (threadIdx.x < rows) {
     const int i = threadIdx.x;
     s_tp[i] = P.p_cut ? __ldcg(&P.w.row_tau[out0 + i]) : -INFINITY;
-    s_lp_m[i] = __ldcg(&P.w.row_m[out0 + i]);
-    s_lp_s[i] = ld_ff(&P.w.row_s[out0 + i]);
+    if (!fast) {
+      s_lp_m[i] = __ldcg(&P.w.row_m[out0 + i]);
+      s_lp_s[i] = ld_ff(&P.w.row_s[out0 + i]);
+    }
     if (!P.greedy) s_u[i] = P.u[out0 + i];
-    const bool fin = isfinite(s_lp_m[i]) &&
-                     (P.greedy || (s_lp_s[i].hi > 0.0f && s_lp_s[i].hi < INFINITY));
-    if (!fin) atomicCAS(&s_err, 0, SV_ERR_NONFINITE);
+    if (!fast) {
+      const bool fin = isfinite(s_lp_m[i]) &&
+                       (P.greedy || (s_lp_s[i].hi > 0.0f && s_lp_s[i].hi < INFINITY));
+      if (!fin) atomicCAS(&s_err, 0, SV_ERR_NONFINITE);
+    }
   }
   if (threadIdx.x >= 32 && threadIdx.x < 32 + K) {
     const int i = threadIdx.x - 32;
@@ -346,16 +419,23 @@ __device__ int decide(const TailParams &P, int b) {
       // a point-mass draft row holds M = 0, S = 1 and q_logits(x) counts
       // as 0, so the threshold below is p(x) / 1
       const int64_t rq = static_cast<int64_t>(R) + static_cast<int64_t>(b) * K + i;
-      s_lq_m[i] = __ldcg(&P.w.row_m[rq]);
-      s_lq_s[i] = ld_ff(&P.w.row_s[rq]);
-      s_ql[i] = point ? 0.0f : P.q_logits[(static_cast<int64_t>(b) * K + i) * V + x];
+      if (!fast) {
+        s_lq_m[i] = __ldcg(&P.w.row_m[rq]);
+        s_lq_s[i] = ld_ff(&P.w.row_s[rq]);
+      }
+      // fast mode: the contraction also left q_logits at the draft token
+      s_ql[i] = point ? 0.0f
+                      : fast ? __ldcg(&P.w.draft_q[static_cast<int64_t>(b) * K + i])
+                             : P.q_logits[(static_cast<int64_t>(b) * K + i) * V + x];
       // truncated sampling: membership of x is decided on the same fp32
       // values the cut was found on
       s_tq[i] = P.q_cut ? __ldcg(&P.w.row_tau[rq]) : -INFINITY;
       s_lbuf[i] = P.p_cut ? __ldcg(&P.w.logits[(out0 + i) * V + x]) : 0.0f;
       s_l[i] = ld_ff(&P.w.draft_logit[static_cast<int64_t>(b) * K + i]);
-      const bool fin = isfinite(s_lq_m[i]) && s_lq_s[i].hi > 0.0f && s_lq_s[i].hi < INFINITY;
-      if (!fin) atomicCAS(&s_err, 0, SV_ERR_NONFINITE);
+      if (!fast) {
+        const bool fin = isfinite(s_lq_m[i]) && s_lq_s[i].hi > 0.0f && s_lq_s[i].hi < INFINITY;
+        if (!fin) atomicCAS(&s_err, 0, SV_ERR_NONFINITE);
+      }
     }
   }
   if (threadIdx.x == 64 &&
@@ -363,7 +443,24 @@ __device__ int decide(const TailParams &P, int b) {
     // a contraction that gave up in this run leaves the partials undefined
     atomicExch(&s_err, SV_ERR_TIMEOUT);
   }
+  if (fast) fast_row_stats(P, b, s_lp_m, s_lp_s, s_lq_m, s_lq_s);
   __syncthreads();
+  if (fast) {
+    // the finiteness checks of the row statistics just computed
+    if (threadIdx.x < rows) {
+      const int i = threadIdx.x;
+      const bool fin = isfinite(s_lp_m[i]) && s_lp_s[i].hi > 0.0f && s_lp_s[i].hi < INFINITY;
+      if (!fin) atomicCAS(&s_err, 0, SV_ERR_NONFINITE);
+    }
+    if (threadIdx.x >= 32 && threadIdx.x < 32 + K) {
+      const int i = threadIdx.x - 32;
+      const int x = s_x[i];
+      if (x >= 0 && static_cast<int64_t>(x) < V) {
+        const bool fin = isfinite(s_lq_m[i]) && s_lq_s[i].hi > 0.0f && s_lq_s[i].hi < INFINITY;
+        if (!fin) atomicCAS(&s_err, 0, SV_ERR_NONFINITE);
+      }
+    }
+  }
   if (threadIdx.x == 0) {
     // proposed tokens of this sequence: K, or the position of the first -1
     // of a point-mass draft, after which every entry must be -1 too
@@ -419,7 +516,7 @@ __device__ int decide(const TailParams &P, int b) {
           break;
         }
         if (s_acc[i]) {
-          P.out_tokens[out0 + i] = s_x[i];
+          if (emit) P.out_tokens[out0 + i] = s_x[i];
         } else {
           n = i;
           mode = point ? kModeResidualPoint : kModeResidual;
@@ -427,8 +524,10 @@ __device__ int decide(const TailParams &P, int b) {
         }
       }
       if (err == 0) {
-        for (int i = n + 1; i < rows; ++i) P.out_tokens[out0 + i] = -1;
-        P.out_n[b] = n;
+        if (emit) {
+          for (int i = n + 1; i < rows; ++i) P.out_tokens[out0 + i] = -1;
+          P.out_n[b] = n;
+        }
         st.mode = mode;
         st.n_acc = n;
         st.p_row = static_cast<int>(out0 + n);
@@ -493,20 +592,26 @@ __device__ int decide(const TailParams &P, int b) {
       }
     }
     if (err != 0) {
-      if (err != SV_ERR_TIMEOUT) set_status(P.w.status, err);
       st.mode = kModeSkip;
-      for (int i = 0; i < rows; ++i) P.out_tokens[out0 + i] = -1;
-      if (P.out_nodes)
-        for (int i = 0; i < K; ++i) P.out_nodes[static_cast<int64_t>(b) * K + i] = -1;
-      P.out_n[b] = -1;
+      if (emit) {
+        if (err != SV_ERR_TIMEOUT) set_status(P.w.status, err);
+        for (int i = 0; i < rows; ++i) P.out_tokens[out0 + i] = -1;
+        if (P.out_nodes)
+          for (int i = 0; i < K; ++i) P.out_nodes[static_cast<int64_t>(b) * K + i] = -1;
+        P.out_n[b] = -1;
+      }
     }
-    P.w.seq[b] = st;
-    __threadfence();
-    *reinterpret_cast<volatile unsigned *>(&P.w.seq_flag[b]) = P.epoch;
     s_fin = kFinNone;
-    if (!P.greedy) {
+    if (local) {
+      *local = st;
+    } else {
+      P.w.seq[b] = st;
       __threadfence();
-      s_fin = arrive_final(P, b);
+      *reinterpret_cast<volatile unsigned *>(&P.w.seq_flag[b]) = P.epoch;
+      if (!P.greedy) {
+        __threadfence();
+        s_fin = arrive_final(P, b);
+      }
     }
   }
   __syncthreads();
@@ -571,21 +676,54 @@ __device__ __forceinline__ void locate_chunk(const float2 *mass, int nchunk, flo
   }
 }
 
-__device__ void select_token(const TailParams &P, int b, SeqState st) {
-  __shared__ ff s_warp[kTailWarps];
-  __shared__ ff s_S, s_base, s_target;
-  __shared__ int s_chunk, s_found, s_last;
-  const int lane = threadIdx.x & 31;
-  const int nchunk = P.dims.nchunk;
-  float2 *mass = P.w.chunk_mass + static_cast<int64_t>(b) * nchunk;
-
-  if (threadIdx.x < 32) locate_chunk(mass, nchunk, st.u_final, lane, s_S, s_base, s_target, s_chunk);
+// The inverse CDF inside the chunk that holds the target: a block scan of
+// this thread's weights r (the chunk's entries threadIdx.x * 8 .. + 7, sum
+// tsum) on top of `base`, the mass before the chunk; thread 0 writes the
+// smallest v with target < C_v (or, if rounding left none, the largest v of
+// the chunk with positive weight) to *out.
+__device__ void scan_chunk(const float (&r)[kChunkPerThread], float tsum, int chunk, ff base,
+                           ff target, int32_t *out, ff *s_warp) {
+  __shared__ int s_found, s_last;
   if (threadIdx.x == 0) {
     s_found = 0x7fffffff;
     s_last = -1;
   }
+  ff run = ff_add(base, block_excl_scan_ff(ff_make(tsum), s_warp));
+  const int64_t v0 = static_cast<int64_t>(chunk) * kChunk + threadIdx.x * kChunkPerThread;
+  int found = 0x7fffffff, last = -1;
+#pragma unroll
+  for (int j = 0; j < kChunkPerThread; ++j) {
+    run = ff_add(run, ff_make(r[j]));
+    if (r[j] > 0.0f) {
+      last = static_cast<int>(v0 + j);
+      if (found == 0x7fffffff && ff_lt(target, run)) found = static_cast<int>(v0 + j);
+    }
+  }
+  if (found != 0x7fffffff) atomicMin(&s_found, found);
+  if (last >= 0) atomicMax(&s_last, last);
   __syncthreads();
-  if (!(s_S.hi > 0.0f) && (st.mode == kModeResidual || st.mode == kModeResidualPoint)) {
+  if (threadIdx.x == 0) *out = s_found != 0x7fffffff ? s_found : s_last;
+}
+
+// The final draw of sequence b by one CTA.  With masses_ready the chunk
+// masses of st's weights are in `mass`; otherwise (or when the residual
+// turns out empty: p_j == q_j on the row) the CTA computes the masses of
+// p_j itself into `mass` and draws from p_j.
+__device__ void select_token(const TailParams &P, int b, SeqState st, float2 *mass,
+                             bool masses_ready) {
+  __shared__ ff s_warp[kTailWarps];
+  __shared__ ff s_S, s_base, s_target;
+  __shared__ int s_chunk;
+  const int lane = threadIdx.x & 31;
+  const int nchunk = P.dims.nchunk;
+  bool recompute = !masses_ready;
+  if (masses_ready) {
+    if (threadIdx.x < 32)
+      locate_chunk(mass, nchunk, st.u_final, lane, s_S, s_base, s_target, s_chunk);
+    __syncthreads();
+    recompute = !(s_S.hi > 0.0f) && (st.mode == kModeResidual || st.mode == kModeResidualPoint);
+  }
+  if (recompute) {
     // p_j == q_j on this row: draw from p_j instead
     st.mode = kModeP;
     for (int c = 0; c < nchunk; ++c) {
@@ -611,22 +749,81 @@ __device__ void select_token(const TailParams &P, int b, SeqState st) {
   const int chunk = s_chunk;
   float r[kChunkPerThread];
   const float tsum = chunk_weights(P, st, chunk, r);
-  ff run = ff_add(s_base, block_excl_scan_ff(ff_make(tsum), s_warp));
-  const int64_t v0 = static_cast<int64_t>(chunk) * kChunk + threadIdx.x * kChunkPerThread;
-  const ff target = s_target;
-  int found = 0x7fffffff, last = -1;
-#pragma unroll
-  for (int j = 0; j < kChunkPerThread; ++j) {
-    run = ff_add(run, ff_make(r[j]));
-    if (r[j] > 0.0f) {
-      last = static_cast<int>(v0 + j);
-      if (found == 0x7fffffff && ff_lt(target, run)) found = static_cast<int>(v0 + j);
+  scan_chunk(r, tsum, chunk, s_base, s_target, out, s_warp);
+}
+
+// Bounded wait (one thread) until *cnt >= target, with acquire ordering.
+__device__ __forceinline__ bool wait_count(const int *cnt, int target, uint64_t limit_ns) {
+  auto load = [cnt]() {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    return v;
+  };
+  if (load() >= target) return true;
+  const uint64_t t0 = globaltimer();
+  while (load() < target) {
+    if (globaltimer() - t0 >= limit_ns) return false;
+    __nanosleep(20);
+  }
+  return true;
+}
+
+// Cooperative selection (the whole tail grid resident at once): every chunk
+// CTA of sequence b publishes its mass and waits until all have; each then
+// locates the chunk holding u * S, and the CTA that computed that chunk
+// scans the weights it still holds.  A CTA whose wait for the other masses
+// ran out reports SV_ERR_TIMEOUT and marks the sequence; the last CTA past
+// the selection then withdraws a marked sequence (outputs -1) and rewinds
+// the sequence's counters.
+__device__ void coop_select(const TailParams &P, int b, int c, const SeqState &st,
+                            const float (&r)[kChunkPerThread], float tsum, ff mass) {
+  __shared__ ff s_warp[kTailWarps];
+  __shared__ ff s_S, s_base, s_target;
+  __shared__ int s_chunk, s_all;
+  const int lane = threadIdx.x & 31;
+  const int nchunk = P.dims.nchunk;
+  float2 *masses = P.w.chunk_mass + static_cast<int64_t>(b) * nchunk;
+  const int64_t rows = P.dims.K + 1;
+  if (threadIdx.x == 0) {
+    st_ff(&masses[c], mass);
+    __threadfence();
+    atomicAdd(&P.w.chunk_count[b], 1);
+    s_all = wait_count(&P.w.chunk_count[b], nchunk, P.wait_limit_ns) ? 1 : 0;
+  }
+  __syncthreads();
+  if (s_all && st.mode != kModeSkip) {
+    if (threadIdx.x < 32)
+      locate_chunk(masses, nchunk, st.u_final, lane, s_S, s_base, s_target, s_chunk);
+    __syncthreads();
+    if (!(s_S.hi > 0.0f)) {
+      // an empty residual (or no mass at all): the first chunk CTA draws
+      // alone, with masses of its own in the second half of chunk_mass
+      if (c == 0)
+        select_token(P, b, st,
+                     P.w.chunk_mass + static_cast<int64_t>(P.dims.B + b) * nchunk, false);
+    } else if (s_chunk == c) {
+      scan_chunk(r, tsum, c, s_base, s_target, P.out_tokens + b * rows + st.n_acc, s_warp);
     }
   }
-  if (found != 0x7fffffff) atomicMin(&s_found, found);
-  if (last >= 0) atomicMax(&s_last, last);
   __syncthreads();
-  if (threadIdx.x == 0) *out = s_found != 0x7fffffff ? s_found : s_last;
+  if (threadIdx.x == 0) {
+    if (!s_all) {
+      set_status(P.w.status, SV_ERR_TIMEOUT);
+      atomicOr(&P.w.seq_final[b], kPoisoned);
+    }
+    __threadfence();
+    if (atomicAdd(&P.w.chunk_done[b], 1) == nchunk - 1) {
+      __threadfence();
+      if (*reinterpret_cast<volatile int *>(&P.w.seq_final[b]) & kPoisoned) {
+        for (int i = 0; i < rows; ++i) P.out_tokens[static_cast<int64_t>(b) * rows + i] = -1;
+        P.out_n[b] = -1;
+      }
+      P.w.chunk_count[b] = 0;
+      P.w.chunk_done[b] = 0;
+      P.w.seq_final[b] = 0;
+      __threadfence();
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -652,7 +849,8 @@ __device__ void finalize_sequence(const TailParams &P, int b, int fin,
 #pragma unroll
       for (int i = 0; i < static_cast<int>(sizeof(SeqState) / 4); ++i) dst[i] = __ldcg(&src[i]);
     }
-    if (st.mode != kModeSkip) select_token(P, b, st);
+    if (st.mode != kModeSkip)
+      select_token(P, b, st, P.w.chunk_mass + static_cast<int64_t>(b) * P.dims.nchunk, true);
   }
 }
 
@@ -668,12 +866,26 @@ __global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const TailParams 
   __shared__ int s_last;
   const int K = P.dims.K;
   const int R = P.dims.R;
-  const int nrow = P.greedy ? R : R + P.dims.RQ;
+  // cooperative selection: chunk CTAs only (each takes its sequence's
+  // decision itself); fast mode: one decision CTA per sequence; otherwise
+  // one CTA per row
+  const int nrow = P.coop ? 0 : P.fast ? P.dims.B : P.greedy ? R : R + P.dims.RQ;
   if (threadIdx.x == 0) s_ticket = atomicAdd(P.w.ticket, 1u);
   __syncthreads();
   const int t = static_cast<int>(s_ticket);
+  if (P.stall && t == 0 && threadIdx.x == 0) {
+    // test of the timeout path: a wait for a flag that nothing sets runs
+    // out; the run reports it and sequence 0 is withdrawn
+    if (!wait_flag(reinterpret_cast<const unsigned *>(P.w.never), 1u, P.wait_limit_ns)) {
+      set_status(P.w.status, SV_ERR_TIMEOUT);
+      atomicOr(&P.w.seq_final[0], kPoisoned);
+      __threadfence();
+    }
+  }
 
-  if (t < nrow) {
+  if (t < nrow && P.fast) {
+    finalize_sequence(P, t, decide(P, t));
+  } else if (t < nrow) {
     // ---- row statistics ----
     const bool qrow = t >= R;
     const int b = qrow ? (t - R) / (K > 0 ? K : 1) : t / (K + 1);
@@ -784,6 +996,20 @@ __global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const TailParams 
     }
     __syncthreads();
     if (s_last) finalize_sequence(P, b, decide(P, b));
+  } else if (P.coop) {
+    // ---- cooperative chunk: the sequence's decision, taken here as in
+    // every chunk CTA of the sequence (the first writes the accepted
+    // prefix), this chunk's mass, then the cooperative selection ----
+    const int b = t / P.dims.nchunk, c = t % P.dims.nchunk;
+    __shared__ SeqState s_st;
+    decide(P, b, &s_st, c == 0);
+    const SeqState st = s_st;
+    float r[kChunkPerThread];
+#pragma unroll
+    for (int j = 0; j < kChunkPerThread; ++j) r[j] = 0.0f;
+    const float m = st.mode != kModeSkip ? chunk_weights(P, st, c, r) : 0.0f;
+    const ff mass = block_sum_ff(ff_make(m), s_wff);
+    coop_select(P, b, c, st, r, m, mass);
   } else {
     // ---- residual chunk ----
     const int idx = t - nrow;
@@ -839,8 +1065,16 @@ __global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const TailParams 
   }
 }
 
+int tail_resident_ctas(int num_sms) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tail_kernel, kTailThreads, 0) !=
+      cudaSuccess)
+    return 0;
+  return per_sm * num_sms;
+}
+
 cudaError_t launch_tail(const TailParams &P, cudaStream_t stream) {
-  const int nrow = P.greedy ? P.dims.R : P.dims.R + P.dims.RQ;
+  const int nrow = P.coop ? 0 : P.fast ? P.dims.B : P.greedy ? P.dims.R : P.dims.R + P.dims.RQ;
   const int nchunk_ctas = P.greedy ? 0 : P.dims.B * P.dims.nchunk;
   void *args[] = {const_cast<TailParams *>(&P)};
   return launch_pdl(reinterpret_cast<const void *>(&tail_kernel), dim3(nrow + nchunk_ctas),

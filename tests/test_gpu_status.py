@@ -1,9 +1,9 @@
 """GPU error paths: every failure is reported through a return code or the
 device status word, the context stays usable, and later runs are correct.
-No test here faults, traps or hangs the GPU: the timeout test sets the
-device-side wait limit to zero, so the first wait that is not already
-satisfied gives up at once and the kernel returns after draining its own
-copies in flight."""
+No test here faults, traps or hangs the GPU: the timeout tests make a
+bounded wait run out, either on a flag that nothing sets (a test switch of
+the library) or by a zero wait limit, and the kernels return after draining
+their own copies in flight."""
 import numpy as np
 import pytest
 import torch
@@ -19,7 +19,9 @@ pytestmark = pytest.mark.gpu
 def setup():
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
-    wl = si.workload("tiny", dtype="bf16", B=3, K=4, V=3000, d=512, w_std=1 / 22.6)
+    # V = 9000: three residual chunks per sequence, so that the selection's
+    # wait for the other chunks' masses is a wait that a zero limit ends
+    wl = si.workload("tiny", dtype="bf16", B=3, K=4, V=9000, d=512, w_std=1 / 22.6)
     W = si.make_weights(wl, seed=5, device=dev)
     inp = si.make_round(wl, W, seed=6)
     eng = sv.SpecVerify(wl.V, wl.d, wl.B, wl.K, wl.dtype, device=dev)
@@ -83,30 +85,58 @@ def test_non_finite_weights_are_reported(setup):
     _check_ok(eng, W, W_np, inp)
 
 
-def test_wait_limit_zero_times_out_and_recovers(setup):
+def test_a_wait_that_runs_out_is_reported_and_recovers(setup):
+    """A bounded device-side wait that runs out.  With the test stall on,
+    each run's decision/selection kernel first waits for a flag that nothing
+    sets; after the wait limit (1 ms here) the run reports SV_ERR_TIMEOUT
+    and withdraws sequence 0, the others come out as the oracle has them,
+    and once the stall is off and the limit restored every run is right."""
+    dev, wl, W, W_np, inp, eng = setup
+    ref = oracle_verify(inp["hidden"], W_np, inp["draft"], inp["q_logits"], inp["uniforms"], 1.0)
+    fl = flagged(ref, 1.0)
+    sv.spec_verify_set_wait_limit(eng.h, 1_000_000)
+    sv.spec_verify_debug_stall(eng.h, True)
+    try:
+        for _ in range(3):
+            got = gpu_verify(eng, W, inp, 1.0)
+            assert got["status"] == sv.SV_ERR_TIMEOUT
+            assert got["n_accepted"][0] == -1 and np.all(got["tokens"][0] == -1)
+            for b in range(1, wl.B):
+                same = np.array_equal(got["tokens"][b], ref["tokens"][b]) and \
+                    got["n_accepted"][b] == ref["n_accepted"][b]
+                assert same or fl[b]
+    finally:
+        sv.spec_verify_debug_stall(eng.h, False)
+        sv.spec_verify_set_wait_limit(eng.h, 1_000_000_000)
+    for _ in range(3):
+        _check_ok(eng, W, W_np, inp)
+
+
+def test_wait_limit_zero_never_draws_from_partial_results(setup):
     """With a zero limit the first wait that is not already satisfied gives
-    up.  Which waits that hits depends on timing (a wait that is satisfied
-    at its first poll does not time out), so each sequence must come out
-    either withdrawn (-1 throughout) or exactly as the oracle has it; never
-    a token drawn from partial results."""
+    up.  Which waits that hits depends on timing (a wait satisfied at its
+    first poll does not time out, and the run may then succeed), so each
+    sequence must come out either withdrawn (-1 throughout, with the status
+    SV_ERR_TIMEOUT) or exactly as the oracle has it; never a token drawn
+    from partial results.  Runs after it are right again."""
     dev, wl, W, W_np, inp, eng = setup
     ref = oracle_verify(inp["hidden"], W_np, inp["draft"], inp["q_logits"], inp["uniforms"], 1.0)
     fl = flagged(ref, 1.0)
     sv.spec_verify_set_wait_limit(eng.h, 0)
-    withdrawn = 0
-    for _ in range(5):
-        got = gpu_verify(eng, W, inp, 1.0)
-        assert got["status"] == sv.SV_ERR_TIMEOUT
-        for b in range(wl.B):
-            if got["n_accepted"][b] == -1:
-                assert np.all(got["tokens"][b] == -1)
-                withdrawn += 1
-            else:
-                same = np.array_equal(got["tokens"][b], ref["tokens"][b]) and \
-                    got["n_accepted"][b] == ref["n_accepted"][b]
-                assert same or fl[b]
-    assert withdrawn > 0
-    sv.spec_verify_set_wait_limit(eng.h, 1_000_000_000)
+    try:
+        for _ in range(5):
+            got = gpu_verify(eng, W, inp, 1.0)
+            assert got["status"] in (sv.SV_OK, sv.SV_ERR_TIMEOUT)
+            for b in range(wl.B):
+                if got["n_accepted"][b] == -1:
+                    assert np.all(got["tokens"][b] == -1)
+                    assert got["status"] == sv.SV_ERR_TIMEOUT
+                else:
+                    same = np.array_equal(got["tokens"][b], ref["tokens"][b]) and \
+                        got["n_accepted"][b] == ref["n_accepted"][b]
+                    assert same or fl[b]
+    finally:
+        sv.spec_verify_set_wait_limit(eng.h, 1_000_000_000)
     for _ in range(3):
         _check_ok(eng, W, W_np, inp)
 
