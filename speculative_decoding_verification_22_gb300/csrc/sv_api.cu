@@ -40,7 +40,9 @@ struct spec_verify {
   int device = 0;
   int num_sms = 0;
   int smem_optin = 0;
-  int tail_resident = 0;  // tail-kernel CTAs that fit on the GPU at once
+  int tail_resident = 0;         // cooperative tail CTAs that fit on the GPU at once
+  int stage_bytes = 0;           // shared memory of the staged cooperative tail (0: none)
+  int tail_resident_staged = 0;  // the same with stage_bytes of shared memory each
   cudaStream_t stream = nullptr;
   sv::Dims dims{};
   sv::Work w{};
@@ -243,7 +245,7 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
   h->device = dev;
   h->num_sms = prop.multiProcessorCount;
   h->smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
-  h->tail_resident = sv::tail_resident_ctas(h->num_sms);
+  h->tail_resident = sv::tail_resident_ctas(h->num_sms, 0);
   h->stream = static_cast<cudaStream_t>(cfg->stream);
 
   sv::Dims &D = h->dims;
@@ -265,6 +267,9 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
       return SV_ERR_SHAPE;
     }
     split_floats = static_cast<size_t>(h->plan.grid) * 2 * sv::kTileM * h->plan.npad;
+    h->stage_bytes = sv::tail_stage_bytes(D, true);
+    h->tail_resident_staged =
+        h->stage_bytes > 0 ? sv::tail_resident_ctas(h->num_sms, h->stage_bytes) : 0;
   }
   const size_t es = esize(cfg->dtype);
   bool ok = dalloc(&h->w.logits, static_cast<size_t>(R) * D.V) &&
@@ -303,6 +308,7 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
          cudaMemset(h->w.chunk_count, 0, sizeof(int) * D.B) == cudaSuccess &&
          cudaMemset(h->w.chunk_done, 0, sizeof(int) * D.B) == cudaSuccess &&
          cudaMemset(h->w.never, 0, sizeof(int)) == cudaSuccess &&
+
          cudaMemset(h->w.seq_flag, 0, sizeof(unsigned) * D.B) == cudaSuccess &&
          cudaMemset(h->w.seq_final, 0, sizeof(int) * D.B) == cudaSuccess &&
          cudaDeviceSynchronize() == cudaSuccess;
@@ -542,8 +548,18 @@ int run_impl(spec_verify_t *h, const void *hidden, const void *W_lm,
   T.stall = h->debug_stall ? 1 : 0;
   T.grid_parts = h->plan.grid;
   // every chunk CTA of a sequence waits for the others' masses: only when
-  // the whole tail grid (nchunk chunk CTAs per sequence) is resident at once
-  T.coop = (fast && static_cast<int64_t>(D.B) * D.nchunk <= h->tail_resident) ? 1 : 0;
+  // the whole tail grid (nchunk chunk CTAs per sequence) is resident at
+  // once; staged (candidate rows in shared memory) if that still holds with
+  // the staging's shared memory
+  const int64_t tail_ctas = static_cast<int64_t>(D.B) * D.nchunk;
+  T.coop = 0;
+  T.stage_rows = 0;
+  if (fast && h->stage_bytes > 0 && tail_ctas <= h->tail_resident_staged) {
+    T.coop = 1;
+    T.stage_rows = D.K + 1 + (q_logits ? D.K : 0);
+  } else if (fast && tail_ctas <= h->tail_resident) {
+    T.coop = 1;
+  }
   T.h_scale = tr.h_scale;
   T.w_scale = tr.w_scale;
   T.p_cut = tr.p_cut;

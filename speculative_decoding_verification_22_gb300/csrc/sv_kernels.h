@@ -87,6 +87,8 @@ struct TailParams {
   int stall;               // tests: CTA 0 first waits for w.never (bounded)
   int coop;                // cooperative selection: the whole tail grid fits
                            // on the GPU at once (see tail_resident_ctas)
+  int stage_rows;          // cooperative: rows of each chunk staged in shared
+                           // memory by bulk copies (0: read from L2)
   int p_cut, q_cut;        // truncated target / draft rows: (M, S, cut) are given
   const int32_t *parents;  // greedy tree verification: [B, K] node parents (else null)
   const float *h_scale;    // FP8 (dtype SV_FP8): [R] hidden-row scales
@@ -94,8 +96,14 @@ struct TailParams {
   int32_t *out_nodes;      // tree: [B, K] accepted path's nodes (may be null)
 };
 cudaError_t launch_tail(const TailParams &P, cudaStream_t stream);
-// CTAs of the tail kernel that fit on the GPU at once (0 if unknown).
-int tail_resident_ctas(int num_sms);
+// CTAs of the cooperative tail kernel that fit on the GPU at once with
+// stage_bytes of dynamic shared memory each (0 if unknown).
+int tail_resident_ctas(int num_sms, int stage_bytes);
+// Shared memory that staging a chunk of the final draw's candidate rows
+// takes (K+1 target rows, and the K draft rows if with_q), or 0 when it is
+// not used (V not a multiple of 4, or above kStageMaxBytes).
+constexpr int kStageMaxBytes = 200 * 1024;
+int tail_stage_bytes(const Dims &d, bool with_q);
 
 // ---- truncated sampling: (M, S, cut) of every truncated row --------------
 struct TruncParams {

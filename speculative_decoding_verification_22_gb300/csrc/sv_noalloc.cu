@@ -203,6 +203,7 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
   // The array keeps the previous call's contents: clear the counters, flags
   // and status word this call relies on starting at zero.
   if (cudaMemsetAsync(arena, 0, zero_bytes, st) != cudaSuccess) return SV_ERR_CUDA;
+
   const unsigned epoch = 1;  // flags were just cleared to 0
   const uint64_t wait_limit_ns = 1000000000ull;
   const float inv_t = greedy ? 1.0f : static_cast<float>(1.0 / static_cast<double>(temperature));
@@ -273,6 +274,15 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
   T.draft_logits_ready = cfg->dtype == SV_BF16 ? 1 : 0;
   T.fast = fast ? 1 : 0;
   T.grid_parts = plan.grid;
-  T.coop = (fast && static_cast<int64_t>(D.B) * D.nchunk <= sv::tail_resident_ctas(sms)) ? 1 : 0;
+  const int64_t tail_ctas = static_cast<int64_t>(D.B) * D.nchunk;
+  const int stage_bytes = fast ? sv::tail_stage_bytes(D, true) : 0;
+  T.coop = 0;
+  T.stage_rows = 0;
+  if (stage_bytes > 0 && tail_ctas <= sv::tail_resident_ctas(sms, stage_bytes)) {
+    T.coop = 1;
+    T.stage_rows = D.K + 1 + (q_logits ? D.K : 0);
+  } else if (fast && tail_ctas <= sv::tail_resident_ctas(sms, 0)) {
+    T.coop = 1;
+  }
   return sv::launch_tail(T, st) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -360,7 +360,13 @@ __device__ void fast_row_stats(const TailParams &P, int b, float *s_lp_m, ff *s_
 // takes the same decision from the same inputs) the decision goes to that
 // shared-memory state instead of being published, and the accepted prefix
 // and count are written only if `emit` (by one of the CTAs).
+// kCoop compiles the cooperative path alone (sampling, no truncation, no
+// tree, row statistics from the contraction's pairs).
+template <bool kCoop>
 __device__ int decide(const TailParams &P, int b, SeqState *local = nullptr, bool emit = true) {
+  const bool greedy = !kCoop && P.greedy;
+  const int32_t *parents = kCoop ? nullptr : P.parents;
+  const int p_cut = kCoop ? 0 : P.p_cut, q_cut = kCoop ? 0 : P.q_cut;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = P.dims.K, rows = K + 1;
   const int64_t V = P.dims.V;
@@ -377,37 +383,45 @@ __device__ int decide(const TailParams &P, int b, SeqState *local = nullptr, boo
   // no draft distribution: the draft was proposed with certainty (q is a
   // point mass at each proposed token) and a -1 ends it early (not for a
   // tree, whose nodes all carry tokens)
-  const bool point = P.q_logits == nullptr && P.parents == nullptr;
+  const bool point = P.q_logits == nullptr && parents == nullptr;
   __shared__ int s_par[SV_MAX_K];               // tree: node parents
   __shared__ int s_depth[SV_MAX_K + 1];         // tree: depth of root / nodes
   __shared__ unsigned char s_match[SV_MAX_K + 1];
 
   // fast mode: this CTA computes the row statistics itself (warps 2..)
-  const bool fast = P.fast != 0;
+  const bool fast = kCoop || P.fast != 0;
   if (threadIdx.x == 0) s_err = 0;
   __syncthreads();
   // everything the walk needs, loaded in parallel
   if (threadIdx.x < rows) {
     const int i = threadIdx.x;
-    s_tp[i] = P.p_cut ? __ldcg(&P.w.row_tau[out0 + i]) : -INFINITY;
+    s_tp[i] = p_cut ? __ldcg(&P.w.row_tau[out0 + i]) : -INFINITY;
     if (!fast) {
       s_lp_m[i] = __ldcg(&P.w.row_m[out0 + i]);
       s_lp_s[i] = ld_ff(&P.w.row_s[out0 + i]);
     }
-    if (!P.greedy) s_u[i] = P.u[out0 + i];
+    if (!greedy) s_u[i] = P.u[out0 + i];
     if (!fast) {
       const bool fin = isfinite(s_lp_m[i]) &&
-                       (P.greedy || (s_lp_s[i].hi > 0.0f && s_lp_s[i].hi < INFINITY));
+                       (greedy || (s_lp_s[i].hi > 0.0f && s_lp_s[i].hi < INFINITY));
       if (!fin) atomicCAS(&s_err, 0, SV_ERR_NONFINITE);
     }
   }
   if (threadIdx.x >= 32 && threadIdx.x < 32 + K) {
     const int i = threadIdx.x - 32;
     const int x = P.draft[static_cast<int64_t>(b) * K + i];
+    // fast mode: the draft logit at the token and the token's exact logit
+    // do not depend on x; load them together with it
+    float ql_fast = 0.0f;
+    ff l_fast = ff_make(0.0f);
+    if (fast && !greedy) {
+      ql_fast = point ? 0.0f : __ldcg(&P.w.draft_q[static_cast<int64_t>(b) * K + i]);
+      l_fast = ld_ff(&P.w.draft_logit[static_cast<int64_t>(b) * K + i]);
+    }
     s_x[i] = x;
-    if (P.parents) {
+    if (parents) {
       // a parent must come before its child
-      const int pa = P.parents[static_cast<int64_t>(b) * K + i];
+      const int pa = parents[static_cast<int64_t>(b) * K + i];
       s_par[i] = pa;
       if (pa < -1 || pa >= i) atomicExch(&s_err, SV_ERR_TOKEN);
     }
@@ -415,7 +429,7 @@ __device__ int decide(const TailParams &P, int b, SeqState *local = nullptr, boo
       // end of a short draft (checked below)
     } else if (x < 0 || static_cast<int64_t>(x) >= V) {
       atomicExch(&s_err, SV_ERR_TOKEN);
-    } else if (!P.greedy) {
+    } else if (!greedy) {
       // a point-mass draft row holds M = 0, S = 1 and q_logits(x) counts
       // as 0, so the threshold below is p(x) / 1
       const int64_t rq = static_cast<int64_t>(R) + static_cast<int64_t>(b) * K + i;
@@ -424,14 +438,12 @@ __device__ int decide(const TailParams &P, int b, SeqState *local = nullptr, boo
         s_lq_s[i] = ld_ff(&P.w.row_s[rq]);
       }
       // fast mode: the contraction also left q_logits at the draft token
-      s_ql[i] = point ? 0.0f
-                      : fast ? __ldcg(&P.w.draft_q[static_cast<int64_t>(b) * K + i])
-                             : P.q_logits[(static_cast<int64_t>(b) * K + i) * V + x];
+      s_ql[i] = point ? 0.0f : fast ? ql_fast : P.q_logits[(static_cast<int64_t>(b) * K + i) * V + x];
       // truncated sampling: membership of x is decided on the same fp32
       // values the cut was found on
-      s_tq[i] = P.q_cut ? __ldcg(&P.w.row_tau[rq]) : -INFINITY;
-      s_lbuf[i] = P.p_cut ? __ldcg(&P.w.logits[(out0 + i) * V + x]) : 0.0f;
-      s_l[i] = ld_ff(&P.w.draft_logit[static_cast<int64_t>(b) * K + i]);
+      s_tq[i] = q_cut ? __ldcg(&P.w.row_tau[rq]) : -INFINITY;
+      s_lbuf[i] = p_cut ? __ldcg(&P.w.logits[(out0 + i) * V + x]) : 0.0f;
+      s_l[i] = fast ? l_fast : ld_ff(&P.w.draft_logit[static_cast<int64_t>(b) * K + i]);
       if (!fast) {
         const bool fin = isfinite(s_lq_m[i]) && s_lq_s[i].hi > 0.0f && s_lq_s[i].hi < INFINITY;
         if (!fin) atomicCAS(&s_err, 0, SV_ERR_NONFINITE);
@@ -479,7 +491,7 @@ __device__ int decide(const TailParams &P, int b, SeqState *local = nullptr, boo
     for (int i = threadIdx.x; i < P.split_cnt_n; i += kTailThreads) P.w.split_cnt[i] = 0;
   }
   if (s_err == 0) {
-    if (!P.greedy) {
+    if (!greedy) {
       // accept thresholds of the proposed positions, one thread each
       if (threadIdx.x < kb) {
         const int i = threadIdx.x;
@@ -490,8 +502,8 @@ __device__ int decide(const TailParams &P, int b, SeqState *local = nullptr, boo
         const float ratio = ff_to_f(ff_div(s_lq_s[i], s_lp_s[i]));
         // outside the truncated target: p(x) = 0, rejected; outside the
         // truncated draft only: q(x) = 0 < p(x), accepted (R2)
-        const bool keep_p = !P.p_cut || s_lbuf[i] >= s_tp[i];
-        const bool keep_q = !P.q_cut || s_ql[i] >= s_tq[i];
+        const bool keep_p = !p_cut || s_lbuf[i] >= s_tp[i];
+        const bool keep_q = !q_cut || s_ql[i] >= s_tq[i];
         const float thr =
             keep_p ? (keep_q ? accept_threshold(lp, lq, ratio) : INFINITY) : 0.0f;
         s_acc[i] = isfinite(l.hi) ? (s_u[i] < thr ? 1 : 0) : -1;
@@ -508,7 +520,7 @@ __device__ int decide(const TailParams &P, int b, SeqState *local = nullptr, boo
     int err = s_err;
     SeqState st = {};
     st.mode = kModeSkip;
-    if (err == 0 && !P.greedy) {
+    if (err == 0 && !greedy) {
       int n = kb, mode = kModeP;
       for (int i = 0; i < kb; ++i) {
         if (s_acc[i] < 0) {
@@ -550,7 +562,7 @@ __device__ int decide(const TailParams &P, int b, SeqState *local = nullptr, boo
       for (int i = 0; i <= kb; ++i) ok = ok && s_arg[i] >= 0;
       if (!ok) {
         err = SV_ERR_NONFINITE;
-      } else if (P.parents) {
+      } else if (parents) {
         // greedy tree verification: one pass over the nodes (parents come
         // first); row 0 is the root, row 1 + j node j
         s_depth[0] = 0;
@@ -608,7 +620,7 @@ __device__ int decide(const TailParams &P, int b, SeqState *local = nullptr, boo
       P.w.seq[b] = st;
       __threadfence();
       *reinterpret_cast<volatile unsigned *>(&P.w.seq_flag[b]) = P.epoch;
-      if (!P.greedy) {
+      if (!greedy) {
         __threadfence();
         s_fin = arrive_final(P, b);
       }
@@ -769,12 +781,13 @@ __device__ __forceinline__ bool wait_count(const int *cnt, int target, uint64_t 
 }
 
 // Cooperative selection (the whole tail grid resident at once): every chunk
-// CTA of sequence b publishes its mass and waits until all have; each then
-// locates the chunk holding u * S, and the CTA that computed that chunk
-// scans the weights it still holds.  A CTA whose wait for the other masses
-// ran out reports SV_ERR_TIMEOUT and marks the sequence; the last CTA past
-// the selection then withdraws a marked sequence (outputs -1) and rewinds
-// the sequence's counters.
+// CTA of sequence b publishes its mass and counts itself in; all but the
+// last to count in wait (bounded) until the count is complete.  Each CTA
+// then locates the chunk holding u * S, and the CTA that computed that
+// chunk scans the weights it still holds.  A CTA whose wait ran out
+// reports SV_ERR_TIMEOUT and marks the sequence; the last CTA past the
+// selection withdraws a marked sequence (outputs -1) and rewinds its
+// counters.
 __device__ void coop_select(const TailParams &P, int b, int c, const SeqState &st,
                             const float (&r)[kChunkPerThread], float tsum, ff mass) {
   __shared__ ff s_warp[kTailWarps];
@@ -787,8 +800,10 @@ __device__ void coop_select(const TailParams &P, int b, int c, const SeqState &s
   if (threadIdx.x == 0) {
     st_ff(&masses[c], mass);
     __threadfence();
-    atomicAdd(&P.w.chunk_count[b], 1);
-    s_all = wait_count(&P.w.chunk_count[b], nchunk, P.wait_limit_ns) ? 1 : 0;
+    const int before = atomicAdd(&P.w.chunk_count[b], 1);
+    s_all = (before == nchunk - 1 || wait_count(&P.w.chunk_count[b], nchunk, P.wait_limit_ns))
+                ? 1
+                : 0;
   }
   __syncthreads();
   if (s_all && st.mode != kModeSkip) {
@@ -866,10 +881,8 @@ __global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const TailParams 
   __shared__ int s_last;
   const int K = P.dims.K;
   const int R = P.dims.R;
-  // cooperative selection: chunk CTAs only (each takes its sequence's
-  // decision itself); fast mode: one decision CTA per sequence; otherwise
-  // one CTA per row
-  const int nrow = P.coop ? 0 : P.fast ? P.dims.B : P.greedy ? R : R + P.dims.RQ;
+  // fast mode: one decision CTA per sequence; otherwise one CTA per row
+  const int nrow = P.fast ? P.dims.B : P.greedy ? R : R + P.dims.RQ;
   if (threadIdx.x == 0) s_ticket = atomicAdd(P.w.ticket, 1u);
   __syncthreads();
   const int t = static_cast<int>(s_ticket);
@@ -884,7 +897,7 @@ __global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const TailParams 
   }
 
   if (t < nrow && P.fast) {
-    finalize_sequence(P, t, decide(P, t));
+    finalize_sequence(P, t, decide<false>(P, t));
   } else if (t < nrow) {
     // ---- row statistics ----
     const bool qrow = t >= R;
@@ -995,21 +1008,7 @@ __global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const TailParams 
       }
     }
     __syncthreads();
-    if (s_last) finalize_sequence(P, b, decide(P, b));
-  } else if (P.coop) {
-    // ---- cooperative chunk: the sequence's decision, taken here as in
-    // every chunk CTA of the sequence (the first writes the accepted
-    // prefix), this chunk's mass, then the cooperative selection ----
-    const int b = t / P.dims.nchunk, c = t % P.dims.nchunk;
-    __shared__ SeqState s_st;
-    decide(P, b, &s_st, c == 0);
-    const SeqState st = s_st;
-    float r[kChunkPerThread];
-#pragma unroll
-    for (int j = 0; j < kChunkPerThread; ++j) r[j] = 0.0f;
-    const float m = st.mode != kModeSkip ? chunk_weights(P, st, c, r) : 0.0f;
-    const ff mass = block_sum_ff(ff_make(m), s_wff);
-    coop_select(P, b, c, st, r, m, mass);
+    if (s_last) finalize_sequence(P, b, decide<false>(P, b));
   } else {
     // ---- residual chunk ----
     const int idx = t - nrow;
@@ -1065,18 +1064,153 @@ __global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const TailParams 
   }
 }
 
-int tail_resident_ctas(int num_sms) {
+// 1-D bulk copy (TMA) of `bytes` from global to this CTA's shared memory,
+// completing on the mbarrier; both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// The weights of chunk c from the rows staged in shared memory (stage row
+// j <= K: target row j of the sequence; K+1+j: draft row j); the same
+// arithmetic as chunk_weights.
+__device__ __forceinline__ float staged_weights(const TailParams &P, const SeqState &st, int b,
+                                                int c, const float *stage,
+                                                float (&r)[kChunkPerThread]) {
+  const int K = P.dims.K;
+  const int64_t V = P.dims.V;
+  const int i0 = threadIdx.x * kChunkPerThread;
+  const int64_t v0 = static_cast<int64_t>(c) * kChunk + i0;
+  const float *ls = stage + static_cast<int64_t>(st.p_row - b * (K + 1)) * kChunk + i0;
+  const bool resid = st.mode == kModeResidual;
+  const float *qs =
+      resid ? stage + static_cast<int64_t>(K + 1 + st.q_row - b * K) * kChunk + i0 : nullptr;
+  float l[kChunkPerThread], q[kChunkPerThread];
+#pragma unroll
+  for (int j = 0; j < kChunkPerThread; j += 4) {
+    const bool in = v0 + j < V;  // V % 4 == 0: a group of four is all in or all out
+    const float4 a = in ? *reinterpret_cast<const float4 *>(ls + j) : make_float4(0, 0, 0, 0);
+    const float4 e = (in && resid) ? *reinterpret_cast<const float4 *>(qs + j) : make_float4(0, 0, 0, 0);
+    l[j] = a.x; l[j + 1] = a.y; l[j + 2] = a.z; l[j + 3] = a.w;
+    q[j] = e.x; q[j + 1] = e.y; q[j + 2] = e.z; q[j + 3] = e.w;
+  }
+  float sum = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kChunkPerThread; ++j) {
+    r[j] = v0 + j < V ? draw_weight(st, v0 + j, l[j], q[j], P.inv_t) : 0.0f;
+    sum = __fadd_rn(sum, r[j]);
+  }
+  return sum;
+}
+
+// The cooperative tail, when the whole grid is resident at once: CTA
+// b * nchunk + c is chunk c of sequence b.  With P.stage_rows it first
+// copies its chunk of every row the final draw may use (the K+1 target
+// rows, then the K draft rows) into shared memory, one bulk copy per row,
+// which lands while it takes the sequence's decision itself (as every chunk
+// CTA of the sequence does, from the same inputs; the first writes the
+// accepted prefix).  Then it computes its chunk's mass and runs the
+// cooperative selection.  No CTA waits for another except in that
+// selection.
+__global__ void __launch_bounds__(kTailThreads, 2) tail_coop_kernel(const TailParams P) {
+  extern __shared__ __align__(1024) unsigned char stage_raw[];
+  __shared__ ff s_wff[kTailWarps];
+  __shared__ SeqState s_st;
+  __shared__ __align__(8) uint64_t s_stage_bar;
+  __shared__ int s_staged;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int nchunk = P.dims.nchunk;
+  const int b = static_cast<int>(blockIdx.x) / nchunk, c = static_cast<int>(blockIdx.x) % nchunk;
+  const uint32_t bar = smem_u32(&s_stage_bar);
+  if (P.stage_rows && threadIdx.x == 0) {
+    const int K = P.dims.K;
+    const int64_t V = P.dims.V;
+    const int64_t v0 = static_cast<int64_t>(c) * kChunk;
+    const uint32_t bytes = static_cast<uint32_t>((V - v0 < kChunk ? V - v0 : kChunk) * 4);
+    mbar_init(bar, 1);
+    mbar_fence_init();
+    mbar_arrive_expect_tx(bar, bytes * static_cast<uint32_t>(P.stage_rows));
+    const uint32_t dst0 = smem_u32(stage_raw);
+    for (int j = 0; j < P.stage_rows; ++j) {
+      const float *row = j <= K ? P.w.logits + (static_cast<int64_t>(b) * (K + 1) + j) * V
+                                : P.q_logits + (static_cast<int64_t>(b) * K + (j - K - 1)) * V;
+      bulk_load(dst0 + static_cast<uint32_t>(j) * kChunk * 4, row + v0, bytes, bar);
+    }
+  }
+  if (P.stall && blockIdx.x == 0 && threadIdx.x == 0) {
+    // test of the timeout path (see tail_kernel)
+    if (!wait_flag(reinterpret_cast<const unsigned *>(P.w.never), 1u, P.wait_limit_ns)) {
+      set_status(P.w.status, SV_ERR_TIMEOUT);
+      atomicOr(&P.w.seq_final[0], kPoisoned);
+      __threadfence();
+    }
+  }
+  decide<true>(P, b, &s_st, c == 0);
+  if (P.stage_rows && threadIdx.x == 0) {
+    // the copies must have landed before the rows are read, and before the
+    // CTA may exit
+    const int never = 0;
+    s_staged = mbar_wait(bar, 0u, P.wait_limit_ns, &never) ? 1 : 0;
+  }
+  __syncthreads();
+  SeqState st = s_st;
+  if (P.stage_rows && !s_staged) {
+    if (threadIdx.x == 0) {
+      set_status(P.w.status, SV_ERR_TIMEOUT);
+      atomicOr(&P.w.seq_final[b], kPoisoned);
+    }
+    st.mode = kModeSkip;
+  }
+  float r[kChunkPerThread];
+#pragma unroll
+  for (int j = 0; j < kChunkPerThread; ++j) r[j] = 0.0f;
+  float m = 0.0f;
+  if (st.mode != kModeSkip)
+    m = P.stage_rows ? staged_weights(P, st, b, c, reinterpret_cast<const float *>(stage_raw), r)
+                     : chunk_weights(P, st, c, r);
+  const ff mass = block_sum_ff(ff_make(m), s_wff);
+  coop_select(P, b, c, st, r, m, mass);
+}
+
+int tail_resident_ctas(int num_sms, int stage_bytes) {
+  if (stage_bytes > 0 &&
+      cudaFuncSetAttribute(tail_coop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           stage_bytes) != cudaSuccess)
+    return 0;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tail_kernel, kTailThreads, 0) !=
-      cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tail_coop_kernel, kTailThreads,
+                                                    stage_bytes) != cudaSuccess)
     return 0;
   return per_sm * num_sms;
 }
 
+int tail_stage_bytes(const Dims &d, bool with_q) {
+  const int rows = d.K + 1 + (with_q ? d.K : 0);
+  const int64_t bytes = static_cast<int64_t>(rows) * kChunk * 4;
+  return (d.V % 4 == 0 && bytes <= kStageMaxBytes) ? static_cast<int>(bytes) : 0;
+}
+
 cudaError_t launch_tail(const TailParams &P, cudaStream_t stream) {
-  const int nrow = P.coop ? 0 : P.fast ? P.dims.B : P.greedy ? P.dims.R : P.dims.R + P.dims.RQ;
-  const int nchunk_ctas = P.greedy ? 0 : P.dims.B * P.dims.nchunk;
   void *args[] = {const_cast<TailParams *>(&P)};
+  if (P.coop) {
+    const size_t smem = static_cast<size_t>(P.stage_rows) * kChunk * 4;
+    // the opt-in above 48 KB is per device; idempotent and cheap
+    if (smem > 48 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          tail_coop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(reinterpret_cast<const void *>(&tail_coop_kernel),
+                      dim3(P.dims.B * P.dims.nchunk), dim3(kTailThreads), smem, stream, args);
+  }
+  const int nrow = P.fast ? P.dims.B : P.greedy ? P.dims.R : P.dims.R + P.dims.RQ;
+  const int nchunk_ctas = P.greedy ? 0 : P.dims.B * P.dims.nchunk;
   return launch_pdl(reinterpret_cast<const void *>(&tail_kernel), dim3(nrow + nchunk_ctas),
                     dim3(kTailThreads), 0, stream, args);
 }
