@@ -46,7 +46,7 @@ namespace tc {
 #define SV_TC_DRAIN_SLOTS 32
 #endif
 #ifndef SV_TC_STAGES_C2
-#define SV_TC_STAGES_C2 5
+#define SV_TC_STAGES_C2 6
 #endif
 #ifndef SV_TC_STAGES_C4
 #define SV_TC_STAGES_C4 2

@@ -215,7 +215,7 @@ def test_contraction_plan_fits_the_gpu_for_every_shape(lib):
 
 def test_contraction_plan_of_the_benchmark_shapes(lib):
     p = sv.spec_verify_plan(128256, 4096, 1, 4)
-    assert (p["drain_cols"], p["chunks"], p["stages"], p["grid"]) == (16, 2, 5, 152)
+    assert (p["drain_cols"], p["chunks"], p["stages"], p["grid"]) == (16, 2, 6, 152)
     p = sv.spec_verify_plan(128256, 4096, 8, 7)
     assert p["drain_cols"] == 64 and p["tmem_slots"] == 8
     p = sv.spec_verify_plan(128256, 4096, 64, 5)
