@@ -146,6 +146,30 @@ int spec_verify_run_host(spec_verify_t *h, const void *hidden_host,
                          float temperature, int32_t *out_tokens_host,
                          int32_t *out_n_accepted_host);
 
+/* End-to-end rounds from HOST buffers, double-buffered, for a caller with
+ * independent rounds to verify back to back (two groups of sequences that
+ * alternate, or replicas of a benchmark); a decode loop whose next round
+ * needs this round's tokens gains nothing over spec_verify_run_host.
+ * spec_verify_submit_host enqueues a round in slot 0 or 1 and returns
+ * without waiting: its inputs are copied into the slot's own device buffers
+ * on a host-to-device stream (so the copies overlap the kernels of the
+ * other slot's round), the step runs on the handle's stream after them, and
+ * out_tokens / out_n_accepted and the status word are copied back on a
+ * device-to-host stream.  spec_verify_wait_host(h, slot) waits for that
+ * round and returns its status (SV_OK, or the device status word, which it
+ * then clears).  The host buffers of a submitted round must stay valid, and
+ * its outputs unread, until the wait returns; a slot must be waited for
+ * before it is submitted again.  The first submit allocates the two slots'
+ * buffers, streams and events (later calls allocate nothing).  Arguments
+ * and errors as spec_verify_run_host, and SV_ERR_ARG for a slot other than
+ * 0 or 1, a busy slot (submit) or an idle one (wait). */
+int spec_verify_submit_host(spec_verify_t *h, int slot, const void *hidden_host,
+                            const void *W_lm, const int32_t *draft_tokens_host,
+                            const float *q_logits_host, const float *uniforms_host,
+                            float temperature, int32_t *out_tokens_host,
+                            int32_t *out_n_accepted_host);
+int spec_verify_wait_host(spec_verify_t *h, int slot);
+
 /* Synchronises the handle's stream, then returns and clears the device
  * status word (SV_OK if no device-side error occurred since the last call),
  * or SV_ERR_CUDA if synchronisation failed. */
@@ -233,18 +257,26 @@ void spec_verify_destroy(spec_verify_t *h);
  * the library, which every GPU that loads the library holds until the
  * process exits.  (The pages describe no such mode; this is a property of
  * the library, not of the method.)
- *   cfg            shape, dtype and stream, as for spec_verify_create
+ *   cfg            shape, dtype (SV_BF16 or SV_FP32) and stream, as for
+ *                  spec_verify_create
  *   other arguments as for spec_verify_run
  * The first call on a device looks up that device's copy of the array
  * (cudaGetSymbolAddress); make it before any stream capture.  Every call
  * reuses the same array and clears the counters it needs at its start, so
  * calls that may overlap on the GPU (different streams, or different host
  * threads on the same device) race and must be serialised by the caller.
- * Errors (returned): as spec_verify_run, and SV_ERR_SHAPE if the scratch
- * for this shape exceeds the array (about R*V*4 bytes of logits plus small
- * tables; the Llama-8B-shaped step needs about 5.5 MiB).  Errors found on
- * the device are not reported through a status word: the affected
- * sequences get out_n_accepted = -1 and out_tokens = -1. */
+ * The scratch of a call is about 4*R*V bytes of logits (R = B*(K+1)),
+ * 8*(R + B*K)*ceil(V/32) of softmax partials, 1 KiB per column and
+ * contraction CTA of stream-K split tiles (up to 152 CTAs, columns = R
+ * rounded up to 16), 16*(R + B*K) per CTA of row statistics and small
+ * tables: 5.1 MiB for V = 128256, d = 4096, B = 1, K = 4; 15.7 MiB for
+ * d = 8192, B = 4, K = 4; 29.1 MiB for d = 4096, B = 8, K = 4.  B = 8,
+ * K = 7 at V = 128256 (44.8 MiB) does not fit.
+ * Errors (returned): as spec_verify_run, SV_ERR_SHAPE if the scratch for
+ * this shape exceeds the array, SV_ERR_ARG if cfg->dtype is not SV_BF16
+ * or SV_FP32.  Errors found on the device are not reported through a
+ * status word: the affected sequences get out_n_accepted = -1 and
+ * out_tokens = -1. */
 int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidden, const void *W_lm,
                             const int32_t *draft_tokens, const float *q_logits,
                             const float *uniforms, float temperature, int32_t *out_tokens,

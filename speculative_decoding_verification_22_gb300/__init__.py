@@ -43,7 +43,7 @@ EXPORTS = ("spec_verify_create", "spec_verify_run", "spec_verify_run_host",
            "spec_verify_strerror", "spec_verify_destroy",
            "spec_verify_run_noalloc", "spec_ngram_draft", "spec_verify_run_truncated",
            "spec_verify_tree_greedy", "spec_verify_run_fp8", "spec_verify_plan",
-           "spec_verify_debug_stall")
+           "spec_verify_debug_stall", "spec_verify_submit_host", "spec_verify_wait_host")
 
 
 class sv_plan_t(ctypes.Structure):
@@ -88,6 +88,9 @@ def load_library():
         lib.spec_verify_debug_lse.argtypes = [vp, vp]
         lib.spec_verify_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
         lib.spec_verify_debug_stall.argtypes = [vp, ctypes.c_int]
+        lib.spec_verify_submit_host.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp, f32, vp,
+                                                vp]
+        lib.spec_verify_wait_host.argtypes = [vp, ctypes.c_int]
         lib.spec_verify_timing.argtypes = [vp, ctypes.c_int]
         lib.spec_verify_timing_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double),
                                                 ctypes.POINTER(i64)]
@@ -179,6 +182,21 @@ def spec_verify_run_host(h, hidden, W_lm, draft_tokens, q_logits, uniforms,
         h, _ptr(hidden), _ptr(W_lm), _ptr(draft_tokens), _ptr(q_logits),
         _ptr(uniforms), float(temperature), _ptr(out_tokens),
         _ptr(out_n_accepted)), "spec_verify_run_host")
+
+
+def spec_verify_submit_host(h, slot: int, hidden, W_lm, draft_tokens, q_logits, uniforms,
+                            temperature: float, out_tokens, out_n_accepted) -> None:
+    """Double-buffered host round: enqueue it in slot 0 or 1 (pinned host
+    tensors for inputs and outputs, W_lm on the device) and return."""
+    _check(load_library().spec_verify_submit_host(
+        h, int(slot), _ptr(hidden), _ptr(W_lm), _ptr(draft_tokens), _ptr(q_logits),
+        _ptr(uniforms), float(temperature), _ptr(out_tokens), _ptr(out_n_accepted)),
+        "spec_verify_submit_host")
+
+
+def spec_verify_wait_host(h, slot: int) -> int:
+    """Waits for the round in `slot`; returns its status code."""
+    return int(load_library().spec_verify_wait_host(h, int(slot)))
 
 
 def spec_verify_status(h) -> int:

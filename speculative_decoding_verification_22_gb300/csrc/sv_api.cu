@@ -56,6 +56,17 @@ struct spec_verify {
   float *st_u = nullptr;
   int32_t *st_tokens = nullptr;
   int32_t *st_n = nullptr;
+  // double-buffered host rounds (spec_verify_submit_host), set up on first use
+  struct Slot {
+    void *hidden = nullptr;
+    int32_t *draft = nullptr, *tokens = nullptr, *n = nullptr;
+    float *q = nullptr, *u = nullptr;
+    int *status_host = nullptr;  // pinned: the status word after the round
+    cudaEvent_t copied = nullptr, kernels = nullptr, done = nullptr;
+    bool busy = false;
+  } slot[2];
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  bool pipe_ready = false;
   // TMA descriptors, re-encoded when the tensor moves
   CUtensorMap tmW{}, tmH{};
   const void *tmW_ptr = nullptr, *tmH_ptr = nullptr;
@@ -88,6 +99,17 @@ void free_all(spec_verify *h) {
     if (p) cudaFree(p);
   for (cudaEvent_t e : h->ev0) cudaEventDestroy(e);
   for (cudaEvent_t e : h->ev1) cudaEventDestroy(e);
+  for (auto &sl : h->slot) {
+    void *dp[] = {sl.hidden, sl.draft, sl.tokens, sl.n, sl.q, sl.u};
+    for (void *p : dp)
+      if (p) cudaFree(p);
+    if (sl.status_host) cudaFreeHost(sl.status_host);
+    cudaEvent_t ev[] = {sl.copied, sl.kernels, sl.done};
+    for (cudaEvent_t e : ev)
+      if (e) cudaEventDestroy(e);
+  }
+  if (h->h2d) cudaStreamDestroy(h->h2d);
+  if (h->d2h) cudaStreamDestroy(h->d2h);
 }
 
 template <typename T>
@@ -646,6 +668,92 @@ int spec_verify_run_host(spec_verify_t *h, const void *hidden_host, const void *
   if (cudaMemcpy(&code, h->w.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return SV_ERR_CUDA;
   return code == 0 ? SV_OK : spec_verify_status(h);
+}
+
+namespace {
+
+// Staging buffers, pinned status words, events and the two copy streams of
+// the double-buffered host rounds (first use only).
+int pipe_setup(spec_verify_t *h) {
+  if (h->pipe_ready) return SV_OK;
+  const sv::Dims &D = h->dims;
+  const size_t es = esize(h->cfg.dtype);
+  bool ok = cudaStreamCreateWithFlags(&h->h2d, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&h->d2h, cudaStreamNonBlocking) == cudaSuccess;
+  for (auto &sl : h->slot) {
+    ok = ok && dalloc(reinterpret_cast<uint8_t **>(&sl.hidden), static_cast<size_t>(D.R) * D.d * es) &&
+         dalloc(&sl.draft, static_cast<size_t>(D.RQ)) &&
+         dalloc(&sl.q, static_cast<size_t>(D.RQ) * D.V) && dalloc(&sl.u, D.R) &&
+         dalloc(&sl.tokens, D.R) && dalloc(&sl.n, D.B) &&
+         cudaMallocHost(reinterpret_cast<void **>(&sl.status_host), sizeof(int)) == cudaSuccess &&
+         cudaEventCreateWithFlags(&sl.copied, cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&sl.kernels, cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming) == cudaSuccess;
+  }
+  if (!ok) return SV_ERR_CUDA;
+  h->pipe_ready = true;
+  return SV_OK;
+}
+
+}  // namespace
+
+int spec_verify_submit_host(spec_verify_t *h, int slot, const void *hidden_host,
+                            const void *W_lm, const int32_t *draft_tokens_host,
+                            const float *q_logits_host, const float *uniforms_host,
+                            float temperature, int32_t *out_tokens_host,
+                            int32_t *out_n_accepted_host) {
+  if (!h || slot < 0 || slot > 1 || !hidden_host || !W_lm || !out_tokens_host ||
+      !out_n_accepted_host)
+    return SV_ERR_ARG;
+  if (h->cfg.dtype == SV_FP8) return SV_ERR_ARG;  // no host path for the FP8 scales
+  const sv::Dims &D = h->dims;
+  const bool greedy = temperature == 0.0f;
+  if (D.K > 0 && !draft_tokens_host) return SV_ERR_ARG;
+  if (!greedy && !uniforms_host) return SV_ERR_ARG;
+  if (int rc = pipe_setup(h)) return rc;
+  auto &sl = h->slot[slot];
+  if (sl.busy) return SV_ERR_ARG;  // wait for this slot's previous round first
+  const size_t es = esize(h->cfg.dtype);
+  // inputs: on the host-to-device stream, free to overlap the other slot's kernels
+  if (cudaMemcpyAsync(sl.hidden, hidden_host, static_cast<size_t>(D.R) * D.d * es,
+                      cudaMemcpyHostToDevice, h->h2d) != cudaSuccess ||
+      (D.K > 0 && cudaMemcpyAsync(sl.draft, draft_tokens_host, sizeof(int32_t) * D.RQ,
+                                  cudaMemcpyHostToDevice, h->h2d) != cudaSuccess) ||
+      (!greedy && D.K > 0 && q_logits_host &&
+       cudaMemcpyAsync(sl.q, q_logits_host, sizeof(float) * static_cast<size_t>(D.RQ) * D.V,
+                       cudaMemcpyHostToDevice, h->h2d) != cudaSuccess) ||
+      (!greedy && cudaMemcpyAsync(sl.u, uniforms_host, sizeof(float) * D.R,
+                                  cudaMemcpyHostToDevice, h->h2d) != cudaSuccess) ||
+      cudaEventRecord(sl.copied, h->h2d) != cudaSuccess ||
+      cudaStreamWaitEvent(h->stream, sl.copied, 0) != cudaSuccess)
+    return SV_ERR_CUDA;
+  // the step, on the handle's stream (kernels only)
+  const int rc = spec_verify_run(h, sl.hidden, W_lm, D.K > 0 ? sl.draft : nullptr,
+                                 q_logits_host ? sl.q : nullptr, greedy ? nullptr : sl.u,
+                                 temperature, sl.tokens, sl.n);
+  if (rc != SV_OK) return rc;
+  // outputs and the status word: on the device-to-host stream
+  if (cudaEventRecord(sl.kernels, h->stream) != cudaSuccess ||
+      cudaStreamWaitEvent(h->d2h, sl.kernels, 0) != cudaSuccess ||
+      cudaMemcpyAsync(out_tokens_host, sl.tokens, sizeof(int32_t) * D.R, cudaMemcpyDeviceToHost,
+                      h->d2h) != cudaSuccess ||
+      cudaMemcpyAsync(out_n_accepted_host, sl.n, sizeof(int32_t) * D.B, cudaMemcpyDeviceToHost,
+                      h->d2h) != cudaSuccess ||
+      cudaMemcpyAsync(sl.status_host, h->w.status, sizeof(int), cudaMemcpyDeviceToHost,
+                      h->d2h) != cudaSuccess ||
+      cudaEventRecord(sl.done, h->d2h) != cudaSuccess)
+    return SV_ERR_CUDA;
+  sl.busy = true;
+  return SV_OK;
+}
+
+int spec_verify_wait_host(spec_verify_t *h, int slot) {
+  if (!h || slot < 0 || slot > 1 || !h->pipe_ready || !h->slot[slot].busy) return SV_ERR_ARG;
+  auto &sl = h->slot[slot];
+  sl.busy = false;
+  if (cudaEventSynchronize(sl.done) != cudaSuccess) return SV_ERR_CUDA;
+  // a device-side error: read and clear the status word (synchronises)
+  return *sl.status_host == 0 ? SV_OK : spec_verify_status(h);
 }
 
 int spec_verify_debug_logits(spec_verify_t *h, float *dst) {

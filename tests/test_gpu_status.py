@@ -151,3 +151,37 @@ def test_run_host_matches_device_run(setup):
                             host["uniforms"], 1.0, ht, hn)
     assert torch.equal(ht, tok_d.cpu()) and torch.equal(hn, n_d.cpu())
     assert eng.status() == sv.SV_OK
+
+
+def test_double_buffered_host_rounds_match_device_runs(setup):
+    """spec_verify_submit_host / spec_verify_wait_host: rounds alternate
+    between the two slots with different inputs each; every round's host
+    outputs equal the device run on the same inputs, and a busy slot (or an
+    idle one) is refused."""
+    dev, wl, W, W_np, inp, eng = setup
+    keys = ("hidden", "draft", "q_logits", "uniforms")
+    rounds = [si.make_round(wl, W, seed=300 + i) for i in range(6)]
+    host = [{k: r[k].cpu().pin_memory() for k in keys} for r in rounds]
+    ht = [torch.empty((wl.B, wl.K + 1), dtype=torch.int32).pin_memory() for _ in range(2)]
+    hn = [torch.empty((wl.B,), dtype=torch.int32).pin_memory() for _ in range(2)]
+    got = []
+    for i, hbuf in enumerate(host):
+        s = i % 2
+        if i >= 2:
+            assert sv.spec_verify_wait_host(eng.h, s) == sv.SV_OK
+            got.append((ht[s].clone(), hn[s].clone()))
+        sv.spec_verify_submit_host(eng.h, s, hbuf["hidden"], W, hbuf["draft"], hbuf["q_logits"],
+                                   hbuf["uniforms"], 1.0, ht[s], hn[s])
+        if i == 0:
+            with pytest.raises(sv.SpecVerifyError) as e:
+                sv.spec_verify_submit_host(eng.h, 0, hbuf["hidden"], W, hbuf["draft"],
+                                           hbuf["q_logits"], hbuf["uniforms"], 1.0, ht[0], hn[0])
+            assert e.value.code == sv.SV_ERR_ARG
+    for s in (0, 1):
+        assert sv.spec_verify_wait_host(eng.h, s) == sv.SV_OK
+        got.append((ht[s].clone(), hn[s].clone()))
+    assert sv.spec_verify_wait_host(eng.h, 0) == sv.SV_ERR_ARG
+    for r, (t, n) in zip(rounds, got):
+        ref_t, ref_n = eng.run(r["hidden"], W, r["draft"], r["q_logits"], r["uniforms"], 1.0)
+        assert torch.equal(t, ref_t.cpu()) and torch.equal(n, ref_n.cpu())
+    assert eng.status() == sv.SV_OK
