@@ -330,6 +330,8 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out) {
          cudaMemset(h->w.chunk_count, 0, sizeof(int) * D.B) == cudaSuccess &&
          cudaMemset(h->w.chunk_done, 0, sizeof(int) * D.B) == cudaSuccess &&
          cudaMemset(h->w.never, 0, sizeof(int)) == cudaSuccess &&
+         // chunk masses start unset (all-ones bits); every launch leaves them so
+         cudaMemset(h->w.chunk_mass, 0xFF, 2 * sizeof(float2) * D.B * D.nchunk) == cudaSuccess &&
 
          cudaMemset(h->w.seq_flag, 0, sizeof(unsigned) * D.B) == cudaSuccess &&
          cudaMemset(h->w.seq_final, 0, sizeof(int) * D.B) == cudaSuccess &&

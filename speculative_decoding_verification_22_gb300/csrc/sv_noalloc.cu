@@ -203,6 +203,9 @@ extern "C" int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidde
   // The array keeps the previous call's contents: clear the counters, flags
   // and status word this call relies on starting at zero.
   if (cudaMemsetAsync(arena, 0, zero_bytes, st) != cudaSuccess) return SV_ERR_CUDA;
+  // chunk masses start unset (all-ones bits): the cooperative selection waits for them
+  if (cudaMemsetAsync(w.chunk_mass, 0xFF, sizeof(float2) * D.B * D.nchunk, st) != cudaSuccess)
+    return SV_ERR_CUDA;
 
   const unsigned epoch = 1;  // flags were just cleared to 0
   const uint64_t wait_limit_ns = 1000000000ull;

@@ -638,9 +638,11 @@ __device__ int decide(const TailParams &P, int b, SeqState *local = nullptr, boo
 // there are at most 32 chunks.  Leaves S, the chunk, the mass before it and
 // the target u * S in shared memory.
 __device__ __forceinline__ void locate_chunk(const float2 *mass, int nchunk, float u, int lane,
-                                             ff &s_S, ff &s_base, ff &s_target, int &s_chunk) {
+                                             ff &s_S, ff &s_base, ff &s_target, int &s_chunk,
+                                             const ff *held = nullptr) {
+  // held: this lane's mass (chunk `lane`), already loaded, when nchunk <= 32
   const bool one = nchunk <= 32;
-  const ff m0 = (one && lane < nchunk) ? ld_ff(&mass[lane]) : ff_make(0.0f);
+  const ff m0 = (one && lane < nchunk) ? (held ? *held : ld_ff(&mass[lane])) : ff_make(0.0f);
   ff S = m0;
   if (!one)
     for (int c = lane + 32; c < nchunk; c += 32) S = ff_add(S, ld_ff(&mass[c]));
@@ -686,6 +688,36 @@ __device__ __forceinline__ void locate_chunk(const float2 *mass, int nchunk, flo
     s_base = base;
     s_target = target;
   }
+}
+
+// Chunk masses not yet published hold all-ones bits (a NaN pair, which no
+// mass can be); every launch leaves them so.  A mass is published, and
+// polled, as one 64-bit access, so a reader sees either the sentinel or the
+// whole pair.
+constexpr unsigned long long kMassUnset = ~0ull;
+
+__device__ __forceinline__ void publish_mass(float2 *slot, ff m) {
+  const unsigned long long bits =
+      (static_cast<unsigned long long>(__float_as_uint(m.lo)) << 32) | __float_as_uint(m.hi);
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(slot), "l"(bits) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long peek_mass(const float2 *slot) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(slot) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ ff mass_of(unsigned long long bits) {
+  return ff{__uint_as_float(static_cast<unsigned>(bits)), __uint_as_float(static_cast<unsigned>(bits >> 32))};
+}
+
+// Rewinds sequence b's masses to the sentinel (one thread; after everything
+// that reads them in this launch).
+__device__ __forceinline__ void unset_masses(const TailParams &P, int b) {
+  unsigned long long *m = reinterpret_cast<unsigned long long *>(
+      P.w.chunk_mass + static_cast<int64_t>(b) * P.dims.nchunk);
+  for (int c = 0; c < P.dims.nchunk; ++c) m[c] = kMassUnset;
 }
 
 // The inverse CDF inside the chunk that holds the target: a block scan of
@@ -781,13 +813,14 @@ __device__ __forceinline__ bool wait_count(const int *cnt, int target, uint64_t 
 }
 
 // Cooperative selection (the whole tail grid resident at once): every chunk
-// CTA of sequence b publishes its mass and counts itself in; all but the
-// last to count in wait (bounded) until the count is complete.  Each CTA
-// then locates the chunk holding u * S, and the CTA that computed that
-// chunk scans the weights it still holds.  A CTA whose wait ran out
-// reports SV_ERR_TIMEOUT and marks the sequence; the last CTA past the
-// selection withdraws a marked sequence (outputs -1) and rewinds its
-// counters.
+// CTA of sequence b publishes its mass (one 64-bit store over the unset
+// sentinel); warp 0 of every CTA polls the sequence's masses, one slot per
+// lane, with relaxed loads (a warp's slots share two cache lines) until
+// none is unset (bounded), and locates the chunk holding u * S from the
+// values it polled; the CTA that computed that chunk scans the weights it
+// still holds.  A CTA whose wait ran out reports SV_ERR_TIMEOUT and marks
+// the sequence; the last CTA past the selection withdraws a marked
+// sequence (outputs -1) and rewinds its counter and masses.
 __device__ void coop_select(const TailParams &P, int b, int c, const SeqState &st,
                             const float (&r)[kChunkPerThread], float tsum, ff mass) {
   __shared__ ff s_warp[kTailWarps];
@@ -797,19 +830,32 @@ __device__ void coop_select(const TailParams &P, int b, int c, const SeqState &s
   const int nchunk = P.dims.nchunk;
   float2 *masses = P.w.chunk_mass + static_cast<int64_t>(b) * nchunk;
   const int64_t rows = P.dims.K + 1;
-  if (threadIdx.x == 0) {
-    st_ff(&masses[c], mass);
-    __threadfence();
-    const int before = atomicAdd(&P.w.chunk_count[b], 1);
-    s_all = (before == nchunk - 1 || wait_count(&P.w.chunk_count[b], nchunk, P.wait_limit_ns))
-                ? 1
-                : 0;
+  if (threadIdx.x == 0) publish_mass(&masses[c], mass);
+  if (threadIdx.x < 32) {
+    bool all = true;
+    ff held = ff_make(0.0f);
+    for (int c0 = lane; c0 < nchunk && all; c0 += 32) {
+      unsigned long long v = peek_mass(&masses[c0]);
+      if (v == kMassUnset) {
+        const uint64_t t0 = globaltimer();
+        while ((v = peek_mass(&masses[c0])) == kMassUnset) {
+          if (globaltimer() - t0 >= P.wait_limit_ns) {
+            all = false;
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
+      if (c0 == lane) held = mass_of(v);
+    }
+    all = __all_sync(0xffffffffu, all);
+    if (all && st.mode != kModeSkip)
+      locate_chunk(masses, nchunk, st.u_final, lane, s_S, s_base, s_target, s_chunk,
+                   nchunk <= 32 ? &held : nullptr);
+    if (lane == 0) s_all = all ? 1 : 0;
   }
   __syncthreads();
   if (s_all && st.mode != kModeSkip) {
-    if (threadIdx.x < 32)
-      locate_chunk(masses, nchunk, st.u_final, lane, s_S, s_base, s_target, s_chunk);
-    __syncthreads();
     if (!(s_S.hi > 0.0f)) {
       // an empty residual (or no mass at all): the first chunk CTA draws
       // alone, with masses of its own in the second half of chunk_mass
@@ -833,7 +879,7 @@ __device__ void coop_select(const TailParams &P, int b, int c, const SeqState &s
         for (int i = 0; i < rows; ++i) P.out_tokens[static_cast<int64_t>(b) * rows + i] = -1;
         P.out_n[b] = -1;
       }
-      P.w.chunk_count[b] = 0;
+      unset_masses(P, b);
       P.w.chunk_done[b] = 0;
       P.w.seq_final[b] = 0;
       __threadfence();
@@ -853,6 +899,7 @@ __device__ void finalize_sequence(const TailParams &P, int b, int fin,
       const int rows = P.dims.K + 1;
       for (int i = 0; i < rows; ++i) P.out_tokens[static_cast<int64_t>(b) * rows + i] = -1;
       P.out_n[b] = -1;
+      unset_masses(P, b);
     }
   } else if (fin == kFinSelect) {
     SeqState st;
@@ -866,6 +913,8 @@ __device__ void finalize_sequence(const TailParams &P, int b, int fin,
     }
     if (st.mode != kModeSkip)
       select_token(P, b, st, P.w.chunk_mass + static_cast<int64_t>(b) * P.dims.nchunk, true);
+    __syncthreads();
+    if (threadIdx.x == 0) unset_masses(P, b);
   }
 }
 
