@@ -79,6 +79,9 @@ def _load():
             lib.sv_oracle_ngram_draft.restype = ctypes.c_int
             lib.sv_oracle_truncate.argtypes = [i64, vp, dbl, i32, dbl, vp, vp, vp, vp]
             lib.sv_oracle_truncate.restype = ctypes.c_int
+            lib.sv_oracle_truncate_ex.argtypes = [i64, vp, dbl, i32, dbl, vp, vp, vp, vp, vp,
+                                                  vp, vp]
+            lib.sv_oracle_truncate_ex.restype = ctypes.c_int
             lib.sv_oracle_verify_truncated.argtypes = [i64, i64, i32, i32, i32, vp, vp, vp,
                                                        vp, vp, dbl, i32, dbl, i32, dbl, dbl,
                                                        dbl, vp, vp, vp, vp, vp]
@@ -266,19 +269,26 @@ def ngram_draft(tokens, lengths, K: int, n_min: int = 2, n_max: int = 5):
     return draft, n
 
 
-def truncate(logits, T: float, top_k: int = 0, top_p: float = 1.0):
+def truncate(logits, T: float, top_k: int = 0, top_p: float = 1.0, cut: bool = False):
     """Warped distribution of one row of logits (reading R11 in
     sv_oracle.c): temperature, top-k (0: off), then top-p (1: off), both
-    cut by value with ties kept.  Returns (p, keep, gap, margin)."""
+    cut by value with ties kept.  Returns (p, keep, gap, margin), and with
+    cut=True also (cut_logit, last_kept, first_dropped): the logit of the
+    last kept token in descending order, that token and the largest dropped
+    one (-inf, -1, -1 when nothing is cut)."""
     x = _c(logits, np.float64)
     p = np.empty_like(x)
     keep = np.empty(x.size, dtype=np.uint8)
-    gap, margin = ctypes.c_double(), ctypes.c_double()
-    rc = _load().sv_oracle_truncate(x.size, _ptr(x), float(T), int(top_k), float(top_p),
-                                    _ptr(p), _ptr(keep), ctypes.byref(gap),
-                                    ctypes.byref(margin))
+    gap, margin, cl = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    a0, a1 = ctypes.c_int64(), ctypes.c_int64()
+    rc = _load().sv_oracle_truncate_ex(x.size, _ptr(x), float(T), int(top_k), float(top_p),
+                                       _ptr(p), _ptr(keep), ctypes.byref(gap),
+                                       ctypes.byref(margin), ctypes.byref(cl), ctypes.byref(a0),
+                                       ctypes.byref(a1))
     if rc != OK:
         raise ValueError(f"sv_oracle_truncate failed ({rc})")
+    if cut:
+        return p, keep.astype(bool), gap.value, margin.value, cl.value, a0.value, a1.value
     return p, keep.astype(bool), gap.value, margin.value
 
 
@@ -288,7 +298,8 @@ def verify_truncated(hidden, W, draft, q_logits, uniforms, temperature: float,
     """The verify step with truncated target and draft distributions (R11);
     arguments as verify().  Adds trunc_sens [B] (the largest warped mass of
     a token next to a cut within tol_gap / tol_mass of flipping) and
-    trunc_xgap [B] (the smallest |logit(x_i) - cut|), see sv_oracle.c."""
+    trunc_xgap [B] (the smallest logit change that moves a draft token
+    across its row's cut), see sv_oracle.c."""
     hidden, dt = _matrix(hidden)
     W, dt2 = _matrix(W)
     if dt != dt2:

@@ -616,7 +616,7 @@ int sv_oracle_ngram_draft(const int32_t *tokens, int64_t ld, const int32_t *leng
  * at the top-p cut (INFINITY when a cut is off).  `order` must hold V
  * int64 (scratch).
  * ---------------------------------------------------------------------- */
-static const double *g_sort_x;
+static _Thread_local const double *g_sort_x; /* the sort key of this thread's qsort */
 static int cmp_desc(const void *a, const void *b) {
   const double xa = g_sort_x[*(const int64_t *)a], xb = g_sort_x[*(const int64_t *)b];
   if (xa > xb) return -1;
@@ -636,7 +636,7 @@ static void truncate_row(int64_t V, const double *x, int32_t top_k, double top_p
     keep[v] = 1;
     order[v] = v;
   }
-  g_sort_x = x; /* the oracle is single-threaded per call */
+  g_sort_x = x;
   qsort(order, (size_t)V, sizeof(int64_t), cmp_desc);
   int64_t n_keep = V; /* kept tokens are order[0..n_keep-1] */
   if (top_k > 0 && (int64_t)top_k < V) {
@@ -693,9 +693,15 @@ static void warped_softmax(int64_t V, const double *x, const unsigned char *keep
 
 /* Truncates one row of logits (R11) and returns its warped distribution;
  * keep_out [V] (may be NULL) marks the kept tokens, *gap (logit units) and
- * *margin are the cut distances described at truncate_row. */
-int sv_oracle_truncate(int64_t V, const double *logits, double T, int32_t top_k, double top_p,
-                       double *p, unsigned char *keep_out, double *gap, double *margin) {
+ * *margin are the cut distances described at truncate_row.  The last three
+ * outputs (may be NULL) describe the final cut: *cut_logit the logit of the
+ * last kept token in descending order (-INFINITY when nothing is cut),
+ * *last_kept that token and *first_dropped the largest dropped one (-1 when
+ * nothing is cut). */
+int sv_oracle_truncate_ex(int64_t V, const double *logits, double T, int32_t top_k,
+                          double top_p, double *p, unsigned char *keep_out, double *gap,
+                          double *margin, double *cut_logit, int64_t *last_kept,
+                          int64_t *first_dropped) {
   if (V < 1 || !logits || !p || !(T > 0.0) || top_k < 0 || !(top_p > 0.0) || top_p > 1.0)
     return SV_ORACLE_EARG;
   double *x = (double *)malloc(sizeof(double) * (size_t)V);
@@ -713,8 +719,17 @@ int sv_oracle_truncate(int64_t V, const double *logits, double T, int32_t top_k,
   if (keep_out) memcpy(keep_out, keep, (size_t)V);
   if (gap) *gap = g * T;
   if (margin) *margin = mg;
+  if (cut_logit) *cut_logit = a0 >= 0 ? cut * T : -INFINITY;
+  if (last_kept) *last_kept = a0;
+  if (first_dropped) *first_dropped = a1;
   free(x); free(keep); free(order);
   return SV_ORACLE_OK;
+}
+
+int sv_oracle_truncate(int64_t V, const double *logits, double T, int32_t top_k, double top_p,
+                       double *p, unsigned char *keep_out, double *gap, double *margin) {
+  return sv_oracle_truncate_ex(V, logits, T, top_k, top_p, p, keep_out, gap, margin, NULL,
+                               NULL, NULL);
 }
 
 /* ------------------------------------------------------------------------
@@ -731,8 +746,13 @@ int sv_oracle_truncate(int64_t V, const double *logits, double T, int32_t top_k,
  *                   cut that lies within those tolerances (0 if none):
  *                   moving that token across the cut moves every threshold
  *                   and CDF edge of the round by about that much;
- *   trunc_xgap [B]  the smallest |logit(x_i) - cut| over the draft tokens
- *                   and their rows' cuts (logit units; INFINITY if none).
+ *   trunc_xgap [B]  the smallest change of a draft token's logit that
+ *                   would move it across its row's cut, over the draft
+ *                   tokens and their target and draft rows (logit units;
+ *                   INFINITY if no row is cut): a kept x_i is that far
+ *                   above the first dropped token, a dropped one that far
+ *                   below the last kept token; 0 when x_i is one of those
+ *                   two and the top-p mass margin is below tol_mass.
  * ---------------------------------------------------------------------- */
 int sv_oracle_verify_truncated(int64_t V, int64_t d, int32_t B, int32_t K, int32_t dtype,
                                const void *hidden, const void *W, const int32_t *draft,
@@ -793,7 +813,9 @@ int sv_oracle_verify_truncated(int64_t V, int64_t d, int32_t B, int32_t K, int32
           if (s > sens) sens = s;
         }
         if (a0 >= 0 && i < K && xb0 && xb0[i] >= 0 && (int64_t)xb0[i] < V) {
-          const double dx = fabs(x[xb0[i]] - cut) * T;
+          const int64_t xi = xb0[i];
+          double dx = keep[xi] ? (x[xi] - x[a1]) * T : (x[a0] - x[xi]) * T;
+          if ((xi == a0 || xi == a1) && mg < tol_mass) dx = 0.0;
           if (dx < xgap) xgap = dx;
         }
       }

@@ -6,15 +6,24 @@ side with its own settings; reading R11) against the CPU oracle.
   of the exact ones) and fp32 exponentials, so a cut whose logit gap or
   top-p mass margin is below 4e-6 may fall either way; the oracle reports
   the largest warped mass of a token next to such a cut (moving it moves
-  every threshold and CDF edge of the round by about that much) and the
-  distance of each draft token's logit from its rows' cuts.  A round is
+  every threshold and CDF edge of the round by about that much) and how far
+  each draft token's logit is from crossing its rows' cuts.  A round is
   flagged when a decision's uniform lies within 1e-6 plus twice that mass
-  of its threshold, or a draft token lies within 4e-6 of a cut;
+  of its threshold, or a draft token lies within 4e-6 of crossing a cut.
+  Every mismatch must be a flagged round;
+* at scale (10^4 rounds per setting at the 8B shape) the flagged rounds
+  are counted by reason and reported;
 * no cut reproduces spec_verify_run bit for bit; top-1 on both sides is
   greedy verification (the pages' greedy corollary);
-* over 2M rounds on the six-token example the emitted law is the warped
+* over 4M rounds on the six-token example the emitted law is the warped
   target ("Speculative Decoding: Two Models, One Voice", three remarks).
+
+SV_PARITY_REPORT=<path> appends one JSON line per at-scale setting.
 """
+import json
+import math
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -22,7 +31,7 @@ import torch
 import oracle
 import spec_inputs as si
 import speculative_decoding_verification_22_gb300 as sv
-from gpu_common import FLAG_SAMPLED
+from gpu_common import _POOL, FLAG_SAMPLED
 
 pytestmark = pytest.mark.gpu
 
@@ -52,12 +61,10 @@ def _oracle(inp, W, T, pk, pp, qk, qp):
 
 
 def _compare(tok, n, ref):
-    """(mismatches outside flagged rounds, flagged rounds); flagged rounds
-    must still match in most cases (a systematic error would not)."""
+    """(mismatches outside flagged rounds, flagged rounds)."""
     fl = ((ref["dist"] <= FLAG_SAMPLED + 2.0 * ref["trunc_sens"])
           | (ref["trunc_xgap"] < GAP_FLAG))
     diff = np.any(tok != ref["tokens"], axis=1) | (n != ref["n_accepted"])
-    assert int((diff & fl).sum()) <= max(1, int(fl.sum()) // 2)
     return int((diff & ~fl).sum()), int(fl.sum())
 
 
@@ -97,6 +104,195 @@ def test_truncated_parity_llama8b(dev, B, K, T):
     eng.close()
 
 
+def _cut_rows(L, T, k, pp):
+    """Per row of logits L [R, V]: (logits, warped p, keep, gap, margin, cut
+    logit, last kept, first dropped)."""
+    return [(L[i],) + oracle.truncate(L[i], T, k, pp, cut=True) for i in range(L.shape[0])]
+
+
+def _row_sens(row, T):
+    """The warped mass of the larger neighbour of a cut that lies within
+    GAP_FLAG / MASS_FLAG of flipping, else 0."""
+    L, pw, _, gap, mg, _, a0, a1 = row
+    if a0 < 0 or not (gap < GAP_FLAG or mg < MASS_FLAG):
+        return 0.0
+    w0 = pw[a0]
+    return max(w0, w0 * math.exp((L[a1] - L[a0]) / T))
+
+
+def _row_xgap(row, x):
+    """How far each draft token in x must move to cross the row's cut."""
+    L, _, keep, _, mg, _, a0, a1 = row
+    if a0 < 0:
+        return np.full(x.shape, np.inf)
+    d = np.where(keep[x], L[x] - L[a1], L[a0] - L[x])
+    if mg < MASS_FLAG:
+        d = np.where((x == a0) | (x == a1), 0.0, d)
+    return d
+
+
+def _draw_from_warped(Qb, T, qk, qp, nvar, seed):
+    """nvar draft-token vectors [nvar, K] drawn from the oracle's warped
+    draft rows of one sequence (inverse CDF of the kept tokens)."""
+    rng = np.random.default_rng(seed)
+    K, V = Qb.shape
+    xs = np.empty((nvar, K), np.int32)
+    for i in range(K):
+        qw = oracle.truncate(Qb[i].astype(np.float64), T, qk, qp)[0]
+        cdf = np.cumsum(qw)
+        r = rng.random(nvar) * cdf[-1]
+        xs[:, i] = np.minimum(np.searchsorted(cdf, r, side="right"), np.flatnonzero(qw)[-1])
+    return xs
+
+
+def _oracle_trunc_sequence(Hb, W_np, Xb, Qb, Ub, T, st, xs, us):
+    """The oracle's own round of one sequence, then its rule on nvar more
+    rounds (drafts xs, uniforms us) with the same warped p and q, with the
+    cut sensitivity and each round's draft-token cut distance."""
+    pk, pp, qk, qp = st
+    own = oracle.verify_truncated(Hb, W_np, Xb, Qb, Ub, T, pk, pp, qk, qp, GAP_FLAG, MASS_FLAG)
+    K = Xb.shape[1]
+    prow = _cut_rows(oracle.logits(Hb[0], W_np), T, pk, pp)
+    qrow = _cut_rows(Qb[0].astype(np.float64), T, qk, qp)
+    sens = max(_row_sens(r, T) for r in prow + qrow)
+    xgap = np.full(len(xs), np.inf)
+    for i in range(K):
+        xgap = np.minimum(xgap, np.minimum(_row_xgap(prow[i], xs[:, i]),
+                                           _row_xgap(qrow[i], xs[:, i])))
+    p = np.stack([r[1] for r in prow])
+    q = np.stack([r[1] for r in qrow])
+    var = oracle.rule_batch(p, q, xs, us.astype(np.float64), split=True)
+    return own, var, sens, xgap
+
+
+class TruncTally:
+    def __init__(self):
+        self.rounds = self.mismatch = self.unflagged = 0
+        self.flag_any = self.flag_accept = self.flag_draw = 0
+        self.flag_sens = self.flag_xgap = 0
+        self.sequences = self.seq_sens = 0
+        self.tests = 0
+        self.worst = 0.0
+
+    def add(self, gt, gn, rt, rn, dacc, ddraw, sens, xgap, K):
+        band = FLAG_SAMPLED + 2.0 * sens
+        fa, fd, fx = dacc <= band, ddraw <= band, xgap < GAP_FLAG
+        fl = fa | fd | fx
+        mism = np.any(gt != rt, axis=1) | (gn != rn)
+        self.rounds += len(rn)
+        self.mismatch += int(mism.sum())
+        self.unflagged += int((mism & ~fl).sum())
+        self.flag_any += int(fl.sum())
+        self.flag_accept += int(fa.sum())
+        self.flag_draw += int(fd.sum())
+        self.flag_xgap += int(fx.sum())
+        self.flag_sens += len(rn) if sens > 0 else 0
+        self.sequences += 1
+        self.seq_sens += int(sens > 0)
+        self.tests += int(np.where(rn < K, rn + 1, rn).sum())
+        if mism.any():
+            self.worst = max(self.worst, float(np.minimum(dacc, ddraw)[mism].max()))
+
+    def record(self, **extra):
+        r = max(self.rounds, 1)
+        rec = {"rounds": self.rounds, "mismatched_rounds": self.mismatch,
+               "unflagged_mismatches": self.unflagged,
+               "flagged_rounds": self.flag_any, "flagged_rate": self.flag_any / r,
+               "flagged_accept": self.flag_accept, "flagged_draw": self.flag_draw,
+               "flagged_draft_near_cut": self.flag_xgap,
+               "rounds_with_cut_sensitivity": self.flag_sens,
+               "sequences": self.sequences, "sequences_with_cut_sensitivity": self.seq_sens,
+               "accept_flag_rate_bound": 2e-6 * self.tests / r,
+               "largest_dist_of_a_mismatch": self.worst}
+        rec.update(extra)
+        line = json.dumps(rec, sort_keys=True)
+        print(line)
+        path = os.environ.get("SV_PARITY_REPORT")
+        if path:
+            with open(path, "a") as f:
+                f.write(line + "\n")
+        return rec
+
+
+def _pad4(n):
+    return (n + 3) // 4 * 4
+
+
+# (workload, overrides, T, (p_top_k, p_top_p, q_top_k, q_top_p), sets,
+#  rounds per set, bound on the fraction of sequences whose cuts are within
+#  4e-6 of moving).  Such a sequence flags all of its rounds with a wider
+#  band; after top-k 50 the token at a top-p cut has mass ~0.01-0.02, so
+#  its mass margin is within 4e-6 for ~5e-4 of the rows (nine rows a
+#  sequence).  A top-p cut inside the bulk of a 128k vocabulary (no top-k
+#  first) sits between tokens of mass ~1e-5 and is within 4e-6 in most
+#  sequences: reported, not bounded.
+AT_SCALE = [("llama8b", {}, 1.0, (50, 0.9, 50, 0.9), 40, 500, 0.1),
+            ("llama8b", {}, 1.0, (0, 0.95, 1000, 1.0), 20, 500, None),
+            ("llama8b_b8k7", {}, 0.7, (50, 0.9, 50, 0.9), 5, 250, 0.1)]
+
+
+@pytest.mark.parametrize("name,over,T,st,nsets,nvar,cut_bound", AT_SCALE)
+def test_truncated_parity_at_scale(dev, name, over, T, st, nsets, nvar, cut_bound):
+    """Every round's tokens and accept count equal the oracle's unless the
+    round is flagged; flags counted by reason."""
+    wl = si.workload(name, **over)
+    W = si.make_weights(wl, seed=301, device=dev)
+    W_np = si.to_oracle(W)
+    B, K, V = wl.B, wl.K, wl.V
+    pk, pp, qk, qp = st
+    eng = sv.SpecVerify(V, wl.d, B, K, wl.dtype, device=dev)
+    rt, rn = _pad4(B * (K + 1)), _pad4(B)
+    ot = torch.empty((nvar, rt), dtype=torch.int32, device=dev)
+    on = torch.empty((nvar, rn), dtype=torch.int32, device=dev)
+    u_pad = torch.zeros((nvar, rt), dtype=torch.float32, device=dev)
+    x_pad = torch.zeros((nvar, _pad4(B * K)), dtype=torch.int32, device=dev)
+    tally = TruncTally()
+    for s in range(nsets):
+        inp = si.make_round(wl, W, seed=400 + s, T=T)
+        tok, n = eng.run_truncated(inp["hidden"], W, inp["draft"], inp["q_logits"],
+                                   inp["uniforms"], T, pk, pp, qk, qp)
+        assert eng.status() == sv.SV_OK
+        own_g = (tok.cpu().numpy(), n.cpu().numpy())
+        H = si.to_oracle(inp["hidden"])
+        X = si.to_oracle(inp["draft"])
+        Q = si.to_oracle(inp["q_logits"])
+        U = si.to_oracle(inp["uniforms"])
+        xs = np.stack(list(_POOL.map(
+            lambda b: _draw_from_warped(Q[b], T, qk, qp, nvar, 500_000 + 64 * s + b),
+            range(B))), axis=1)                                   # [nvar, B, K]
+        us = si.draw_uniforms(nvar, B, K, seed=600_000 + s, device=dev)
+        u_pad[:, :B * (K + 1)] = us.reshape(nvar, -1)
+        x_pad[:, :B * K] = torch.from_numpy(xs.reshape(nvar, -1)).to(dev)
+        for v in range(nvar):
+            sv.spec_verify_run_truncated(eng.h, inp["hidden"], W, x_pad[v], inp["q_logits"],
+                                         u_pad[v], T, pk, pp, qk, qp, ot[v], on[v])
+        assert eng.status() == sv.SV_OK
+        vt = ot[:, :B * (K + 1)].reshape(nvar, B, K + 1).cpu().numpy()
+        vn = on[:, :B].cpu().numpy()
+        usn = us.cpu().numpy()
+        res = list(_POOL.map(
+            lambda b: _oracle_trunc_sequence(H[b:b + 1], W_np, X[b:b + 1], Q[b:b + 1],
+                                             U[b:b + 1], T, st, xs[:, b], usn[:, b]),
+            range(B)))
+        for b, (own, var, sens, xgap) in enumerate(res):
+            # the own round: the oracle's end-to-end flags
+            fl_own = ((own["dist"] <= FLAG_SAMPLED + 2.0 * own["trunc_sens"])
+                      | (own["trunc_xgap"] < GAP_FLAG))
+            mism = (np.any(own_g[0][b] != own["tokens"][0])
+                    or own_g[1][b] != own["n_accepted"][0])
+            assert not (mism and not fl_own[0]), ("own round", s, b)
+            tk, na, _, dacc, ddraw = var
+            tally.add(vt[:, b], vn[:, b], tk, na, dacc, ddraw, sens, xgap, K)
+    eng.close()
+    rec = tally.record(config=f"{name} truncated top_k/top_p {st}", T=T, nsets=nsets,
+                       nvar=nvar)
+    assert rec["unflagged_mismatches"] == 0, rec
+    if cut_bound is not None:
+        assert rec["sequences_with_cut_sensitivity"] <= cut_bound * rec["sequences"], rec
+    # a draft token within 4e-6 of crossing a cut of its rows
+    assert rec["flagged_draft_near_cut"] <= 0.01 * rec["rounds"], rec
+
+
 def test_no_cut_is_the_plain_run_and_top_one_is_greedy(dev):
     wl = si.workload("tiny", B=32, K=4)
     T = 1.0
@@ -120,7 +316,7 @@ def test_no_cut_is_the_plain_run_and_top_one_is_greedy(dev):
     eng.close()
 
 
-def test_truncated_emitted_law_over_two_million_rounds(dev, golden):
+def test_truncated_emitted_law_over_four_million_rounds(dev, golden):
     g = golden("six_token_example.json")
     P, Q = np.array(g["p"]), np.array(g["q"])
     V, d, B, K = len(P), 4, 1000, 1
@@ -138,7 +334,7 @@ def test_truncated_emitted_law_over_two_million_rounds(dev, golden):
     gen = torch.Generator(device=dev)
     gen.manual_seed(3)
     counts = torch.zeros(V, dtype=torch.int64, device=dev)
-    launches = 2000
+    launches = 4000
     for _ in range(launches):
         r = torch.rand((B, K), generator=gen, device=dev, dtype=torch.float64)
         x = torch.searchsorted(cdf, r, right=True).clamp_max(V - 1).to(torch.int32).contiguous()
@@ -153,6 +349,6 @@ def test_truncated_emitted_law_over_two_million_rounds(dev, golden):
     total = c.sum()
     assert np.all(c[p_w == 0] == 0)
     emp = c / total
-    assert 0.5 * np.abs(emp - p_w).sum() < 1.5e-3
+    assert 0.5 * np.abs(emp - p_w).sum() < 1e-3
     keep = p_w > 0
     assert stats.chisquare(c[keep], total * p_w[keep]).pvalue > 1e-4

@@ -32,6 +32,24 @@ def test_kept_sets_by_hand(golden):
             assert abs(gap - c["gap"]) < 1e-12
 
 
+def test_cut_description_by_hand(golden):
+    """The final cut's description: the kept token with the smallest logit
+    (the last in descending order, ties by index), the dropped token with
+    the largest, and the former's logit."""
+    g = golden("truncation_examples.json")
+    for c in g["cases"]:
+        L = np.array(c["logits"])
+        _, keep, _, _, cut, a0, a1 = oracle.truncate(L, c["T"], c["top_k"], c["top_p"], cut=True)
+        if keep.all():
+            assert (cut, a0, a1) == (-np.inf, -1, -1), c["name"]
+            continue
+        kept, dropped = np.flatnonzero(keep), np.flatnonzero(~keep)
+        lo = kept[L[kept] == L[kept].min()].max()
+        hi = dropped[L[dropped] == L[dropped].max()].min()
+        assert (a0, a1) == (lo, hi), c["name"]
+        assert abs(cut - L[lo]) <= 1e-12 * max(1.0, abs(L[lo]))
+
+
 def test_no_cut_is_the_plain_rule():
     rng = np.random.default_rng(2)
     V, K, B = 40, 3, 30
@@ -88,3 +106,36 @@ def test_emitted_law_is_the_warped_target():
         law += q_w[xv] * np.bincount(got["tokens"][:, 0], minlength=6) / n
     assert np.abs(law - p_w).max() < 6e-3
     assert np.all(law[p_w == 0] == 0)
+
+
+def test_draft_token_cut_distance_by_hand():
+    """trunc_xgap: how far a draft token's logit must move to cross its
+    row's cut.  Target row 0 keeps {0,1,2} (top-3; first dropped 3 at 2.5),
+    the draft row keeps {3,4,5} (last kept 3 at logit 3.0)."""
+    lp = np.array([[5.0, 4.0, 3.0, 2.5, 1.0, 0.0], [0.0, 0.5, 1.0, 1.5, 2.0, 2.5]])
+    lq = np.array([[[0.0, 1.0, 2.0, 3.0, 4.0, 5.0]]], dtype=np.float32)
+    H, W = _embed(lp)
+    u = np.full((1, 2), 0.5, np.float32)
+    # token: (target side, draft side) -> the smaller
+    want = {2: min(3.0 - 2.5, 3.0 - 2.0),   # kept / dropped
+            0: min(5.0 - 2.5, 3.0 - 0.0),   # kept / dropped
+            3: min(3.0 - 2.5, 3.0 - 2.0),   # dropped / kept
+            5: min(3.0 - 0.0, 5.0 - 2.0)}   # dropped / kept
+    for xv, d in want.items():  # fp32-exact logits
+        got = oracle.verify_truncated(H, W, np.array([[xv]], np.int32), lq, u, 1.0, 3, 1.0, 3,
+                                      1.0, 4e-6, 4e-6)
+        assert abs(got["trunc_xgap"][0] - d) < 1e-12, (xv, got["trunc_xgap"][0], d)
+        assert got["trunc_sens"][0] == 0.0
+    # a top-p cut that lands on a cumulative mass of exactly top_p (up to
+    # rounding): the last kept and first dropped tokens are at distance 0,
+    # and their masses are reported as sensitivity (logits rounded to fp32)
+    P = np.array([0.5, 0.3, 0.2])
+    lp2 = np.log(np.stack([P, P]))
+    H2, W2 = _embed(lp2)
+    lq2 = np.zeros((1, 1, 3), np.float32)
+    u2 = np.full((1, 2), 0.5, np.float32)
+    for xv, d in ((1, 0.0), (2, 0.0), (0, np.log(0.5 / 0.2))):
+        got = oracle.verify_truncated(H2, W2, np.array([[xv]], np.int32), lq2, u2, 1.0, 0, 0.8,
+                                      0, 1.0, 4e-6, 4e-6)
+        assert abs(got["trunc_xgap"][0] - d) < 1e-6, (xv, got["trunc_xgap"][0], d)
+        assert abs(got["trunc_sens"][0] - 0.375) < 1e-7  # 0.3 / (0.5 + 0.3), kept
