@@ -775,7 +775,9 @@ def main():
         if ngram:
             dbuf.update(draft=torch.empty_like(sets[0]["draft"]),
                         dlen=torch.empty_like(sets[0]["dlen"]))
-        dtok, dn = out_tok[0], out_n[0]
+        # outputs of their own: the timed rounds' outputs stay for the
+        # parity sample
+        dtok, dn = torch.empty_like(out_tok[0]), torch.empty_like(out_n[0])
 
     def e2e_step(p):
         if fp8:

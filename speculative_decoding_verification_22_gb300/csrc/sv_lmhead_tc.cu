@@ -30,6 +30,10 @@
 //    fp32 logits with a TMA store, and computes the per-32-entry (max,
 //    sum-exp) partials of logits / T (or the max for T == 0); four more
 //    warps stream the draft logits q / T of the tile for the same partials.
+//    They run on the two warp schedulers that host neither the TMA
+//    producer nor the MMA issuer (warps 6, 7, 10, 11; warps 8 and 9 have
+//    no role): sharing a scheduler with those two latency-critical loops
+//    cost up to 11 us per launch at 64 columns.
 #include <atomic>
 
 #include "sv_internal.cuh"
@@ -68,7 +72,16 @@ constexpr int kWSlabBytes = kTileM * 128;          // 16 KB: 128 rows x 128 byte
 constexpr int kMaxStages = SV_TC_MAX_STAGES;
 constexpr int kNumEpiWarps = 4;
 constexpr int kNumQWarps = 4;
-constexpr int kThreads = 64 + 32 * (kNumEpiWarps + kNumQWarps);  // 320
+// warp w runs on scheduler w % 4; the draft-logit warps take schedulers 2
+// and 3 only (see the top of the file), so the block has two idle warps
+constexpr int kThreads = 64 + 32 * (kNumEpiWarps + kNumQWarps + 2);  // 384
+__device__ __forceinline__ bool is_q_warp(int warp) {
+  return warp >= 2 + kNumEpiWarps && (warp & 3) >= 2;
+}
+// 0 .. kNumQWarps - 1 for warps 6, 7, 10, 11
+__device__ __forceinline__ int q_warp_index(int warp) {
+  return ((warp - 2 - kNumEpiWarps) >> 2) * 2 + (warp & 1);
+}
 constexpr int kMaxDrainSlots = 32;
 // TMEM slots of the drain ring for a column capacity NCOL (<= 512 columns)
 // (direct mode: the two tile buffers)
@@ -632,10 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(smem_u32(&ctl->teardown), 0u, kCleanupLimitNs, &never);
     }
     __syncwarp();
-  } else if (warp >= 2 + kNumEpiWarps) {
+  } else if (is_q_warp(warp)) {
     // ---------------- draft-logit partials (independent of the GEMM) -------
     if (!P.greedy && P.dims.RQ > 0) {
-      const int quad = (warp - 2 - kNumEpiWarps) & 3;
+      const int quad = q_warp_index(warp);
       // the exact logit of every draft token (one warp each, spread over
       // the grid) and the draft logit at that token; the decision pass reads
       // them instead of recomputing.  First, so that these dependent loads
@@ -668,27 +681,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (P.w.draft_q) P.w.draft_q[idx] = qx;
         }
       }
-      // row statistics: this warp's draft rows (quad, quad + 4, ...) start
+      // row statistics: this warp's draft rows (quad, quad + kNumQWarps, ...) start
       // empty in shared memory (row_stats runs in drain mode only, where
       // RQ < kQaccRows and no CTA pair splits the columns)
       const bool qstats = P.row_stats && P.q_logits != nullptr;
       float4 *qacc = qstats ? ctl->qacc : nullptr;
       if (qstats && lane == 0)
-        for (int r = quad; r < P.dims.RQ; r += 4) qacc[r] = make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
+        for (int r = quad; r < P.dims.RQ; r += kNumQWarps)
+          qacc[r] = make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
       __syncwarp();
       // no draft distribution (point-mass drafts): nothing to normalise
       for (int t = t_first; t <= t_last && P.q_logits != nullptr; ++t) {
         int kb0, kb1;
         tile_range(t, u0, u1, ngr, C, kb0, kb1);
         if (kb0 != 0) continue;  // the CTA holding a tile's first k block does it
-        q_partials(P, t, quad + 4 * hsel, P.half ? 8 : 4, lane, qacc);
+        q_partials(P, t, quad + kNumQWarps * hsel, P.half ? 2 * kNumQWarps : kNumQWarps, lane,
+                   qacc);
       }
       __syncwarp();
       if (qstats)
-        for (int r = quad + 4 * lane; r < P.dims.RQ; r += 128)
+        for (int r = quad + kNumQWarps * lane; r < P.dims.RQ; r += 32 * kNumQWarps)
           P.w.rowpart[static_cast<int64_t>(P.dims.R + r) * gridDim.x + blockIdx.x] = qacc[r];
     }
-  } else {
+  } else if (warp < 2 + kNumEpiWarps) {
     // ---------------- epilogue warps ----------------
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row_in_tile = quad * 32 + lane;
