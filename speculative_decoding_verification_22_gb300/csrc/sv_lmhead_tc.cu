@@ -99,9 +99,22 @@ constexpr int drain_slots() {
 #ifndef SV_TC_KPS
 #define SV_TC_KPS 4
 #endif
+#ifndef SV_TC_KPS16
+#define SV_TC_KPS16 1
+#endif
 template <int NCOL>
 constexpr int kblocks_per_slot() {
-  return NCOL >= 32 ? SV_TC_KPS : 1;
+  return NCOL >= 32 ? SV_TC_KPS : SV_TC_KPS16;
+}
+#ifndef SV_TC_TEMPTY_BATCH
+#define SV_TC_TEMPTY_BATCH 4
+#endif
+// Drain slots the MMA issuer takes per wait on the epilogue (long rings
+// only): the epilogue frees slots in order, so once the last of a batch is
+// free the whole batch is.
+template <int NCOL>
+constexpr int tempty_batch() {
+  return drain_slots<NCOL>() >= 16 ? SV_TC_TEMPTY_BATCH : 1;
 }
 constexpr uint64_t kCleanupLimitNs = 2000000000ull;
 // Epilogue staging: one 2 KB box ([16 columns][32 entries] fp32) per
@@ -560,9 +573,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool group_first = gpos == 0;
         const bool group_last = gpos == kblocks_per_slot<NCOL>() - 1 || kb == kb1 - 1;
         if constexpr (NCOL != 0) {
-          if (group_first &&
-              !__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->tempty[slot]), tphase ^ 1u,
-                                                 P.wait_limit_ns, abort))) {
+          if (group_first && slot % tempty_batch<NCOL>() == 0 &&
+              !__all_sync(0xffffffffu,
+                          mbar_wait(smem_u32(&ctl->tempty[slot + tempty_batch<NCOL>() - 1]),
+                                    tphase ^ 1u, P.wait_limit_ns, abort))) {
             if (lane == 0) raise_abort(ctl, P);
             ok = false;
             break;
