@@ -57,6 +57,7 @@ KERNEL_SRCS = [os.path.join(ROOT, "speculative_decoding_verification_22_gb300", 
                for f in ("sv_lmhead_tc.cu", "sv_internal.cuh", "sv_kernels.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lmhead_tc_llama8b.md")
 TRAFFIC_FILE_FP8 = os.path.join(ROOT, "profiles", "lmhead_tc_llama8b_fp8.md")
+TRAFFIC_FILE_B8K7 = os.path.join(ROOT, "profiles", "lmhead_tc_llama8b_b8k7.md")
 
 
 # ---------------------------------------------------------------------------
@@ -744,8 +745,12 @@ def main():
     if fp8:
         step_bytes += 4 * wl.V + 4 * wl.B * (wl.K + 1)
     # ncu captures exist for the default workload and its FP8 variant only
-    plain = args.workload == "llama8b" and not (ngram or truncated or args.tree)
-    traffic_file = (TRAFFIC_FILE_FP8 if fp8 else TRAFFIC_FILE) if plain else None
+    plain = not (ngram or truncated or args.tree)
+    traffic_file = None
+    if plain and args.workload == "llama8b":
+        traffic_file = TRAFFIC_FILE_FP8 if fp8 else TRAFFIC_FILE
+    elif plain and args.workload == "llama8b_b8k7" and not fp8:
+        traffic_file = TRAFFIC_FILE_B8K7
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "traffic": recorded_traffic(traffic_file),
