@@ -41,6 +41,16 @@ constexpr int kFastK = 256;                  // largest top_k of the fast path
 constexpr int kMaxSub = 4096;                // subtile maxima staged (V <= 131072)
 constexpr int kCandCap = 2048;               // gathered candidate entries
 constexpr int kFastKept = kTruncThreads;     // kept entries ranked for top-p
+// Fixed-point unit of the general path's bin masses: a weight exp(x/T - M)
+// <= 1 is added as round(w * 2^e), e = min(44, 62 - ceil(log2 V)), so a
+// row's total stays below 2^63 and each weight carries an absolute error
+// of at most 2^-(e+1) (2^-45 up to V = 2^18).
+__device__ __forceinline__ float mass_unit(int64_t V) {
+  int bits = 0;
+  while ((int64_t(1) << bits) < V) ++bits;
+  const int e = 62 - bits < 44 ? 62 - bits : 44;
+  return __int_as_float((127 + e) << 23);  // 2^e, exactly
+}
 
 __device__ __forceinline__ uint32_t float_key(float f) {
   const uint32_t u = __float_as_uint(f);
@@ -110,7 +120,10 @@ struct TruncSmem {
   ff warp_ff[kTailWarps];
   int owner, bin, n, overflow;
   union {
-    float mass[kBins];  // general path
+    struct {  // general path: bin masses in fixed point, then as floats
+      unsigned long long mass_fx[kBins];
+      float mass[kBins];
+    } g;
     struct {
       float sub_max[kMaxSub];  // subtile maxima
       float cand[kCandCap];    // candidate entries
@@ -443,9 +456,10 @@ __global__ void __maxnreg__(72) trunc_kernel(const TruncParams P) {
       for (int p = 0; p < 3; ++p) {
         const int shift = digit_shift(p);
         const uint32_t dm = digit_mask(p);
+        const float unit = mass_unit(V);
         for (int i = threadIdx.x; i < kBins; i += kTruncThreads) {
           sm.cnt[i] = 0;
-          sm.u.mass[i] = 0.0f;
+          sm.u.g.mass_fx[i] = 0ull;
         }
         __syncthreads();
         float mine = 0.0f;
@@ -454,15 +468,20 @@ __global__ void __maxnreg__(72) trunc_kernel(const TruncParams P) {
           if (key >= floor && (key & pmask) == prefix) {
             const float w = expf(fmaf(v, inv_t, -M));
             const uint32_t dg = (key >> shift) & dm;
-            atomicAdd(&sm.u.mass[dg], w);
+            // integer adds commute: the bin masses, and so the cut, do not
+            // depend on the order the threads add in
+            atomicAdd(&sm.u.g.mass_fx[dg], __float2ull_rn(w * unit));
             atomicAdd(&sm.cnt[dg], 1);
             mine = __fadd_rn(mine, w);
           }
         });
         if (p == 0) r = ff_to_f(ff_mul_f(block_sum_ff(ff_make(mine), sm.warp_ff), top_p));
         __syncthreads();
+        for (int i = threadIdx.x; i < kBins; i += kTruncThreads)
+          sm.u.g.mass[i] = __ull2float_rn(sm.u.g.mass_fx[i]) / unit;
+        __syncthreads();
         float above = 0.0f;
-        find_cut_bin<float>(sm, sm.u.mass, static_cast<int>(dm) + 1, r, sm.incl_f, sm.warp_f,
+        find_cut_bin<float>(sm, sm.u.g.mass, static_cast<int>(dm) + 1, r, sm.incl_f, sm.warp_f,
                             above);
         r -= above;
         prefix |= static_cast<uint32_t>(sm.bin) << shift;

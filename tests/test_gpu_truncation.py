@@ -293,6 +293,30 @@ def test_truncated_parity_at_scale(dev, name, over, T, st, nsets, nvar, cut_boun
     assert rec["flagged_draft_near_cut"] <= 0.01 * rec["rounds"], rec
 
 
+def test_truncated_runs_repeat_bitwise(dev):
+    """The cuts come from integer histogram counts and masses and from
+    fixed-order sums, so repeated runs on the same inputs give the same
+    tokens and normalisers bit for bit.  A top-p cut inside the bulk of the
+    vocabulary and a draft top-k above the fast path's limit take the
+    general (radix-select) path on every row."""
+    wl = si.workload("llama8b", B=8, K=7, T=0.7)
+    W = si.make_weights(wl, seed=501, device=dev)
+    inp = si.make_round(wl, W, seed=502, T=wl.T)
+    eng = sv.SpecVerify(wl.V, wl.d, wl.B, wl.K, wl.dtype, device=dev)
+    first = None
+    for it in range(20):
+        tok, n = eng.run_truncated(inp["hidden"], W, inp["draft"], inp["q_logits"],
+                                   inp["uniforms"], wl.T, 0, 0.95, 1000, 0.9)
+        cur = (tok.cpu().numpy(), n.cpu().numpy(), eng.lse().cpu().numpy())
+        assert eng.status() == sv.SV_OK
+        if first is None:
+            first = cur
+        else:
+            for a, b in zip(first, cur):
+                assert np.array_equal(a, b), it
+    eng.close()
+
+
 def test_no_cut_is_the_plain_run_and_top_one_is_greedy(dev):
     wl = si.workload("tiny", B=32, K=4)
     T = 1.0
