@@ -918,9 +918,8 @@ __device__ void finalize_sequence(const TailParams &P, int b, int fin,
   }
 }
 
-// two CTAs per SM (64 registers): one fits beside a contraction CTA, so
-// programmatic dependent launch stages it early, and twice as many run at
-// once when a round has many rows
+// two CTAs per SM (64 registers), so twice as many run at once when a
+// round has many rows
 __global__ void __launch_bounds__(kTailThreads, 2) tail_kernel(const TailParams P) {
   pdl_wait();
   pdl_launch_dependents();

@@ -108,9 +108,8 @@ __device__ __forceinline__ T block_suffix_incl(T x, T *s_warp) {
   return x + later;
 }
 
-// Shared memory of one CTA (about 40 KB: a CTA fits beside a contraction
-// CTA on one SM).  The general path's mass histogram and the fast path's
-// buffers are never live together.
+// Shared memory of one CTA (about 40 KB).  The general path's mass
+// histogram and the fast path's buffers are never live together.
 struct TruncSmem {
   int cnt[kBins];
   int incl_i[kTruncThreads];
@@ -220,8 +219,7 @@ __device__ uint32_t kth_largest_smem(TruncSmem &sm, const float *vals, int n, in
   return prefix;
 }
 
-// 72 registers: a 512-thread CTA then fits beside a contraction CTA on one
-// SM, so programmatic dependent launch can stage it early.
+// At most 72 registers per thread (36,864 for a 512-thread CTA).
 __global__ void __maxnreg__(72) trunc_kernel(const TruncParams P) {
   pdl_wait();
   pdl_launch_dependents();
