@@ -124,6 +124,9 @@ int spec_verify_create(const sv_config_t *cfg, spec_verify_t **out);
  *   out_n_accepted device, int32 [B]: accepted draft tokens (the round
  *                  emitted n + 1 tokens); -1 for a sequence with an invalid
  *                  draft token or non-finite logits
+ * The outputs depend on the inputs only: repeated calls on the same inputs
+ * give the same tokens bit for bit (every sum has a fixed order; a tile
+ * split between two CTAs is always finished by the same one).
  * Errors (returned): SV_ERR_ARG (null handle/pointer, T < 0 or not finite),
  * SV_ERR_ALIGN, SV_ERR_CUDA (launch failed).
  * Errors (device status word): SV_ERR_TOKEN, SV_ERR_NONFINITE,
@@ -296,7 +299,9 @@ int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidden, const vo
  * (top_k = 0 or >= V: no cut), top-p every token whose logit is at least
  * that of the first token, in descending order, at which the cumulative
  * probability reaches top_p (top_p = 1: no cut).  Membership is decided on
- * the fp32 logits the step computes.  At T == 0 (greedy) the cuts change
+ * the fp32 logits the step computes; the cumulative masses that place a
+ * top-p cut are summed in fixed point, so repeated calls give the same
+ * outputs bit for bit, as for spec_verify_run.  At T == 0 (greedy) the cuts change
  * nothing; with q_logits == NULL the draft settings are unused.  One more
  * launch (the cut of every truncated row) runs between the contraction and
  * the decision kernel.
