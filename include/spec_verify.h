@@ -300,7 +300,8 @@ int spec_verify_run_noalloc(const sv_config_t *cfg, const void *hidden, const vo
  * that of the first token, in descending order, at which the cumulative
  * probability reaches top_p (top_p = 1: no cut).  Membership is decided on
  * the fp32 logits the step computes; the cumulative masses that place a
- * top-p cut are summed in fixed point, so repeated calls give the same
+ * top-p cut are summed in a fixed order (per-bin masses in fixed point
+ * where a whole row is histogrammed), so repeated calls give the same
  * outputs bit for bit, as for spec_verify_run.  At T == 0 (greedy) the cuts change
  * nothing; with q_logits == NULL the draft settings are unused.  One more
  * launch (the cut of every truncated row) runs between the contraction and
