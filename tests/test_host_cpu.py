@@ -237,3 +237,20 @@ def test_contraction_plan_rejects_what_create_rejects(lib):
     cfg = sv.sv_config_t(128256, 4096, 1, 4, sv.SV_BF16, None)
     assert lib.spec_verify_plan(ctypes.byref(cfg), 152, 48 * 1024, ctypes.byref(out)) == \
         sv.SV_ERR_SHAPE
+
+
+@pytest.mark.parametrize("path,shape,elt", [
+    (bench.TRAFFIC_FILE, (128256, 4096, 1, 4), 2),
+    (bench.TRAFFIC_FILE_B8K7, (128256, 4096, 8, 7), 2),
+    (bench.TRAFFIC_FILE_FP8, (128256, 4096, 1, 4), 1),
+])
+def test_recorded_dram_traffic_is_one_pass_over_the_inputs(path, shape, elt):
+    """A committed ncu figure that bench.py reports as `traffic` (only while
+    its source hash matches the contraction's sources) reads the kernel's
+    algorithmic bytes once: DRAM traffic within 1% above them (the rest is
+    the logits and partials written back)."""
+    traffic = bench.recorded_traffic(path)
+    if traffic is None:
+        pytest.skip("the contraction changed since this capture")
+    algo = bench.contraction_bytes(*shape, elt=elt)
+    assert algo <= traffic <= 1.01 * algo, (traffic, algo)
