@@ -247,6 +247,22 @@ def test_truncated_parity_at_scale(dev, name, over, T, st, nsets, nvar, cut_boun
     u_pad = torch.zeros((nvar, rt), dtype=torch.float32, device=dev)
     x_pad = torch.zeros((nvar, _pad4(B * K)), dtype=torch.int32, device=dev)
     tally = TruncTally()
+
+    def collect(s, own_g, vt, vn, futs):
+        for b, f in enumerate(futs):
+            own, var, sens, xgap = f.result()
+            # the own round: the oracle's end-to-end flags
+            fl_own = ((own["dist"] <= FLAG_SAMPLED + 2.0 * own["trunc_sens"])
+                      | (own["trunc_xgap"] < GAP_FLAG))
+            mism = (np.any(own_g[0][b] != own["tokens"][0])
+                    or own_g[1][b] != own["n_accepted"][0])
+            assert not (mism and not fl_own[0]), ("own round", s, b)
+            tk, na, _, dacc, ddraw = var
+            tally.add(vt[:, b], vn[:, b], tk, na, dacc, ddraw, sens, xgap, K)
+
+    # the oracle's sequences of every set run on the host threads while the
+    # GPU takes the next sets; finished sets are folded as they come
+    pending = []
     for s in range(nsets):
         inp = si.make_round(wl, W, seed=400 + s, T=T)
         tok, n = eng.run_truncated(inp["hidden"], W, inp["draft"], inp["q_logits"],
@@ -257,9 +273,10 @@ def test_truncated_parity_at_scale(dev, name, over, T, st, nsets, nvar, cut_boun
         X = si.to_oracle(inp["draft"])
         Q = si.to_oracle(inp["q_logits"])
         U = si.to_oracle(inp["uniforms"])
-        xs = np.stack(list(_POOL.map(
-            lambda b: _draw_from_warped(Q[b], T, qk, qp, nvar, 500_000 + 64 * s + b),
-            range(B))), axis=1)                                   # [nvar, B, K]
+        xs = np.stack([f.result() for f in
+                       [_POOL.submit(_draw_from_warped, Q[b], T, qk, qp, nvar,
+                                     500_000 + 64 * s + b) for b in range(B)]],
+                      axis=1)                                     # [nvar, B, K]
         us = si.draw_uniforms(nvar, B, K, seed=600_000 + s, device=dev)
         u_pad[:, :B * (K + 1)] = us.reshape(nvar, -1)
         x_pad[:, :B * K] = torch.from_numpy(xs.reshape(nvar, -1)).to(dev)
@@ -267,22 +284,18 @@ def test_truncated_parity_at_scale(dev, name, over, T, st, nsets, nvar, cut_boun
             sv.spec_verify_run_truncated(eng.h, inp["hidden"], W, x_pad[v], inp["q_logits"],
                                          u_pad[v], T, pk, pp, qk, qp, ot[v], on[v])
         assert eng.status() == sv.SV_OK
-        vt = ot[:, :B * (K + 1)].reshape(nvar, B, K + 1).cpu().numpy()
-        vn = on[:, :B].cpu().numpy()
+        # copies: the buffers are refilled by the next set while these wait
+        vt = ot[:, :B * (K + 1)].reshape(nvar, B, K + 1).cpu().numpy().copy()
+        vn = on[:, :B].cpu().numpy().copy()
         usn = us.cpu().numpy()
-        res = list(_POOL.map(
-            lambda b: _oracle_trunc_sequence(H[b:b + 1], W_np, X[b:b + 1], Q[b:b + 1],
-                                             U[b:b + 1], T, st, xs[:, b], usn[:, b]),
-            range(B)))
-        for b, (own, var, sens, xgap) in enumerate(res):
-            # the own round: the oracle's end-to-end flags
-            fl_own = ((own["dist"] <= FLAG_SAMPLED + 2.0 * own["trunc_sens"])
-                      | (own["trunc_xgap"] < GAP_FLAG))
-            mism = (np.any(own_g[0][b] != own["tokens"][0])
-                    or own_g[1][b] != own["n_accepted"][0])
-            assert not (mism and not fl_own[0]), ("own round", s, b)
-            tk, na, _, dacc, ddraw = var
-            tally.add(vt[:, b], vn[:, b], tk, na, dacc, ddraw, sens, xgap, K)
+        futs = [_POOL.submit(_oracle_trunc_sequence, H[b:b + 1], W_np, X[b:b + 1], Q[b:b + 1],
+                             U[b:b + 1], T, st, xs[:, b].copy(), usn[:, b].copy())
+                for b in range(B)]
+        pending.append((s, own_g, vt, vn, futs))
+        while pending and all(f.done() for f in pending[0][4]):
+            collect(*pending.pop(0))
+    for item in pending:
+        collect(*item)
     eng.close()
     rec = tally.record(config=f"{name} truncated top_k/top_p {st}", T=T, nsets=nsets,
                        nvar=nvar)
